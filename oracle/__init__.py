@@ -1,0 +1,191 @@
+"""fp64 CPU oracle of the R-KV decode-time KV-cache compression step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product library (``decode_kv_cache_02_gb300``) never imports,
+loads or calls it, and the two share no code.
+
+The arithmetic lives in ``rkv_oracle.c`` (plain fp64 loops, a pthread pool over
+independent problems); this module only marshals numpy arrays through ctypes.
+Every function follows the R-KV review page (yoonschallenge.tistory.com/1236):
+the opening notes and the summary-table rows "Decoding-time compression
+scheme", "importance", "redundancy" and "final selection criterion", and
+question 2, cause 3 (the steps of one compression round).  The readings of the
+points those passages leave open are listed at the top of ``rkv_oracle.c``.
+
+Parity status: every function here is pinned by ``tests/test_oracle.py``
+(closed forms, brute force over subsets, library routines, invariants).  What
+no pin can decide is whether readings R1-R9 are what the R-KV authors ran: the
+pages print no value that could settle it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rkv_oracle.c")
+_LIB = os.path.join(_HERE, "librkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BORDER_EPS = 1e-5  # |S_ij - tau| below this marks a threshold-borderline pair
+
+
+def build(force: bool = False) -> str:
+    """Compile ``rkv_oracle.c`` into ``librkv_oracle.so`` next to it.
+
+    ISO C11 with ``-ffp-contract=off`` so that no fused multiply-add changes
+    the rounding between the x86 and the Arm host."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+           "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            lib.rkv_oracle_cosine.argtypes = [dp, ctypes.c_int, ctypes.c_int, dp]
+            lib.rkv_oracle_cosine.restype = None
+            lib.rkv_oracle_attention.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, dp]
+            lib.rkv_oracle_attention.restype = None
+            lib.rkv_oracle_score.argtypes = [
+                dp, dp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double,
+                ctypes.c_double, dp, dp, dp, dp, dp, i32p, u8p, ctypes.c_int]
+            lib.rkv_oracle_score.restype = ctypes.c_int
+            lib.rkv_oracle_select.argtypes = [dp, ctypes.c_int64, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, i32p]
+            lib.rkv_oracle_select.restype = ctypes.c_int
+            lib.rkv_oracle_gather_bytes.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                i32p, ctypes.c_int, ctypes.c_void_p]
+            lib.rkv_oracle_gather_bytes.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Any array-like (numpy, or a CPU torch tensor via ``.numpy()``) as a
+    contiguous float64 numpy array; bf16/fp32 values upcast exactly."""
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def cosine(K) -> np.ndarray:
+    """S [N, N] of one problem's keys K [N, d] (redundancy row; cause 3)."""
+    K = _f64(K)
+    N, d = K.shape
+    S = np.empty((N, N), dtype=np.float64)
+    _load().rkv_oracle_cosine(_ptr(K, ctypes.c_double), N, d, _ptr(S, ctypes.c_double))
+    return S
+
+
+def attention(K, Q) -> np.ndarray:
+    """p [G, n_obs, N]: causal softmax of the observation queries Q
+    [G, n_obs, d] over one problem's keys K [N, d] (importance row)."""
+    K, Q = _f64(K), _f64(Q)
+    N, d = K.shape
+    G, n_obs, dq = Q.shape
+    assert dq == d
+    p = np.empty((G, n_obs, N), dtype=np.float64)
+    _load().rkv_oracle_attention(_ptr(K, ctypes.c_double), _ptr(Q, ctypes.c_double),
+                                 N, d, G, n_obs, _ptr(p, ctypes.c_double))
+    return p
+
+
+def score(K, Q, n_obs: int, lam: float, beta: int, tau: float,
+          nthreads: int | None = None) -> dict:
+    """Scores of P problems.  K [P, N, d] (the N = n_cached merged rows),
+    Q [P, G, n_obs, d].  Returns a dict of numpy arrays [P, N]:
+    I, R, Z (Z = +inf for observation tokens), sum, sim, newer, border."""
+    K, Q = _f64(K), _f64(Q)
+    P, N, d = K.shape
+    Pq, G, nq, dq = Q.shape
+    assert Pq == P and nq == n_obs and dq == d
+    out = {k: np.empty((P, N), dtype=np.float64) for k in ("I", "R", "Z", "sum", "sim")}
+    out["newer"] = np.empty((P, N), dtype=np.int32)
+    out["border"] = np.empty((P, N), dtype=np.uint8)
+    rc = _load().rkv_oracle_score(
+        _ptr(K, ctypes.c_double), _ptr(Q, ctypes.c_double), P, N, d, G, n_obs,
+        float(lam), int(beta), float(tau), BORDER_EPS,
+        _ptr(out["I"], ctypes.c_double), _ptr(out["R"], ctypes.c_double),
+        _ptr(out["Z"], ctypes.c_double), _ptr(out["sum"], ctypes.c_double),
+        _ptr(out["sim"], ctypes.c_double), _ptr(out["newer"], ctypes.c_int32),
+        _ptr(out["border"], ctypes.c_uint8),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle score: invalid sizes")
+    return out
+
+
+def select(Z, n_obs: int, budget: int) -> np.ndarray:
+    """idx [P, budget] (int32, ascending) of the kept tokens for scores
+    Z [P, N]; ties go to the larger index; N <= budget keeps everything and
+    pads the row with -1."""
+    Z = _f64(Z)
+    P, N = Z.shape
+    idx = np.empty((P, budget), dtype=np.int32)
+    rc = _load().rkv_oracle_select(_ptr(Z, ctypes.c_double), P, N, n_obs, budget,
+                                   _ptr(idx, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError("oracle select: invalid sizes")
+    return idx
+
+
+def gather(src: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """out[p, r] = src[p, idx[p, r]] for the budget rows, bytes copied
+    exactly; src [P, n_cap, ...] of any dtype.  Rows past budget are zero."""
+    src = np.ascontiguousarray(src)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    P, n_cap = src.shape[:2]
+    budget = idx.shape[1]
+    row_bytes = src[0, 0].nbytes if src.size else 0
+    out = np.zeros_like(src)
+    _load().rkv_oracle_gather_bytes(src.ctypes.data, P, n_cap, row_bytes,
+                                    _ptr(idx, ctypes.c_int32), budget, out.ctypes.data)
+    return out
+
+
+def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
+             beta: int, tau: float, nthreads: int | None = None) -> dict:
+    """Scores and selection of one compression round of P problems.
+    K [P, n_cap, d] (rows >= n_cached ignored), Q [P, G, n_obs, d].  Returns
+    dict(idx, scores); the kept rows themselves are ``gather(src, idx)``.
+
+    n_cached <= budget is the identity (nothing evicted)."""
+    Kn = np.asarray(K.detach().cpu() if hasattr(K, "detach") else K)
+    P = Kn.shape[0]
+    if n_cached <= budget:
+        idx = np.tile(np.arange(budget, dtype=np.int32), (P, 1))
+        idx[:, n_cached:] = -1
+        sc = None
+    else:
+        sc = score(_f64(K)[:, :n_cached], Q, n_obs, lam, beta, tau, nthreads)
+        idx = select(sc["Z"], n_obs, budget)
+    return {"idx": idx, "scores": sc}

@@ -1,0 +1,328 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test names the passage of the R-KV review page
+(yoonschallenge.tistory.com/1236) it checks and the mistake it would catch.
+The pages print no worked example (no score of any concrete input), so the
+pins are closed forms, brute force over subsets, reductions to library
+routines (numpy matmul, torch softmax / topk) and invariants.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_kv_cache_02_gb300 import workloads as wl
+
+
+def _basis(N, d):
+    K = np.zeros((N, d))
+    for i in range(N):
+        K[i, i % d] = 1.0
+    return K
+
+
+# ---------------------------------------------------------------- cosine --
+
+def test_cosine_equals_normalised_matmul():
+    """Redundancy row: cosine similarity of key vectors.  numpy's matmul of
+    row-normalised keys is an independent route (catches a missing norm, a
+    transposed operand or a wrong index)."""
+    rng = np.random.default_rng(0)
+    K = rng.standard_normal((37, 19)) * rng.uniform(0.1, 5.0, size=(37, 1))
+    Kn = K / np.linalg.norm(K, axis=1, keepdims=True)
+    np.testing.assert_allclose(oracle.cosine(K), Kn @ Kn.T, rtol=0, atol=1e-13)
+
+
+def test_cosine_zero_key_is_zero():
+    K = np.zeros((4, 3))
+    K[1] = [1.0, 2.0, 3.0]
+    K[2] = [-1.0, 0.5, 0.0]
+    S = oracle.cosine(K)
+    assert np.all(S[0] == 0.0) and np.all(S[:, 0] == 0.0)
+
+
+# ------------------------------------------------------------- attention --
+
+@pytest.mark.parametrize("N,d,G,n_obs", [(23, 16, 3, 8), (9, 4, 1, 1), (40, 64, 5, 8)])
+def test_attention_equals_torch_softmax(N, d, G, n_obs):
+    """Importance row: softmax attention of the observation queries.  Each
+    query row equals torch's fp64 softmax over its causal prefix of keys with
+    scale 1/sqrt(d) (catches a wrong scale, mask offset or normaliser)."""
+    g = torch.Generator().manual_seed(N * 100 + d)
+    K = torch.randn(N, d, generator=g, dtype=torch.float64)
+    Q = torch.randn(G, n_obs, d, generator=g, dtype=torch.float64) * 2.0
+    p = oracle.attention(K.numpy(), Q.numpy())
+    for h in range(G):
+        for q in range(n_obs):
+            last = N - n_obs + q
+            ref = torch.softmax(Q[h, q] @ K[: last + 1].T / math.sqrt(d), dim=0)
+            np.testing.assert_allclose(p[h, q, : last + 1], ref.numpy(), rtol=1e-12, atol=1e-15)
+            assert np.all(p[h, q, last + 1:] == 0.0)
+
+
+def test_importance_zero_queries_closed_form():
+    """Q = 0: every observation query attends uniformly to its causal prefix,
+    so I_i = (1/n_obs) * sum_q [i <= N-n_obs+q] / (N-n_obs+q+1) (catches a
+    mean taken over the wrong axis or a shifted mask)."""
+    N, d, G, n_obs = 30, 8, 4, 8
+    rng = np.random.default_rng(1)
+    K = rng.standard_normal((1, N, d))
+    Q = np.zeros((1, G, n_obs, d))
+    sc = oracle.score(K, Q, n_obs, 0.1, 2, 0.9)
+    expect = np.zeros(N)
+    for q in range(n_obs):
+        last = N - n_obs + q
+        expect[: last + 1] += 1.0 / (last + 1)
+    expect /= n_obs
+    np.testing.assert_allclose(sc["I"][0], expect, rtol=1e-13, atol=0)
+
+
+def test_importance_gqa_max_pool():
+    """Importance row: under GQA the heads sharing one KV head are max-pooled.
+    With one head of queries set to zero (uniform attention) and the others
+    copies of one query set, I is the elementwise max of the two single-head
+    importances (catches a mean or sum over heads)."""
+    N, d, n_obs = 25, 16, 8
+    rng = np.random.default_rng(2)
+    K = rng.standard_normal((1, N, d))
+    Qa = rng.standard_normal((1, 1, n_obs, d)) * 3.0
+    Qz = np.zeros((1, 1, n_obs, d))
+    Ia = oracle.score(K, Qa, n_obs, 0.1, 2, 0.9)["I"][0]
+    Iz = oracle.score(K, Qz, n_obs, 0.1, 2, 0.9)["I"][0]
+    Q3 = np.concatenate([Qa, Qz, Qa], axis=1)
+    I3 = oracle.score(K, Q3, n_obs, 0.1, 2, 0.9)["I"][0]
+    np.testing.assert_allclose(I3, np.maximum(Ia, Iz), rtol=1e-14, atol=0)
+    assert np.any(Ia > Iz) and np.any(Iz > Ia)
+
+
+# ------------------------------------------------------------- redundancy --
+
+def test_identical_keys_give_R_one():
+    """Closed form: all keys identical -> every cosine is 1; each candidate
+    has at least n_obs >= beta similar newer tokens, so none is protected and
+    R = (N-1)/(N-1) = 1 exactly (catches self-similarity counted, a wrong
+    denominator, or protection applied to every token)."""
+    N, d = 50, 32
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal(d)
+    K = np.tile(k, (1, N, 1)) * rng.uniform(0.5, 2.0, size=(1, N, 1))  # scaled copies
+    Q = rng.standard_normal((1, 4, 8, d))
+    sc = oracle.score(K, Q, 8, 0.1, 2, 0.9)
+    C = N - 8
+    np.testing.assert_allclose(sc["R"][0, :C], 1.0, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(sc["sum"][0], N - 1, rtol=0, atol=1e-11)
+
+
+def test_orthonormal_keys_give_R_zero():
+    N, d = 20, 24
+    K = _basis(N, d)[None]
+    Q = np.random.default_rng(4).standard_normal((1, 2, 8, d))
+    sc = oracle.score(K, Q, 8, 0.1, 2, 0.9)
+    assert np.all(sc["R"][0] == 0.0) and np.all(sc["sum"][0] == 0.0)
+
+
+def _triple_case(beta, tau=0.9, N=16):
+    """Orthonormal keys (in N+1 dims) except positions a=2 < b=5 < c=9,
+    which are scaled copies of one key: S is 1 inside the triple, 0 elsewhere."""
+    K = np.zeros((N, N + 1))
+    K[:, :N] = np.eye(N)
+    K[5] = 2.5 * K[2]
+    K[9] = 0.3 * K[2]
+    Q = np.zeros((1, 1, 4, N + 1))
+    return oracle.score(K[None], Q, 4, 0.0, beta, tau)
+
+
+@pytest.mark.parametrize("beta,expect", [
+    (0, (2, 2, 2)),   # nobody protected
+    (1, (2, 2, 0)),   # only the newest copy (no similar token newer than it)
+    (2, (2, 0, 0)),   # the two newest copies
+    (3, (0, 0, 0)),   # all three
+])
+def test_recency_protection_triple(beta, expect):
+    """Redundancy row: among similar tokens the beta most recent are
+    protected.  A triple of copies at a < b < c with beta = 0..3 gives these
+    closed forms (R in units of 1/(N-1)); catches 'older' counted instead of
+    'newer', an off-by-one in the beta comparison, and a missing
+    normalisation (the copies are scaled by 2.5 and 0.3)."""
+    N = 16
+    sc = _triple_case(beta)
+    a, b, c = 2, 5, 9
+    np.testing.assert_allclose(
+        [sc["R"][0, a], sc["R"][0, b], sc["R"][0, c]],
+        np.array(expect) / (N - 1), rtol=0, atol=1e-15)
+    assert list(sc["newer"][0, [a, b, c]]) == [2, 1, 0]
+    others = [i for i in range(N - 4) if i not in (a, b, c)]
+    assert np.all(sc["R"][0, others] == 0.0)
+
+
+def test_similarity_threshold_is_strict():
+    """S exactly equal to tau is not 'similar' (reading of the threshold as a
+    strict inequality): with tau = 1 the triple's cosines of exactly 1 protect
+    nothing, with tau just below 1 they do."""
+    N = 16
+    strict = _triple_case(beta=1, tau=1.0)
+    assert list(strict["newer"][0, [2, 5, 9]]) == [0, 0, 0]
+    np.testing.assert_allclose(strict["R"][0, [2, 5, 9]], 2 / (N - 1), atol=1e-15)
+    below = _triple_case(beta=1, tau=1.0 - 1e-9)
+    assert list(below["newer"][0, [2, 5, 9]]) == [2, 1, 0]
+
+
+def test_negative_similarity_lowers_R():
+    """A key and its negation have cosine -1: redundancy is a signed mean, and
+    -1 is never above tau (catches an absolute value)."""
+    N = 12
+    K = np.zeros((1, N, N))
+    K[0, :, :] = np.eye(N)
+    K[0, 6] = -K[0, 3]
+    sc = oracle.score(K, np.zeros((1, 1, 4, N)), 4, 0.1, 2, 0.9)
+    np.testing.assert_allclose(sc["R"][0, 3], -1 / (N - 1), atol=1e-15)
+    np.testing.assert_allclose(sc["R"][0, 6], -1 / (N - 1), atol=1e-15)
+    assert sc["newer"][0, 3] == 0
+
+
+def test_combined_score_extremes():
+    """Final selection criterion: Z rises with importance and falls with
+    redundancy.  lambda = 1 gives Z = I, lambda = 0 gives Z = -R; the
+    observation tokens carry +inf (always kept)."""
+    P, N, d, n_obs = 3, 40, 16, 8
+    rng = np.random.default_rng(5)
+    K = rng.standard_normal((P, N, d))
+    Q = rng.standard_normal((P, 2, n_obs, d))
+    s1 = oracle.score(K, Q, n_obs, 1.0, 2, 0.5)
+    s0 = oracle.score(K, Q, n_obs, 0.0, 2, 0.5)
+    C = N - n_obs
+    np.testing.assert_array_equal(s1["Z"][:, :C], s1["I"][:, :C])
+    np.testing.assert_array_equal(s0["Z"][:, :C], -s0["R"][:, :C])
+    assert np.all(np.isinf(s1["Z"][:, C:]))
+
+
+# -------------------------------------------------------------- selection --
+
+def _key_order_ok(Z, kept, C):
+    """Every kept candidate beats every evicted one on (Z, index)."""
+    ev = [i for i in range(C) if i not in kept]
+    if not ev or not kept:
+        return True
+    worst_kept = min((Z[i], i) for i in kept)
+    best_evicted = max((Z[i], i) for i in ev)
+    return worst_kept > best_evicted
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_selection_brute_force(seed):
+    """Top-k row ('keep the top tokens to fit the budget'): for tiny problems,
+    enumerate every k-subset of candidates; the oracle's kept set has the
+    largest total score, and ties are broken toward larger indices."""
+    rng = np.random.default_rng(100 + seed)
+    N, d, n_obs, budget = 12, 4, 3, 8
+    K = rng.standard_normal((1, N, d))
+    Q = rng.standard_normal((1, 2, n_obs, d))
+    sc = oracle.score(K, Q, n_obs, 0.1, 1, 0.6)
+    Z = sc["Z"][0]
+    if seed % 2:  # quantise to create exact ties
+        Z = np.round(Z * 20) / 20
+        Z[N - n_obs:] = np.inf
+    idx = oracle.select(Z[None], n_obs, budget)[0]
+    C, k = N - n_obs, budget - n_obs
+    kept = [int(i) for i in idx[:k]]
+    best = max(sum(Z[list(s)]) for s in itertools.combinations(range(C), k))
+    assert abs(sum(Z[kept]) - best) < 1e-12
+    assert _key_order_ok(Z, set(kept), C)
+    assert list(idx[k:]) == list(range(C, N))
+    assert all(idx[r] < idx[r + 1] for r in range(budget - 1))
+
+
+def test_selection_all_ties_keeps_newest():
+    """Equal scores everywhere: the tie rule keeps the most recent candidates."""
+    Z = np.zeros((1, 20))
+    Z[0, 15:] = np.inf
+    idx = oracle.select(Z, 5, 9)[0]
+    assert list(idx) == [11, 12, 13, 14, 15, 16, 17, 18, 19]
+
+
+def test_lambda_one_is_attention_topk():
+    """lambda = 1 reduces to attention-only eviction (the SnapKV-style
+    baseline the page compares against): the kept candidates are torch.topk of
+    the importance."""
+    w = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(w)
+    sc = oracle.score(K, Q, w.n_obs, 1.0, w.beta, w.tau)
+    idx = oracle.select(sc["Z"], w.n_obs, w.budget)
+    C, k = w.n_cached - w.n_obs, w.budget - w.n_obs
+    for p in range(w.problems):
+        top = torch.topk(torch.from_numpy(sc["I"][p, :C]), k).indices
+        assert set(top.tolist()) == set(idx[p, :k].tolist())
+
+
+def test_lambda_zero_is_bottom_redundancy():
+    w = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(w)
+    sc = oracle.score(K, Q, w.n_obs, 0.0, w.beta, w.tau)
+    idx = oracle.select(sc["Z"], w.n_obs, w.budget)
+    C, k = w.n_cached - w.n_obs, w.budget - w.n_obs
+    for p in range(w.problems):
+        low = np.argsort(sc["R"][p, :C], kind="stable")[:k]
+        assert set(low.tolist()) == set(idx[p, :k].tolist())
+
+
+@pytest.mark.parametrize("copies,beta", [(2, 1), (3, 2)])
+def test_duplicate_earlier_copy_goes_first(copies, beta):
+    """Redundancy row + recency protection: with equal importance (Q = 0, so
+    every candidate gets the same attention) and a key repeated `copies` times,
+    evicting one token removes the earliest copy; the newer copies are
+    protected."""
+    rng = np.random.default_rng(7)
+    N, d, n_obs = 24, 512, 4
+    K = rng.standard_normal((1, N, d))
+    pos = [3, 8, 14][:copies]
+    for p_ in pos[1:]:
+        K[0, p_] = K[0, pos[0]] * (1.0 + 0.1 * p_) + 1e-3 * rng.standard_normal(d)
+    Q = np.zeros((1, 2, n_obs, d))
+    sc = oracle.score(K, Q, n_obs, 0.1, beta, 0.9)
+    idx = oracle.select(sc["Z"], n_obs, N - 1)[0]
+    evicted = sorted(set(range(N)) - set(idx.tolist()))
+    assert evicted == [pos[0]]
+
+
+# ------------------------------------------------------------- invariants --
+
+def test_compress_invariants_tiny_and_identity():
+    """Scheme row: exactly `budget` tokens stay, the newest n_obs always stay,
+    indices are ascending; with n_cached <= budget nothing is evicted."""
+    w = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(w, n_cap=w.n_cached + 5)
+    res = oracle.compress(K, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau)
+    idx = res["idx"]
+    assert idx.shape == (w.problems, w.budget)
+    assert np.all(np.diff(idx, axis=1) > 0)
+    assert np.all(idx[:, -w.n_obs:] == np.arange(w.n_cached - w.n_obs, w.n_cached))
+    ident = oracle.compress(K, Q, 50, w.budget, w.n_obs, w.lam, w.beta, w.tau)["idx"]
+    assert np.all(ident[:, :50] == np.arange(50)) and np.all(ident[:, 50:] == -1)
+
+
+def test_gather_copies_bytes():
+    rng = np.random.default_rng(9)
+    src = rng.standard_normal((2, 10, 6)).astype(np.float32)
+    idx = np.array([[0, 3, 4, 9], [1, 2, 7, 8]], dtype=np.int32)
+    out = oracle.gather(src, idx)
+    for p in range(2):
+        np.testing.assert_array_equal(out[p, :4], src[p, idx[p]])
+        assert np.all(out[p, 4:] == 0)
+
+
+def test_page_parameters_fixture():
+    """The page's printed defaults (buffer 128, 8 observation tokens,
+    lambda = 0.1) are the ones every workload uses."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "rkv_page_parameters.json")
+    fx = json.load(open(path))
+    for w in wl.WORKLOADS:
+        assert w.n_obs == fx["n_obs"]["value"]
+        assert w.lam == fx["lambda"]["value"]
+        if w.keys == "ar1":
+            assert w.n_cached - w.budget == fx["buffer"]["value"] or w.name == "stream"
+    assert wl.BY_NAME["stream"].buffer == fx["buffer"]["value"]
