@@ -1,0 +1,414 @@
+"""Benchmark of the R-KV compression step on GB300.
+
+One step = one ``rkv_compress`` call over every (layer, sequence, KV head)
+problem of the workload: key statistics, importance, thresholded Gram ->
+redundancy and Z, top-k select, and the copy of the kept K/V rows.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  ``value`` is compressed KV tokens per second
+(P * n_cached token slots per step) over all ranks, device-timed with CUDA
+events on the launching stream, inputs resident in HBM (K + V are far larger
+than L2, so no L2 flush is needed).  ``e2e`` is the same metric with the
+host->device copy of K, V, Q_obs from pinned memory and the device->host copy
+of the compacted K, V and the indices inside the timed region.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_kv_cache_02_gb300 import rkv, workloads as wl  # noqa: E402
+
+METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM roofline"
+UNIT = "tokens/s"
+
+
+# ------------------------------------------------------------------ utils --
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(elapsed_ms: float, units: float, world: int):
+    """Max of the ranks' elapsed times and the sum of their units (the
+    whole-job throughput is sum(units) / max(time))."""
+    if world == 1:
+        return elapsed_ms, units
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------- algorithmic work model --
+
+def work_model(w: wl.Workload) -> dict:
+    """Algorithmic bytes (HBM) / flops per launch of each kernel, for the
+    whole step (all P problems).  See the kernel table in the design doc."""
+    P, N, d, G, es = w.problems, w.n_cached, w.head_dim, w.gqa, (2 if w.dtype == "bf16" else 4)
+    B, n_obs = w.budget, w.n_obs
+    k_bytes = P * N * d * es
+    return {
+        "key_stats": {"bytes": k_bytes + 2 * P * N * 4},
+        "importance": {"bytes": k_bytes + P * G * n_obs * d * es + P * N * 4},
+        "gram_tc": {"flops": P * N * (N - 1) * d, "bytes": k_bytes + 3 * P * N * 4},
+        "gram_simt": {"flops": 2 * P * N * N * d, "bytes": k_bytes + 3 * P * N * 4},
+        "select": {"bytes": P * (N - n_obs) * 4 + P * B * 4},
+        "gather": {"bytes": 4 * P * B * d * es + P * B * 4},
+    }
+
+
+def roofline(kernels: dict, model: dict, peaks: dict, steps: int) -> dict:
+    """Roofline of the kernel with the largest device time."""
+    name = max(kernels, key=lambda k: kernels[k]["ms"])
+    ms = kernels[name]["ms"] / max(1, kernels[name]["launches"]) if kernels[name]["launches"] \
+        else kernels[name]["ms"]
+    per_launch_ms = kernels[name]["ms"] / max(1, kernels[name]["launches"])
+    m = model.get(name, {})
+    if name == "gram_tc":
+        achieved = m["flops"] / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        r = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
+             "unit": "TFLOP/s", "peak_kind": "bf16 sustained (of " + peaks["source"] + ")"}
+    elif name == "gram_simt":
+        achieved = m["flops"] / (per_launch_ms * 1e-3) / 1e12
+        peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        r = {"kernel": name, "bound": "alu", "achieved": achieved, "peak": peak,
+             "unit": "TFLOP/s", "peak_kind": "fp32 FFMA, 152 SMs x 128 lanes x 2 x max SM clock"}
+    else:
+        achieved = m["bytes"] / (per_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        r = {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": peak,
+             "unit": "GB/s", "peak_kind": "HBM copy (of " + peaks["source"] + ")"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["ms_per_launch"] = per_launch_ms
+    r["traffic"] = None  # dram bytes per launch from ncu; filled from profiles/ when current
+    del ms
+    return r
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_oracle_sample(w: wl.Workload, K, Q, seconds: float = 15.0, max_problems: int = 4096):
+    """Times the oracle (as it stands) on a bounded sample of the workload's
+    problems on all host cores; returns a cpu_baseline dict in tokens/s."""
+    import oracle
+    cores = oracle.default_threads()
+    # calibrate on a few problems, then size the sample to ~`seconds`
+    n0 = min(max(cores, 4), K.shape[0])
+    Kh = K[:n0, :w.n_cached].cpu()
+    Qh = Q[:n0].cpu()
+    t0 = time.perf_counter()
+    oracle.score(Kh, Qh, w.n_obs, w.lam, w.beta, w.tau, nthreads=cores)
+    dt = time.perf_counter() - t0
+    per_problem = dt / n0
+    n = int(min(max_problems, K.shape[0], max(n0, seconds / max(per_problem, 1e-9))))
+    Kh = K[:n, :w.n_cached].cpu()
+    Qh = Q[:n].cpu()
+    t0 = time.perf_counter()
+    sc = oracle.score(Kh, Qh, w.n_obs, w.lam, w.beta, w.tau, nthreads=cores)
+    oracle.select(sc["Z"], w.n_obs, w.budget)
+    dt = time.perf_counter() - t0
+    return {"value": n * w.n_cached / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.problems} problems of {w.name} (N={w.n_cached}, d={w.head_dim}),"
+                      f" scores + selection in fp64, {dt:.1f} s",
+            "seconds": dt, "problems": n}
+
+
+# ------------------------------------------------------------------ arms --
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step scores and selects a
+    bounded sample of the workload's problems on the host cores."""
+    import oracle
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    cores = oracle.default_threads()
+    P = min(w.problems, args.ref_problems or max(cores, 16))
+    K, V, Q = wl.make_inputs(w, device="cpu", problems=P)
+    Kh = K[:, :w.n_cached].double().numpy()
+    Qh = Q.double().numpy()
+    oracle.score(Kh[:1], Qh[:1], w.n_obs, w.lam, w.beta, w.tau, nthreads=1)  # warm-up
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sc = oracle.score(Kh, Qh, w.n_obs, w.lam, w.beta, w.tau, nthreads=cores)
+        oracle.select(sc["Z"], w.n_obs, w.budget)
+    dt = time.perf_counter() - t0
+    value = args.steps * P * w.n_cached / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, sample_problems=P),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{P} of {w.problems} problems per step (scores + selection)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, **extra):
+    c = {"workload": w.name, "layers": w.layers, "batch": w.batch, "kv_heads": w.kv_heads,
+         "gqa": w.gqa, "head_dim": w.head_dim, "problems": w.problems, "n_cached": w.n_cached,
+         "budget": w.budget, "n_obs": w.n_obs, "lambda": w.lam, "beta": w.beta, "tau": w.tau,
+         "l2": "no flush: K+V inputs exceed the 129 MB L2"}
+    c.update(extra)
+    return c
+
+
+def run_ours(args, w):
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rkv.load()
+    K, V, Q = wl.make_inputs(w, device=dev, seed=w.seed + rank)
+    out_K = torch.empty_like(K)
+    out_V = torch.empty_like(V)
+    idx = torch.empty((w.problems, w.budget), dtype=torch.int32, device=dev)
+    ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rkv.rkv_compress(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
+                         out_K=out_K, out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error during warm-up")
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rkv.rkv_timing_read(reset=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        _barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        rkv.rkv_timing_enable(True)
+        for _ in range(args.steps):
+            step()
+        rkv.rkv_timing_enable(False)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+    elapsed = start.elapsed_time(stop)
+    timing = rkv.rkv_timing_read(reset=True)
+    kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in timing.items() if v[1] > 0}
+    launches = sum(v["launches"] for v in kernels.values())
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error in the timed region")
+
+    units = args.steps * w.problems * w.n_cached
+    t_max, u_sum = aggregate(elapsed, units, world)
+    peaks = _peaks()
+    model = work_model(w)
+    line = {
+        "metric": METRIC, "value": u_sum / (t_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": _config(w, mode="out-of-place (outputs in separate buffers)",
+                          parallelism=f"replicas x{world}, no collective"),
+        "steps_per_s": world * args.steps / (t_max * 1e-3),
+        "evicted_tokens_per_s": world * args.steps * w.problems * (w.n_cached - w.budget)
+        / (t_max * 1e-3),
+        "gpu_launches": launches,
+        "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
+        "clocks": clocks.summary(),
+    }
+    line["roofline"] = roofline(kernels, model, peaks, args.steps)
+    # all kernels' fractions, for the record
+    line["roofline_all"] = {}
+    for k, v in kernels.items():
+        if k not in model or not v["launches"]:
+            continue
+        per = v["ms"] / v["launches"] * 1e-3
+        m = model[k]
+        entry = {"ms_per_launch": per * 1e3}
+        if "bytes" in m:
+            entry["hbm_frac"] = m["bytes"] / per / 1e9 / peaks["hbm_gbs"]
+        if k == "gram_tc":
+            entry["tensor_frac"] = m["flops"] / per / 1e12 / peaks["bf16_tflops_sustained"]
+        line["roofline_all"][k] = entry
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, K, Q, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world):
+    """Same step through the public API with host buffers: pinned K, V, Q
+    copied in, compacted K, V (the kept rows) and idx copied out, each step."""
+    B = w.budget
+    hK = torch.empty(K.shape, dtype=K.dtype, pin_memory=True)
+    hV = torch.empty(V.shape, dtype=V.dtype, pin_memory=True)
+    hQ = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
+    hK.copy_(K)
+    hV.copy_(V)
+    hQ.copy_(Q)
+    oK = torch.empty((K.shape[0], B, K.shape[2]), dtype=K.dtype, pin_memory=True)
+    oV = torch.empty_like(oK, pin_memory=True)
+    oI = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True)
+
+    def step():
+        K.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        Q.copy_(hQ, non_blocking=True)
+        rkv.rkv_compress(K, V, Q, w.n_cached, B, w.n_obs, w.lam, w.beta, w.tau, out_K=out_K,
+                         out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
+        oK.copy_(out_K[:, :B], non_blocking=True)
+        oV.copy_(out_V[:, :B], non_blocking=True)
+        oI.copy_(idx, non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    for _ in range(steps):
+        step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    t_max, u_sum = aggregate(s0.elapsed_time(s1), steps * w.problems * w.n_cached, world)
+    h2d = hK.numel() * hK.element_size() + hV.numel() * hV.element_size() + \
+        hQ.numel() * hQ.element_size()
+    d2h = oK.numel() * oK.element_size() * 2 + oI.numel() * oI.element_size()
+    return {"value": u_sum / (t_max * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": t_max / steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama8b_full", choices=list(wl.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-problems", type=int, default=0)
+    args = ap.parse_args()
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,49 @@
+// rkv_internal.h -- launchers shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rkv {
+
+struct DeviceStatus;
+
+// Everything the scoring kernels of one call need.
+struct ScoreArgs {
+    const void* K;       // [P, n_cap, d]
+    const void* Q;       // [P, G, n_obs, d]
+    int64_t P;
+    int G, d, n_cap, N, n_obs, beta;
+    int dtype;           // RKV_DTYPE_*
+    float lambda, tau;
+    // workspace rows (stride ld_ws floats per problem)
+    float* inv_norm;     // 1 / max(|k_i|, eps)
+    float* sum_s;        // sum_{j != i} S_ij
+    int64_t ld_ws;
+    // outputs (stride ld_out floats per problem); R may be null
+    float* I;
+    float* R;
+    float* Z;
+    int64_t ld_out;
+    DeviceStatus* status;
+};
+
+cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_importance(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_gram_simt(const ScoreArgs& a, cudaStream_t s);
+bool gram_tc_supported(const ScoreArgs& a);
+cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);
+
+cudaError_t launch_select(int64_t P, int N, const float* Z, int64_t ldz, int n_obs,
+                          int budget, int32_t* idx, DeviceStatus* st, cudaStream_t s);
+
+// Copies kept rows of up to two tensors (b may be null).  row_bytes is a
+// multiple of 16; in_place means dst == src for both tensors.
+cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, void* dst_b,
+                          const int32_t* idx, int64_t P, int n_cap, int budget,
+                          int row_bytes, bool in_place, DeviceStatus* st, cudaStream_t s);
+
+// idx rows = 0..n-1 then -1 (nothing evicted).
+cudaError_t launch_identity_idx(int64_t P, int n, int budget, int32_t* idx, cudaStream_t s);
+
+}  // namespace rkv

@@ -1,0 +1,250 @@
+"""Thin ctypes binding of librkv (include/rkv.h), one function per C entry
+point with the same name.
+
+The binding only checks tensor metadata, allocates outputs the caller did not
+pass, and forwards raw device pointers plus the current CUDA stream to the
+library; every step of the computation runs in librkv's kernels.  There is no
+fallback: if ``librkv.so`` is missing the import of a function raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librkv.so")
+
+RKV_OK = 0
+RKV_DTYPE_BF16 = 0
+RKV_DTYPE_FP32 = 1
+RKV_MAX_TOKENS = 32768
+
+EXPORTED = [
+    "rkv_workspace_size", "rkv_compress", "rkv_score", "rkv_select", "rkv_gather",
+    "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
+    "rkv_timing_read", "rkv_kernel_name",
+]
+
+
+class RkvError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("num_problems", ctypes.c_int64), ("gqa_group", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_capacity", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Loads librkv.so (built by ``decode_kv_cache_02_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"librkv.so not found at {p}; build it with "
+                "`python -m decode_kv_cache_02_gb300.build` (no fallback exists)")
+        lib = ctypes.CDLL(p)
+        vp, sz, i32, i64, f32 = (ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                 ctypes.c_int64, ctypes.c_float)
+        dp = ctypes.POINTER(_Desc)
+        lib.rkv_workspace_size.argtypes = [dp, i32, i32]
+        lib.rkv_workspace_size.restype = sz
+        lib.rkv_compress.argtypes = [dp, vp, vp, vp, i32, i32, i32, f32, i32, f32, vp, vp, vp,
+                                     vp, sz, vp]
+        lib.rkv_compress.restype = i32
+        lib.rkv_score.argtypes = [dp, vp, vp, i32, i32, f32, i32, f32, vp, vp, vp, vp, sz, vp]
+        lib.rkv_score.restype = i32
+        lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
+        lib.rkv_select.restype = i32
+        lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
+        lib.rkv_gather.restype = i32
+        lib.rkv_workspace_init.argtypes = [vp, vp]
+        lib.rkv_workspace_init.restype = i32
+        lib.rkv_get_device_status.argtypes = [vp, vp]
+        lib.rkv_get_device_status.restype = i32
+        lib.rkv_strerror.argtypes = [i32]
+        lib.rkv_strerror.restype = ctypes.c_char_p
+        lib.rkv_timing_enable.argtypes = [i32]
+        lib.rkv_timing_enable.restype = i32
+        lib.rkv_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_int64), i32, i32]
+        lib.rkv_timing_read.restype = i32
+        lib.rkv_kernel_name.argtypes = [i32]
+        lib.rkv_kernel_name.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    return load().rkv_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != RKV_OK:
+        raise RkvError(rc, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RKV_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return RKV_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def make_desc(K: torch.Tensor, gqa_group: int) -> _Desc:
+    """Descriptor of a K (or V) tensor [P, n_capacity, head_dim]."""
+    if K.dim() != 3:
+        raise ValueError("K must be [P, n_capacity, head_dim]")
+    P, n_cap, d = K.shape
+    return _Desc(P, int(gqa_group), d, n_cap, _dtype_code(K))
+
+
+def rkv_workspace_size(K: torch.Tensor, gqa_group: int, n_cached: int, n_obs: int) -> int:
+    desc = make_desc(K, gqa_group)
+    return int(load().rkv_workspace_size(ctypes.byref(desc), int(n_cached), int(n_obs)))
+
+
+def alloc_workspace(K: torch.Tensor, gqa_group: int, n_cached: int, n_obs: int) -> torch.Tensor:
+    """A zero-filled uint8 device tensor of rkv_workspace_size() bytes."""
+    n = rkv_workspace_size(K, gqa_group, n_cached, n_obs)
+    if n == 0:
+        raise ValueError("invalid workspace request")
+    return torch.zeros(n, dtype=torch.uint8, device=K.device)
+
+
+def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
+                 beta: int = 2, tau: float = 0.9, out_K=None, out_V=None, out_idx=None,
+                 workspace=None, stream=None):
+    """One compression round of every problem in K/V [P, n_cap, d] with
+    Q_obs [P, G, n_obs, d].  Returns (out_K, out_V, out_idx); pass
+    out_K=K, out_V=V to compact in place."""
+    for t, n in ((K, "K"), (V, "V"), (Q_obs, "Q_obs")):
+        _cuda(t, n)
+    if V.shape != K.shape or V.dtype != K.dtype or Q_obs.dtype != K.dtype:
+        raise ValueError("K, V, Q_obs must share shape/dtype")
+    if Q_obs.dim() != 4 or Q_obs.shape[0] != K.shape[0] or Q_obs.shape[2] != n_obs \
+            or Q_obs.shape[3] != K.shape[2]:
+        raise ValueError("Q_obs must be [P, G, n_obs, d]")
+    G = Q_obs.shape[1]
+    desc = make_desc(K, G)
+    if out_K is None:
+        out_K = torch.empty_like(K)
+    if out_V is None:
+        out_V = torch.empty_like(V)
+    if out_idx is None:
+        out_idx = torch.empty((K.shape[0], budget), dtype=torch.int32, device=K.device)
+    if workspace is None:
+        workspace = alloc_workspace(K, G, max(n_cached, 1), n_obs)
+    for t, n in ((out_K, "out_K"), (out_V, "out_V"), (out_idx, "out_idx")):
+        _cuda(t, n)
+    if out_K.shape != K.shape or out_V.shape != K.shape or out_idx.shape != (K.shape[0], budget) \
+            or out_idx.dtype != torch.int32:
+        raise ValueError("output shapes")
+    rc = load().rkv_compress(ctypes.byref(desc), K.data_ptr(), V.data_ptr(), Q_obs.data_ptr(),
+                             int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
+                             float(tau), out_K.data_ptr(), out_V.data_ptr(), out_idx.data_ptr(),
+                             workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _check(rc, "rkv_compress")
+    return out_K, out_V, out_idx
+
+
+def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
+              tau: float = 0.9, workspace=None, stream=None):
+    """(I, R, Z), each fp32 [P, n_cached]."""
+    _cuda(K, "K")
+    _cuda(Q_obs, "Q_obs")
+    G = Q_obs.shape[1]
+    desc = make_desc(K, G)
+    P = K.shape[0]
+    I = torch.empty((P, n_cached), dtype=torch.float32, device=K.device)
+    R = torch.empty_like(I)
+    Z = torch.empty_like(I)
+    if workspace is None:
+        workspace = alloc_workspace(K, G, n_cached, n_obs)
+    rc = load().rkv_score(ctypes.byref(desc), K.data_ptr(), Q_obs.data_ptr(), int(n_cached),
+                          int(n_obs), float(lam), int(beta), float(tau), I.data_ptr(),
+                          R.data_ptr(), Z.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          _stream_ptr(stream))
+    _check(rc, "rkv_score")
+    return I, R, Z
+
+
+def rkv_select(Z, n_obs: int, budget: int, out_idx=None, stream=None):
+    """idx [P, budget] of the kept tokens for fp32 scores Z [P, n]."""
+    _cuda(Z, "Z")
+    if Z.dtype != torch.float32 or Z.dim() != 2:
+        raise ValueError("Z must be fp32 [P, n]")
+    P, n = Z.shape
+    if out_idx is None:
+        out_idx = torch.empty((P, budget), dtype=torch.int32, device=Z.device)
+    rc = load().rkv_select(P, n, Z.data_ptr(), int(n_obs), int(budget), out_idx.data_ptr(),
+                           _stream_ptr(stream))
+    _check(rc, "rkv_select")
+    return out_idx
+
+
+def rkv_gather(src, idx, budget: int, dst=None, stream=None):
+    """dst[p, r] = src[p, idx[p, r]] for r < budget (dst=src: in place)."""
+    _cuda(src, "src")
+    _cuda(idx, "idx")
+    if idx.dtype != torch.int32 or idx.shape != (src.shape[0], budget):
+        raise ValueError("idx must be int32 [P, budget]")
+    desc = make_desc(src, 1)
+    if dst is None:
+        dst = torch.empty_like(src)
+    rc = load().rkv_gather(ctypes.byref(desc), src.data_ptr(), idx.data_ptr(), int(budget),
+                           dst.data_ptr(), _stream_ptr(stream))
+    _check(rc, "rkv_gather")
+    return dst
+
+
+def rkv_workspace_init(workspace, stream=None):
+    _check(load().rkv_workspace_init(workspace.data_ptr(), _stream_ptr(stream)),
+           "rkv_workspace_init")
+
+
+def rkv_get_device_status(workspace, stream=None) -> int:
+    """Synchronises the stream; returns RKV_OK or the device error code."""
+    return int(load().rkv_get_device_status(workspace.data_ptr(), _stream_ptr(stream)))
+
+
+def rkv_timing_enable(on: bool = True):
+    load().rkv_timing_enable(1 if on else 0)
+
+
+def rkv_timing_read(reset: bool = True) -> dict:
+    """{kernel name: (total ms, launches)} of the timed launches so far."""
+    lib = load()
+    n = 16
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    k = lib.rkv_timing_read(ms, cnt, n, 1 if reset else 0)
+    if k < 0:
+        raise RkvError(-k, "rkv_timing_read")
+    return {lib.rkv_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(min(k, n))}

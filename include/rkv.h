@@ -1,0 +1,153 @@
+/*
+ * rkv.h -- C ABI of librkv, the GB300 (sm_103a) implementation of R-KV's
+ * decode-time KV-cache compression step.
+ *
+ * The operation (R-KV review, yoonschallenge.tistory.com/1236):
+ *   - opening notes and summary-table row "Decoding-time compression
+ *     scheme": the fixed cache B_budget and the buffer B_buffer of newly
+ *     generated tokens are merged (here: rows 0..budget-1 followed by the
+ *     buffer rows, n_cached rows in all); the newest n_obs (8) observation
+ *     tokens are always kept; every other token is scored and only the top
+ *     ones are kept, so that exactly `budget` rows remain.
+ *   - row "importance": I_i is the softmax attention the n_obs observation
+ *     queries give key i (mean over the queries, scale 1/sqrt(d), causal among
+ *     the observation tokens), max-pooled over the G query heads that share
+ *     the KV head.
+ *   - row "redundancy": R_i is the mean cosine similarity of key i to the
+ *     other n_cached-1 keys of the same KV head; a similar pair is one with
+ *     cosine > tau; token i is protected (its above-tau similarities are
+ *     dropped from its sum) when fewer than beta newer tokens are similar to
+ *     it, i.e. the beta most recent tokens of a similar group are protected.
+ *   - row "final selection criterion": Z_i = lambda*I_i - (1-lambda)*R_i
+ *     (lambda = 0.1 on the page); ties go to the newer token.
+ *   - question 2, cause 3: the kept K/V rows are copied into the new cache.
+ *
+ * One "problem" is one (layer, sequence, KV head).  All P problems of a call
+ * share n_cached, budget and the parameters and are processed by one launch
+ * per kernel.
+ *
+ * Layouts (every array contiguous, row-major; element type `dtype`):
+ *   K, V, out_K, out_V   [P, n_capacity, head_dim]; problem p starts at
+ *                        element p*n_capacity*head_dim.  head_dim*elem_size
+ *                        must be a multiple of 16 bytes and every base pointer
+ *                        16-byte aligned.
+ *   Q_obs                [P, G, n_obs, head_dim]: query q of query head g of
+ *                        problem p.  Query head g of the G that share the KV
+ *                        head of problem p.
+ *   out_idx              [P, budget] int32.
+ *   out_I, out_R, out_Z  [P, n_cached] float.
+ *
+ * Ownership and execution: every pointer is device memory owned by the
+ * caller.  The calls never allocate or free device memory and never
+ * synchronise: they check their arguments on the host, enqueue kernels on
+ * `stream` (a cudaStream_t, or NULL for the legacy default stream) and return.
+ * Results are valid in stream order.  Scratch memory is the caller's
+ * `workspace` of at least rkv_workspace_size() bytes, 256-byte aligned; one
+ * workspace must not be used by two calls that may overlap on the GPU.
+ *
+ * Errors: each call returns RKV_OK or an RKV_ERR_* code and enqueues nothing
+ * on error.  Errors raised on the device (a bounded wait that timed out, an
+ * index found out of range) are recorded in the workspace and read by
+ * rkv_get_device_status().  Not thread-safe only where stated.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    RKV_OK = 0,
+    RKV_ERR_INVALID_ARG = 1, /* a size, count or pointer is invalid */
+    RKV_ERR_UNSUPPORTED = 2, /* dtype / head_dim / group size not supported */
+    RKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
+    RKV_ERR_ALIAS = 4,       /* outputs partially overlap inputs */
+    RKV_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    RKV_ERR_DEVICE = 6       /* a kernel recorded an error (see status) */
+};
+
+enum { RKV_DTYPE_BF16 = 0, RKV_DTYPE_FP32 = 1 };
+
+/* Shape of one call's problems. */
+typedef struct {
+    int64_t num_problems; /* P = layers * sequences * kv_heads (>= 0)        */
+    int32_t gqa_group;    /* G, query heads per KV head, 1..16               */
+    int32_t head_dim;     /* d, 64 or 128                                    */
+    int32_t n_capacity;   /* rows allocated per problem in K/V/out_K/out_V   */
+    int32_t dtype;        /* RKV_DTYPE_BF16 or RKV_DTYPE_FP32 (K, V, Q, out) */
+} rkv_desc;
+
+/* Largest n_cached accepted by rkv_compress / rkv_score. */
+#define RKV_MAX_TOKENS 32768
+
+/* Bytes of workspace rkv_compress / rkv_score need for `desc` and n_cached
+ * tokens with n_obs observation tokens.  0 if the arguments are invalid. */
+size_t rkv_workspace_size(const rkv_desc* desc, int n_cached, int n_obs);
+
+/* One compression round (the whole step above) for all P problems.
+ *   n_cached   rows in use per problem (merged cache + buffer), <= n_capacity
+ *   budget     rows kept per problem, n_obs <= budget <= n_capacity
+ *   n_obs      observation tokens (the newest n_obs rows), >= 1
+ *   lambda, beta, tau   the parameters of Z, protection and similarity
+ *   out_K/out_V  receive the kept rows in ascending original position in
+ *              their rows 0..budget-1; rows >= budget are not touched.  They
+ *              may be K/V themselves (in-place compaction) but must not
+ *              overlap them otherwise (RKV_ERR_ALIAS).
+ *   out_idx    [P, budget]: kept original row indices, strictly ascending;
+ *              the last n_obs are n_cached-n_obs .. n_cached-1.
+ * n_cached <= budget evicts nothing: out_idx = 0..n_cached-1 then -1, and the
+ * rows are copied only when the outputs are not the inputs. */
+int rkv_compress(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                 int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                 void* out_K, void* out_V, int32_t* out_idx,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* The scores alone (for tests and analysis): out_I, out_R, out_Z
+ * [P, n_cached].  Observation tokens get R = 0 and Z = +inf. */
+int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cached,
+              int n_obs, float lambda, int beta, float tau,
+              float* out_I, float* out_R, float* out_Z,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* The selection alone: for scores Z [P, n] (fp32), out_idx [P, budget] as
+ * rkv_compress would produce it (top budget-n_obs of the candidates
+ * 0..n-n_obs-1 by Z, ties to the larger index, then the n_obs observation
+ * tokens, ascending).  Requires n_obs <= budget < n <= RKV_MAX_TOKENS. */
+int rkv_select(int64_t num_problems, int n, const float* Z, int n_obs, int budget,
+               int32_t* out_idx, void* stream);
+
+/* The copy alone: dst[p, r, :] = src[p, idx[p, r], :] for r < budget where
+ * idx >= 0, src and dst laid out as K in `desc`; idx rows strictly ascending.
+ * dst may equal src (in place) but must not overlap it otherwise. */
+int rkv_gather(const rkv_desc* desc, const void* src, const int32_t* idx, int budget,
+               void* dst, void* stream);
+
+/* Clears the device error word at the start of `workspace` (enqueued on
+ * `stream`).  Call once on a fresh workspace before its first use, unless the
+ * workspace was allocated zero-filled. */
+int rkv_workspace_init(void* workspace, void* stream);
+
+/* Synchronises `stream`, returns the first error a kernel recorded in
+ * `workspace` since the last call (RKV_OK if none) and clears it. */
+int rkv_get_device_status(void* workspace, void* stream);
+
+/* Human-readable name of an RKV_* code. */
+const char* rkv_strerror(int code);
+
+/* Per-kernel timing (not thread-safe).  While enabled, each launch of the
+ * library is bracketed by CUDA events on its stream.  rkv_timing_read waits for
+ * the events, writes per-kernel totals (milliseconds) and launch counts for up
+ * to `max_kernels` kernels in the order of rkv_kernel_name(), returns the
+ * number of kernel kinds, and with reset != 0 clears the totals. */
+int rkv_timing_enable(int on);
+int rkv_timing_read(double* total_ms, int64_t* launches, int max_kernels, int reset);
+const char* rkv_kernel_name(int kernel);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H */

@@ -1,0 +1,102 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds, loads and
+exports every function include/rkv.h declares; sizes and argument errors are
+answered on the host without touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_kv_cache_02_gb300 import build, rkv
+    build.build()
+    return rkv.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(rkv_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert "rkv_compress" in declared and "rkv_score" in declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    from decode_kv_cache_02_gb300 import rkv
+    assert set(rkv.EXPORTED) >= declared
+
+
+def test_strerror(lib):
+    from decode_kv_cache_02_gb300 import rkv
+    assert rkv.strerror(0) == "ok"
+    assert "workspace" in rkv.strerror(3)
+    assert rkv.strerror(999) == "unknown error code"
+
+
+def _desc(P=4, G=4, d=128, n_cap=1152, dtype=0):
+    from decode_kv_cache_02_gb300 import rkv
+    return rkv._Desc(P, G, d, n_cap, dtype)
+
+
+def test_workspace_size(lib):
+    d = _desc()
+    n = lib.rkv_workspace_size(ctypes.byref(d), 1152, 8)
+    # status block + four fp32 [P, N] arrays, each rounded to 256 bytes
+    assert n == 256 + 4 * ((4 * 1152 * 4 + 255) // 256 * 256)
+    assert lib.rkv_workspace_size(None, 1152, 8) == 0
+    bad = _desc(d=96)
+    assert lib.rkv_workspace_size(ctypes.byref(bad), 1152, 8) == 0
+
+
+def test_argument_errors_need_no_device(lib):
+    from decode_kv_cache_02_gb300 import rkv
+    d = _desc()
+    fake = 1 << 20  # never dereferenced: every call below fails its checks first
+    ws = 1 << 24
+    call = lambda **kw: lib.rkv_compress(
+        ctypes.byref(kw.get("desc", d)), kw.get("K", fake), fake + 2 ** 30, fake + 2 ** 31,
+        kw.get("n", 1152), kw.get("budget", 1024), kw.get("n_obs", 8), 0.1, kw.get("beta", 2),
+        0.9, kw.get("oK", fake + 2 ** 32), kw.get("oV", fake + 2 ** 33), fake + 2 ** 34,
+        kw.get("ws", ws), kw.get("ws_bytes", 1), None)
+    assert lib.rkv_compress(None, 0, 0, 0, 1, 1, 1, 0.1, 2, 0.9, 0, 0, 0, 0, 0, None) == 1
+    assert call(n_obs=0) == 1                      # no observation token
+    assert call(n_obs=2000) == 1                   # n_obs > budget
+    assert call(n=2000) == 1                       # n_cached > capacity
+    assert call(beta=-1) == 1
+    assert call(K=fake + 2) == 1                   # misaligned
+    assert call(desc=_desc(d=80)) == 2             # unsupported head_dim
+    assert call(desc=_desc(dtype=7)) == 2
+    assert call(ws_bytes=10) == 3                  # workspace too small
+    assert call(ws=ws + 16, ws_bytes=1 << 40) == 3  # workspace misaligned
+    assert call(oK=fake + 4096, ws_bytes=1 << 40) == 4  # partial overlap with K
+    assert lib.rkv_select(1, 100, fake, 8, 100, fake, None) == 1   # budget >= n
+    assert lib.rkv_select(1, 100, fake, 9, 8, fake, None) == 1     # n_obs > budget
+    assert lib.rkv_gather(ctypes.byref(d), fake, fake, 0, fake, None) == 1
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    from decode_kv_cache_02_gb300 import rkv
+    K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        rkv.rkv_compress(K, K.clone(), torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16), 16, 12)
+
+
+def test_product_path_does_not_touch_oracle():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "decode_kv_cache_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in src and "rkv_oracle" not in src, fn
