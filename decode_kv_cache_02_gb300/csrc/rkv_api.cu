@@ -334,6 +334,7 @@ const char* rkv_strerror(int code) {
         case RKV_ERR_ALIAS: return "outputs partially overlap inputs";
         case RKV_ERR_CUDA: return "CUDA launch or runtime error";
         case RKV_ERR_DEVICE: return "a kernel recorded an error";
+        case RKV_ERR_TOO_LARGE: return "request exceeds the static scratch of rkv_compress_noalloc";
         default: return "unknown error code";
     }
 }

@@ -25,8 +25,9 @@ RKV_MAX_TOKENS = 32768
 EXPORTED = [
     "rkv_workspace_size", "rkv_compress", "rkv_score", "rkv_select", "rkv_gather",
     "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
-    "rkv_timing_read", "rkv_kernel_name",
+    "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc",
 ]
+RKV_ERR_TOO_LARGE = 7
 
 
 class RkvError(RuntimeError):
@@ -82,6 +83,9 @@ def load(path: str | None = None):
         lib.rkv_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int64), i32, i32]
         lib.rkv_timing_read.restype = i32
+        lib.rkv_compress_noalloc.argtypes = [dp, vp, vp, vp, i32, i32, i32, f32, i32, f32, vp,
+                                             vp, vp, vp]
+        lib.rkv_compress_noalloc.restype = i32
         lib.rkv_kernel_name.argtypes = [i32]
         lib.rkv_kernel_name.restype = ctypes.c_char_p
         _lib = lib
@@ -171,6 +175,32 @@ def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: f
                              float(tau), out_K.data_ptr(), out_V.data_ptr(), out_idx.data_ptr(),
                              workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _check(rc, "rkv_compress")
+    return out_K, out_V, out_idx
+
+
+def rkv_compress_noalloc(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8,
+                         lam: float = 0.1, beta: int = 2, tau: float = 0.9, out_K=None,
+                         out_V=None, out_idx=None, stream=None):
+    """rkv_compress with the library's static scratch instead of a workspace,
+    for callers that may not allocate device memory while they run (pass
+    preallocated out_K / out_V / out_idx to allocate nothing at all).  Calls
+    that may overlap on the GPU share the scratch and must be serialised."""
+    for t, n in ((K, "K"), (V, "V"), (Q_obs, "Q_obs")):
+        _cuda(t, n)
+    if V.shape != K.shape or V.dtype != K.dtype or Q_obs.dtype != K.dtype or Q_obs.dim() != 4:
+        raise ValueError("K, V, Q_obs must share shape/dtype; Q_obs is [P, G, n_obs, d]")
+    desc = make_desc(K, Q_obs.shape[1])
+    if out_K is None:
+        out_K = torch.empty_like(K)
+    if out_V is None:
+        out_V = torch.empty_like(V)
+    if out_idx is None:
+        out_idx = torch.empty((K.shape[0], budget), dtype=torch.int32, device=K.device)
+    rc = load().rkv_compress_noalloc(ctypes.byref(desc), K.data_ptr(), V.data_ptr(),
+                                     Q_obs.data_ptr(), int(n_cached), int(budget), int(n_obs),
+                                     float(lam), int(beta), float(tau), out_K.data_ptr(),
+                                     out_V.data_ptr(), out_idx.data_ptr(), _stream_ptr(stream))
+    _check(rc, "rkv_compress_noalloc")
     return out_K, out_V, out_idx
 
 

@@ -67,7 +67,8 @@ enum {
     RKV_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small */
     RKV_ERR_ALIAS = 4,       /* outputs partially overlap inputs */
     RKV_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
-    RKV_ERR_DEVICE = 6       /* a kernel recorded an error (see status) */
+    RKV_ERR_DEVICE = 6,      /* a kernel recorded an error (see status) */
+    RKV_ERR_TOO_LARGE = 7    /* request exceeds rkv_compress_noalloc's scratch */
 };
 
 enum { RKV_DTYPE_BF16 = 0, RKV_DTYPE_FP32 = 1 };
@@ -134,6 +135,26 @@ int rkv_workspace_init(void* workspace, void* stream);
 /* Synchronises `stream`, returns the first error a kernel recorded in
  * `workspace` since the last call (RKV_OK if none) and clears it. */
 int rkv_get_device_status(void* workspace, void* stream);
+
+/* rkv_compress without a caller workspace.  The pages have no counterpart:
+ * this is a deployment convenience for callers that may not allocate device
+ * memory while they run (an engine plugin or custom op whose host framework
+ * owns all device memory, a process whose memory is reserved up front for the
+ * KV cache).  Same arguments, results and stream semantics as rkv_compress;
+ * the scratch is a static array of RKV_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads it until exit.  Requests whose
+ * rkv_workspace_size() exceeds it return RKV_ERR_TOO_LARGE before anything is
+ * enqueued (16 MiB holds the scratch of about one million token slots, e.g.
+ * one Llama-8B layer at batch 64 with N = 1152, or 240 problems of 4096).  Never allocates or frees device memory.
+ * The first call on each device, made with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that first
+ * call before any stream capture.  All calls share the array (its error word
+ * is cleared at the start of each call and not reported), so calls that may
+ * overlap on the GPU race and must be serialised by the caller. */
+#define RKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+int rkv_compress_noalloc(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                         int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                         void* out_K, void* out_V, int32_t* out_idx, void* stream);
 
 /* Human-readable name of an RKV_* code. */
 const char* rkv_strerror(int code);
