@@ -148,6 +148,7 @@ def work_model(w: wl.Workload) -> dict:
     return {
         "key_stats": {"bytes": k_bytes + 2 * P * N * 4},
         "importance": {"bytes": k_bytes + P * G * n_obs * d * es + P * N * 4},
+        "importance_tc": {"bytes": k_bytes + P * G * n_obs * d * es + P * N * 4},
         "gram_tc": {"flops": P * N * (N - 1) * d, "bytes": k_bytes + 3 * P * N * 4},
         "gram_simt": {"flops": 2 * P * N * N * d, "bytes": k_bytes + 3 * P * N * 4},
         "select": {"bytes": P * (N - n_obs) * 4 + P * B * 4},
@@ -402,8 +403,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-problems", type=int, default=0)
+    ap.add_argument("--problems", type=int, default=0,
+                    help="override the problem count (smaller copies for profiling; "
+                         "such a run is not the workload's bench line)")
     args = ap.parse_args()
     w = wl.BY_NAME[args.workload]
+    if args.problems:
+        w = w.scaled(layers=1, batch=1, kv_heads=args.problems)
     if args.impl == "reference":
         run_reference(args, w)
     else:

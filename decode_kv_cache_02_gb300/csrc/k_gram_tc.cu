@@ -48,9 +48,12 @@
 #include "../../include/rkv.h"
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
+#include "tcgen05.cuh"
 
 namespace rkv {
 namespace {
+
+using namespace tc;
 
 constexpr int kRows = 128;           // rows (and columns) of one Gram tile
 constexpr int kChunkElems = 64;      // bf16 elements per 128-byte swizzle row
@@ -59,7 +62,6 @@ constexpr int kMaxBlocks = 34;       // N <= 4352
 constexpr int kThreads = 192;        // producer warp, MMA warp, 4 epilogue warps
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz per wait
 
 template <int D>
 struct Cfg {
@@ -87,113 +89,8 @@ struct Params {
     DeviceStatus* status;
 };
 
-// ----------------------------------------------------------- PTX helpers --
-RKV_DEV uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-RKV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-RKV_DEV void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-RKV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-RKV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false on timeout or when
-// another role has already aborted.
-RKV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) return false;
-    }
-    return true;
-}
-RKV_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-RKV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-RKV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-RKV_DEV void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst)),
-                 "r"(ncols)
-                 : "memory");
-}
-RKV_DEV void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-RKV_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-RKV_DEV void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                      uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-RKV_DEV void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-RKV_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
-        "[%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-RKV_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: 8-row groups 1024 bytes apart (stride byte offset), rows
-// of 128 bytes.  The tile base must be 1024-byte aligned; advancing the start
-// address by 32 bytes selects the next 16-element K slice.
-RKV_DEV uint64_t sdesc_sw128(const void* p) {
-    const uint64_t a = smem_u32(p);
-    uint64_t d = (a >> 4) & 0x3FFFull;   // start address
-    d |= 1ull << 16;                      // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;     // stride byte offset
-    d |= 1ull << 46;                      // descriptor version
-    d |= 2ull << 61;                      // 128-byte swizzle
-    return d;
-}
-
 // Instruction descriptor: D fp32, A and B bf16, both K-major, M = N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRows >> 3) << 17) |
-                            ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdesc = tc::idesc_bf16(kRows, kRows);
 
 // ---------------------------------------------------------------- kernel --
 template <int D>
@@ -444,54 +341,20 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
 }
 
 // ------------------------------------------------------------------ host --
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        n = 148;
-    return n;
-}
-
 template <int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D>;
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.N, (cuuint64_t)a.P};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.n_cap * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kChunkElems, (cuuint32_t)kRows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.K), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (!make_map_3d_bf16(&map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
+        return cudaErrorInvalidValue;
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,
                a.sum_s,  a.ld_ws, a.I,       a.R,    a.Z,      a.ld_out, a.status};
     auto kern = gram_tc_kernel<D>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t grid = a.P < sm_count() ? a.P : sm_count();
+    const int64_t sms = sm_count();
+    const int64_t grid = a.P < sms ? a.P : sms;
     kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(map, prm);
     return cudaGetLastError();
 }

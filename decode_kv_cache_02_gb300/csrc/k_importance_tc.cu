@@ -1,0 +1,386 @@
+// k_importance_tc.cu -- attention importance on the sm_103a tensor cores.
+//
+// R-KV review (yoonschallenge.tistory.com/1236), summary-table row
+// "importance": the attention the recent observation queries give each past
+// key, max-pooled over the query heads of a GQA group.  With R = G * n_obs
+// query rows (g, q) per problem:
+//     l_{c,j} = (q_c . k_j) / sqrt(d)          c = g*n_obs + q, j <= N - n_obs + q
+//     I_j     = max_g (1/n_obs) sum_q softmax_j(l_{c,.})
+//
+// The logits of a block of 128 keys are one tcgen05.mma chain: A = the key
+// block (M = 128, K-major bf16 from TMA), B = the problem's query rows padded
+// to RP (N = RP, rows >= R zero-filled by TMA), fp32 accumulators in TMEM.
+// One epilogue thread owns one key row of the block.  Two passes over the
+// problem's keys (the second is expected to hit L2):
+//   pass 1  per-thread online (max, sum of exp) per query row, then a block
+//           reduction (warp shuffles + shared memory) to the row's max M_c and
+//           1 / sum_j exp(l - M_c);
+//   pass 2  p = exp(l - M_c) / S_c, mean over q, max over g -> I_j.
+// Warp 0 (one lane) issues the TMA loads, warp 1 owns TMEM and one lane issues
+// the MMAs, warps 2..5 are the epilogue; one persistent CTA per SM, with a
+// five-stage ring of key blocks so the next problem's keys stream in while
+// the epilogue reduces.  All waits are bounded.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rkv.h"
+#include "rkv_common.cuh"
+#include "rkv_internal.h"
+#include "tcgen05.cuh"
+
+namespace rkv {
+namespace {
+
+using namespace tc;
+
+constexpr int kRows = 128;
+constexpr int kChunkElems = 64;
+constexpr int kChunkBytes = kRows * 128;
+constexpr int kThreads = 192;
+constexpr int kEpi = 128;
+constexpr int kAcc = 4;            // accumulators in flight
+constexpr int kAccCols = 64;       // TMEM columns per accumulator
+constexpr uint32_t kTmemCols = 256;
+constexpr int kMaxQueryRows = 48;  // G * n_obs handled here
+
+template <int D, int RP>
+struct ICfg {
+    static constexpr int KC = D / kChunkElems;
+    static constexpr int kBlockBytes = KC * kChunkBytes;
+    static constexpr int kQChunkBytes = RP * 128;
+    static constexpr int kStages = D == 128 ? 5 : 10;
+    static constexpr size_t kQOff = (size_t)kStages * kBlockBytes;
+    static constexpr size_t kRedOff = kQOff + (size_t)KC * kQChunkBytes;
+    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 8 * RP;
+    static constexpr int kNumBars = 2 * kStages + 2 + 2 * kAcc + 2;
+    static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
+};
+
+constexpr int kMaxObs = kMaxQueryRows;
+
+struct IParams {
+    int64_t P;
+    int N, n_obs, G;
+    float scale;
+    float* I;
+    int64_t ld;
+    DeviceStatus* status;
+    // bit c of colmask[k]: query row c exists and its query index c % n_obs
+    // is >= k (so it sees a key k positions past N - n_obs); bit c of
+    // lastmask: c is the last query row of its head.
+    unsigned long long colmask[kMaxObs + 1];
+    unsigned long long lastmask;
+};
+
+RKV_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+template <int D, int RP>
+__global__ void __launch_bounds__(kThreads, 1)
+importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap qmap, const IParams prm) {
+    using C = ICfg<D, RP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sK = smem;
+    uint8_t* sQ = smem + C::kQOff;
+    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [4][RP]
+    float* redS = redM + 4 * RP;                                 // [4][RP]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = k_full + C::kStages;
+    uint64_t* q_full = k_empty + C::kStages;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* acc_full = q_empty + 1;
+    uint64_t* acc_empty = acc_full + kAcc;
+    uint64_t* epi_bar = acc_empty + kAcc;
+    uint64_t* drain_bar = epi_bar + 1;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    __shared__ unsigned long long s_colmask[kMaxObs + 1];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = prm.N, n_obs = prm.n_obs;
+    for (int k = threadIdx.x; k <= n_obs && k <= kMaxObs; k += blockDim.x) s_colmask[k] = prm.colmask[k];
+    const int T = (N + kRows - 1) / kRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int a = 0; a < kAcc; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], kEpi);
+        }
+        mbar_init(epi_bar, kEpi);
+        mbar_init(drain_bar, 1);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t kk = 0, kq = 0;
+            bool ok = true;
+            for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+                if (!(ok = mbar_wait(q_empty, (kq & 1) ^ 1, s_abort))) break;
+                mbar_arrive_expect_tx(q_full, C::KC * C::kQChunkBytes);
+                for (int c = 0; c < C::KC; ++c)
+                    tma_load_3d(sQ + c * C::kQChunkBytes, &qmap, q_full, c * kChunkElems, 0, (int)p);
+                ++kq;
+                for (int pass = 0; ok && pass < 2; ++pass) {
+                    for (int b = 0; b < T; ++b) {
+                        const int s = kk % C::kStages;
+                        if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort)))
+                            break;
+                        mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
+                        for (int c = 0; c < C::KC; ++c)
+                            tma_load_3d(sK + s * C::kBlockBytes + c * kChunkBytes, &kmap, &k_full[s],
+                                        c * kChunkElems, b * kRows, (int)p);
+                        ++kk;
+                    }
+                }
+            }
+            if (!ok) {
+                *s_abort = 1;
+                set_error(prm.status, kDevErrTimeout, 11u);
+                volatile int never = 0;
+                for (uint32_t u = kk > (uint32_t)C::kStages ? kk - C::kStages : 0; u < kk; ++u)
+                    mbar_wait(&k_full[u % C::kStages], (u / C::kStages) & 1, &never);
+                if (kq > 0) mbar_wait(q_full, (kq - 1) & 1, &never);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kRows, RP);
+            uint32_t kk = 0, kq = 0, ka = 0;
+            bool ok = true;
+            for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+                if (!(ok = mbar_wait(q_full, kq & 1, s_abort))) break;
+                for (int pass = 0; ok && pass < 2; ++pass) {
+                    for (int b = 0; b < T; ++b) {
+                        const int s = kk % C::kStages;
+                        if (!(ok = mbar_wait(&k_full[s], (kk / C::kStages) & 1, s_abort))) break;
+                        const int a = ka % kAcc;
+                        if (!(ok = mbar_wait(&acc_empty[a], ((ka / kAcc) & 1) ^ 1, s_abort))) break;
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem + (uint32_t)(a * kAccCols);
+#pragma unroll
+                        for (int c = 0; c < C::KC; ++c) {
+                            const uint64_t ad = sdesc_sw128(sK + s * C::kBlockBytes + c * kChunkBytes);
+                            const uint64_t bd = sdesc_sw128(sQ + c * C::kQChunkBytes);
+#pragma unroll
+                            for (int k = 0; k < kChunkElems / 16; ++k)
+                                mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (c | k) != 0);
+                        }
+                        mma_commit(&acc_full[a]);
+                        mma_commit(&k_empty[s]);
+                        ++kk;
+                        ++ka;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(q_empty);
+                ++kq;
+            }
+            if (!ok) {
+                *s_abort = 1;
+                set_error(prm.status, kDevErrTimeout, 12u);
+            }
+            mma_commit(drain_bar);
+            volatile int never = 0;
+            mbar_wait(drain_bar, 0, &never);
+        }
+    } else {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
+        const int lim = N - n_obs;  // key j is seen by query q iff j <= lim + q
+        const float inv_nobs = 1.0f / (float)n_obs;
+        const unsigned long long lastmask = prm.lastmask;
+        uint32_t ka = 0, ke = 0;
+        bool ok = true;
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+            float m[RP], s[RP];
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                m[c] = -INFINITY;
+                s[c] = 0.f;
+            }
+            // ---- pass 1: online max / sum of exp per query row
+            for (int b = 0; b < T; ++b) {
+                const int a = ka % kAcc;
+                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (ka / kAcc) & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                const int j = b * kRows + row;
+                const unsigned long long vm =
+                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+#pragma unroll
+                for (int cc = 0; cc < RP / 16; ++cc) {
+                    uint32_t r[16];
+                    tmem_ld_16cols(t_row + (uint32_t)(a * kAccCols + cc * 16), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = cc * 16 + e;
+                        if ((vm >> c) & 1ull) {
+                            const float l = __uint_as_float(r[e]) * prm.scale;
+                            const float mn = fmaxf(m[c], l);
+                            s[c] = s[c] * __expf(m[c] - mn) + __expf(l - mn);
+                            m[c] = mn;
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[a]);
+                ++ka;
+            }
+            if (!ok) break;
+            // ---- block reduction: row max, then the rescaled sums
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                const float mx = warp_max(m[c]);
+                if (lane == 0) redM[qd * RP + c] = mx;
+            }
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                const float M = fmaxf(fmaxf(redM[c], redM[RP + c]), fmaxf(redM[2 * RP + c], redM[3 * RP + c]));
+                const float part = (m[c] == -INFINITY) ? 0.f : s[c] * __expf(m[c] - M);
+                const float ws = warp_sum(part);
+                if (lane == 0) redS[qd * RP + c] = ws;
+                m[c] = M;
+            }
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+#pragma unroll
+            for (int c = 0; c < RP; ++c)
+                s[c] = 1.0f / ((redS[c] + redS[RP + c]) + (redS[2 * RP + c] + redS[3 * RP + c]));
+            // ---- pass 2: probabilities -> importance
+            for (int b = 0; b < T; ++b) {
+                const int a = ka % kAcc;
+                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (ka / kAcc) & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                const int j = b * kRows + row;
+                const unsigned long long vm =
+                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                float best = -INFINITY, acc = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < RP / 16; ++cc) {
+                    uint32_t r[16];
+                    tmem_ld_16cols(t_row + (uint32_t)(a * kAccCols + cc * 16), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = cc * 16 + e;
+                        if ((vm >> c) & 1ull) {
+                            const float l = __uint_as_float(r[e]) * prm.scale;
+                            acc += __expf(l - m[c]) * s[c];
+                        }
+                        if ((lastmask >> c) & 1ull) {  // last query row of a head
+                            best = fmaxf(best, acc * inv_nobs);
+                            acc = 0.f;
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[a]);
+                ++ka;
+                if (j < N) prm.I[p * prm.ld + j] = best;
+            }
+        }
+        if (!ok) {
+            *s_abort = 1;
+            set_error(prm.status, kDevErrTimeout, 13u);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D, int RP>
+cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
+    using C = ICfg<D, RP>;
+    CUtensorMap kmap, qmap;
+    const int R = a.G * a.n_obs;
+    if (!make_map_3d_bf16(&kmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
+        return cudaErrorInvalidValue;
+    if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, RP))
+        return cudaErrorInvalidValue;
+    IParams prm{};
+    prm.P = a.P;
+    prm.N = a.N;
+    prm.n_obs = a.n_obs;
+    prm.G = a.G;
+    prm.scale = 1.0f / sqrtf((float)D);
+    prm.I = a.I;
+    prm.ld = a.ld_out;
+    prm.status = a.status;
+    for (int k = 0; k <= a.n_obs && k <= kMaxObs; ++k) {
+        unsigned long long m = 0;
+        for (int c = 0; c < R; ++c)
+            if (c % a.n_obs >= k) m |= 1ull << c;
+        prm.colmask[k] = m;
+    }
+    for (int c = 0; c < R; ++c)
+        if (c % a.n_obs == a.n_obs - 1) prm.lastmask |= 1ull << c;
+    auto kern = importance_tc_kernel<D, RP>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = (int64_t)sm_count();
+    const int64_t grid = a.P < cap ? a.P : cap;
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(kmap, qmap, prm);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const ScoreArgs& a, cudaStream_t s) {
+    const int R = a.G * a.n_obs;
+    if (R <= 32) return launch_t<D, 32>(a, s);
+    return launch_t<D, 48>(a, s);
+}
+
+}  // namespace
+
+bool importance_tc_supported(const ScoreArgs& a) {
+    return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.G * a.n_obs <= kMaxQueryRows &&
+           a.N >= 2 && a.P <= 0x7fffffff && encode_fn() != nullptr;
+}
+
+cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s) {
+    if (a.P == 0) return cudaSuccess;
+    return a.d == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
+}
+
+}  // namespace rkv

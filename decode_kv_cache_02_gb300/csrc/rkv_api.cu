@@ -4,7 +4,7 @@
 // One compression round (R-KV review, yoonschallenge.tistory.com/1236,
 // question 2, cause 3, in the page's order):
 //   key statistics (norms, plain similarity sums)      k_key_stats.cu
-//   attention importance                                k_importance.cu
+//   attention importance                                k_importance_tc.cu / k_importance.cu
 //   thresholded Gram -> redundancy, protection, R, Z    k_gram_tc.cu / k_gram_simt.cu
 //   top-k selection                                     k_select.cu
 //   copy of the kept K/V rows                           k_gather.cu
@@ -28,6 +28,7 @@ using rkv::ScoreArgs;
 enum KernelId {
     kKeyStats = 0,
     kImportance,
+    kImportanceTc,
     kGramTc,
     kGramSimt,
     kSelect,
@@ -36,7 +37,8 @@ enum KernelId {
     kNumKernels
 };
 const char* const kKernelNames[kNumKernels] = {
-    "key_stats", "importance", "gram_tc", "gram_simt", "select", "gather", "identity_idx"};
+    "key_stats", "importance", "importance_tc", "gram_tc", "gram_simt", "select", "gather",
+    "identity_idx"};
 
 // ---------------------------------------------------------------- timing --
 struct TimedLaunch {
@@ -172,7 +174,12 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.ld_out = ld_out;
     a.status = w.status;
     cudaError_t e = timed(kKeyStats, s, [&] { return rkv::launch_key_stats(a, s); });
-    if (e == cudaSuccess) e = timed(kImportance, s, [&] { return rkv::launch_importance(a, s); });
+    if (e == cudaSuccess) {
+        if (rkv::importance_tc_supported(a))
+            e = timed(kImportanceTc, s, [&] { return rkv::launch_importance_tc(a, s); });
+        else
+            e = timed(kImportance, s, [&] { return rkv::launch_importance(a, s); });
+    }
     if (e == cudaSuccess) {
         if (rkv::gram_tc_supported(a))
             e = timed(kGramTc, s, [&] { return rkv::launch_gram_tc(a, s); });

@@ -30,6 +30,8 @@ struct ScoreArgs {
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_importance(const ScoreArgs& a, cudaStream_t s);
+bool importance_tc_supported(const ScoreArgs& a);
+cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_gram_simt(const ScoreArgs& a, cudaStream_t s);
 bool gram_tc_supported(const ScoreArgs& a);
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);

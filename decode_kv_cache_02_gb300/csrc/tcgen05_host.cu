@@ -1,0 +1,48 @@
+// tcgen05_host.cu -- host helpers of the tensor-core kernels: the driver's
+// tensor-map encoder (looked up at run time) and the SM count.
+#include <mutex>
+
+#include "tcgen05.cuh"
+
+namespace rkv {
+namespace tc {
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool make_map_3d_bf16(CUtensorMap* map, const void* base, int inner, int rows, int64_t outer,
+                      int64_t row_stride_elems, int64_t outer_stride_elems, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows < 1 || outer < 1) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_stride_elems * 2,
+                                   (cuuint64_t)outer_stride_elems * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+}  // namespace tc
+}  // namespace rkv
