@@ -22,28 +22,36 @@
 //   * The problem's keys are cut into T = ceil(N/128) row blocks of 128.  Only
 //     the upper-triangular block pairs (I, J >= I) are multiplied: S is
 //     symmetric, so a pair found in block (I, J), J > I, counts for row i
-//     directly and for row j through a shared-memory atomic (rare: only
-//     similar pairs).  newer_j never changes there because i < j.
+//     directly and for row j through a warp reduce-scatter of the sub-tile's
+//     columns and one shared-memory atomic per column (only in sub-tiles that
+//     hold a similar pair).  newer_j never changes there because i < j.
 //   * warp 0, one lane: TMA producer.  Block I (the A operand, 2 slots) and
 //     blocks J > I (the B operand, a ring of stages) are fetched with
 //     cp.async.bulk.tensor (3-D map [P][N][d], 128B swizzle, rows past N
-//     zero-filled).  No multicast.
-//   * warp 1: owns 256 TMEM columns (two 128x128 fp32 accumulators); one lane
-//     issues tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32, M = N =
-//     128, K = 16 per instruction, exact products) and tcgen05.commit.
-//   * warps 2..5 (128 threads, one per accumulator row / TMEM lane): the
-//     epilogue.  tcgen05.ld brings 32 columns at a time into registers;
-//     t = acc * inv_j, and a warp-wide max test skips the 32x32 sub-tile unless
-//     some t exceeds tau / inv_i.  Diagonal blocks take the exact path for
-//     every element (self-pair excluded).
+//     zero-filled); the problem's inverse norms arrive by cp.async.bulk into a
+//     double buffer one problem ahead.  No multicast.
+//   * warp 1: owns all 512 TMEM columns (four 128x128 fp32 accumulators); one
+//     lane issues tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
+//     M = N = 128, K = 16 per instruction, exact products) and tcgen05.commit.
+//   * warps 2..9 (256 threads): the epilogue.  Warp w reads TMEM lanes
+//     32*(w%4).. (one accumulator row per thread) and one half of the 128
+//     columns: two tcgen05.ld of 32 columns in flight, then a filter per 32x32
+//     sub-tile -- the largest raw accumulator (an integer max over the bits,
+//     valid for positive floats) times the largest inverse norm of the 32
+//     columns -- skips the sub-tile unless some S could exceed tau (in
+//     diagonal blocks the row's own column is left out of that maximum).  The
+//     exact path is branch-free: a per-lane hit mask, row sums in registers,
+//     popc for the newer count.
+//   * Row-side partials (sum of above-tau S, count of newer similar tokens)
+//     of the two column halves meet in shared memory through atomics; the
+//     count is kept as one saturating byte per row (exact for beta <= 127), so
+//     R and Z are written once per problem, with no barrier per row block.
 //   * Every mbarrier wait is bounded; on timeout the kernel records
 //     kDevErrTimeout in the device status, stops issuing work, waits (bounded)
 //     for its own copies and MMAs in flight, frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "../../include/rkv.h"
 #include "rkv_common.cuh"
@@ -55,13 +63,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRows = 128;           // rows (and columns) of one Gram tile
-constexpr int kChunkElems = 64;      // bf16 elements per 128-byte swizzle row
+constexpr int kRows = 128;                // rows (and columns) of one Gram tile
+constexpr int kChunkElems = 64;           // bf16 elements per 128-byte swizzle row
 constexpr int kChunkBytes = kRows * 128;  // one [128 x 64] bf16 TMA box
-constexpr int kMaxBlocks = 34;       // N <= 4352
-constexpr int kThreads = 192;        // producer warp, MMA warp, 4 epilogue warps
-constexpr int kEpiThreads = 128;
-constexpr uint32_t kTmemCols = 256;  // two 128-column fp32 accumulators
+constexpr int kMaxBlocks = 34;            // N <= 4352
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
+constexpr int kAccBufs = 4;
+constexpr uint32_t kTmemCols = kAccBufs * kRows;  // 512: all of TMEM
+constexpr int kInvFloats = kMaxBlocks * kRows;
 
 template <int D>
 struct Cfg {
@@ -69,9 +80,12 @@ struct Cfg {
     static constexpr int kBlockBytes = KC * kChunkBytes;
     static constexpr int kAStages = 2;
     static constexpr int kBStages = D == 128 ? 3 : 6;
-    static constexpr size_t kBarOff = (size_t)(kAStages + kBStages) * kBlockBytes +
-                                      2 * (size_t)kMaxBlocks * kRows * sizeof(float);
-    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 4 + 2;
+    static constexpr size_t kInvOff = (size_t)(kAStages + kBStages) * kBlockBytes;
+    static constexpr size_t kSimOff = kInvOff + 2 * sizeof(float) * kInvFloats;
+    static constexpr size_t kNewerOff = kSimOff + sizeof(float) * kInvFloats;
+    static constexpr size_t kInvMaxOff = kNewerOff + kInvFloats;  // one byte per row
+    static constexpr size_t kBarOff = kInvMaxOff + 2 * sizeof(float) * kMaxBlocks * 4;
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kAccBufs + 4 + 2;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
 };
 
@@ -89,8 +103,46 @@ struct Params {
     DeviceStatus* status;
 };
 
-// Instruction descriptor: D fp32, A and B bf16, both K-major, M = N = 128.
-constexpr uint32_t kIdesc = tc::idesc_bf16(kRows, kRows);
+constexpr uint32_t kIdesc = idesc_bf16(kRows, kRows);
+
+// Fixed-point scale of the shared-memory similarity sums (integer atomics are
+// native in shared memory): a similarity is stored in units of 2^-18, so a row
+// sum of up to 4352 similarities fits in 31 bits and each addition rounds by
+// at most 2^-19.
+constexpr float kSimScale = 262144.0f;
+
+// Reduce-scatter over the warp: on return, lane L holds in v[0] the sum over
+// all lanes of their v[L].
+RKV_DEV float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float send = upper ? v[k] : v[k + w];
+            const float keep = upper ? v[k + w] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return v[0];
+}
+
+RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Largest of 32 raw fp32 accumulators compared as signed integers: exact for
+// the positive ones, and <= 0 when none is positive.
+RKV_DEV int raw_max32(const uint32_t (&r)[32]) {
+    int m = __vimax3_s32((int)r[0], (int)r[1], (int)r[2]);
+#pragma unroll
+    for (int e = 3; e < 31; e += 2) m = __vimax3_s32(m, (int)r[e], (int)r[e + 1]);
+    return max(m, (int)r[31]);
+}
 
 // ---------------------------------------------------------------- kernel --
 template <int D>
@@ -102,23 +154,30 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + C::kAStages * C::kBlockBytes;
-    float* s_inv = reinterpret_cast<float*>(sB + C::kBStages * C::kBlockBytes);
-    float* s_sim = s_inv + kMaxBlocks * kRows;
+    float* s_inv = reinterpret_cast<float*>(smem + C::kInvOff);        // [2][kInvFloats]
+    // above-tau similarity sums per row, fixed point (kSimScale units)
+    int* s_sim = reinterpret_cast<int*>(smem + C::kSimOff);            // [kInvFloats]
+    // newer-similar counts, one saturating byte per row, four rows per word
+    unsigned int* s_newer = reinterpret_cast<unsigned int*>(smem + C::kNewerOff);
+    float* s_invmax = reinterpret_cast<float*>(smem + C::kInvMaxOff);  // [2][kMaxBlocks*4]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* a_full = bars;
     uint64_t* a_empty = a_full + C::kAStages;
     uint64_t* b_full = a_empty + C::kAStages;
     uint64_t* b_empty = b_full + C::kBStages;
     uint64_t* acc_full = b_empty + C::kBStages;
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* epi_bar = acc_empty + 2;   // 128 epilogue threads meet here
-    uint64_t* drain_bar = epi_bar + 1;   // MMA completion at exit
+    uint64_t* acc_empty = acc_full + kAccBufs;
+    uint64_t* inv_full = acc_empty + kAccBufs;  // [2]
+    uint64_t* inv_empty = inv_full + 2;         // [2]
+    uint64_t* epi_bar = inv_empty + 2;
+    uint64_t* drain_bar = epi_bar + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N;
     const int T = (N + kRows - 1) / kRows;
+    const uint32_t inv_bytes = (uint32_t)((N + 3) / 4) * 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kAStages; ++s) {
@@ -129,9 +188,13 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
             mbar_init(&b_full[s], 1);
             mbar_init(&b_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kAccBufs; ++s) {
             mbar_init(&acc_full[s], 1);
             mbar_init(&acc_empty[s], kEpiThreads);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&inv_full[s], 1);
+            mbar_init(&inv_empty[s], kEpiThreads);
         }
         mbar_init(epi_bar, kEpiThreads);
         mbar_init(drain_bar, 1);
@@ -152,8 +215,15 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
     if (warp == 0) {
         // ------------------------------------------------------ producer --
         if (lane == 0) {
-            uint32_t ka = 0, kb = 0;
+            uint32_t ka = 0, kb = 0, kinv = 0;
             bool ok = true;
+            // inverse norms of the first problem
+            if (blockIdx.x < prm.P) {
+                mbar_arrive_expect_tx(&inv_full[0], inv_bytes);
+                bulk_copy_g2s(s_inv, prm.inv_norm + (int64_t)blockIdx.x * prm.ld_ws, inv_bytes,
+                              &inv_full[0]);
+                kinv = 1;
+            }
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
                 for (int I = 0; ok && I < T; ++I) {
                     const int sa = ka % C::kAStages;
@@ -174,18 +244,30 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                                         &b_full[sb], c * kChunkElems, J * kRows, (int)p);
                         ++kb;
                     }
+                    if (ok && I == 0 && p + gridDim.x < prm.P) {
+                        // inverse norms of the next problem into the other buffer
+                        const int ib = kinv & 1;
+                        if (!(ok = mbar_wait(&inv_empty[ib], ((kinv >> 1) & 1) ^ 1, s_abort))) break;
+                        mbar_arrive_expect_tx(&inv_full[ib], inv_bytes);
+                        bulk_copy_g2s(s_inv + ib * kInvFloats,
+                                      prm.inv_norm + (p + gridDim.x) * prm.ld_ws, inv_bytes,
+                                      &inv_full[ib]);
+                        ++kinv;
+                    }
                 }
             }
             if (!ok) {
                 *s_abort = 1;
                 set_error(prm.status, kDevErrTimeout, 1u);
-                // let the copies already issued land before the CTA exits
-                volatile int never = 0;
-                for (uint32_t u = ka > (uint32_t)C::kAStages ? ka - C::kAStages : 0; u < ka; ++u)
-                    mbar_wait(&a_full[u % C::kAStages], (u / C::kAStages) & 1, &never);
-                for (uint32_t u = kb > (uint32_t)C::kBStages ? kb - C::kBStages : 0; u < kb; ++u)
-                    mbar_wait(&b_full[u % C::kBStages], (u / C::kBStages) & 1, &never);
             }
+            // every copy issued has landed before the CTA may exit
+            volatile int never = 0;
+            for (uint32_t u = ka > (uint32_t)C::kAStages ? ka - C::kAStages : 0; u < ka; ++u)
+                mbar_wait(&a_full[u % C::kAStages], (u / C::kAStages) & 1, &never);
+            for (uint32_t u = kb > (uint32_t)C::kBStages ? kb - C::kBStages : 0; u < kb; ++u)
+                mbar_wait(&b_full[u % C::kBStages], (u / C::kBStages) & 1, &never);
+            for (uint32_t u = kinv > 2u ? kinv - 2 : 0; u < kinv; ++u)
+                mbar_wait(&inv_full[u & 1], (u >> 1) & 1, &never);
         }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer --
@@ -206,8 +288,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                                 break;
                             b_base = sB + sb * C::kBlockBytes;
                         }
-                        const int acc = kacc & 1;
-                        if (!(ok = mbar_wait(&acc_empty[acc], ((kacc >> 1) & 1) ^ 1, s_abort)))
+                        const int acc = kacc % kAccBufs;
+                        if (!(ok = mbar_wait(&acc_empty[acc], ((kacc / kAccBufs) & 1) ^ 1, s_abort)))
                             break;
                         tc_fence_after();
                         const uint32_t d_tmem = tmem + (uint32_t)(acc * kRows);
@@ -242,91 +324,153 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         }
     } else {
         // ------------------------------------------------------- epilogue --
-        const int et = threadIdx.x - 64;      // 0..127
+        const int et = threadIdx.x - 64;      // 0..255
         const int q = warp & 3;               // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;     // which 64 of the 128 columns
         const int row = q * 32 + lane;        // accumulator row of this thread
-        const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+        const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
         const int Cn = N - prm.n_obs;
         const float inv_nm1 = 1.0f / (float)(N - 1);
-        uint32_t kacc = 0, kepi = 0;
+        uint32_t kacc = 0, kepi = 0, kinv = 0;
         bool ok = true;
+        for (int x = et; x < kInvFloats; x += kEpiThreads) s_sim[x] = 0;
+        for (int x = et; x < kInvFloats / 4; x += kEpiThreads) s_newer[x] = 0u;
         for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
-            const float* invp = prm.inv_norm + p * prm.ld_ws;
-            for (int x = et; x < T * kRows; x += kEpiThreads) {
-                s_inv[x] = x < N ? invp[x] : 0.f;
-                s_sim[x] = 0.f;
+            const int ib = kinv & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&inv_full[ib], (kinv >> 1) & 1, s_abort));
+            if (!ok) break;
+            const float* inv = s_inv + ib * kInvFloats;
+            float* invmax = s_invmax + ib * kMaxBlocks * 4;
+            for (int x = et; x < T * 4; x += kEpiThreads) {
+                float m = -INFINITY;
+                const int j_end = min(N, (x + 1) * 32);
+                for (int j = x * 32; j < j_end; ++j) m = fmaxf(m, inv[j]);
+                invmax[x] = m;
             }
+            // the previous problem's s_sim / s_newer entries are zero again
             mbar_arrive(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
             ++kepi;
             for (int I = 0; ok && I < T; ++I) {
                 const int i = I * kRows + row;
                 const bool valid_i = i < N;
-                const float inv_i = valid_i ? s_inv[i] : 0.f;
+                const float inv_i = valid_i ? inv[i] : 0.f;
                 const float thr = valid_i ? prm.tau / inv_i : INFINITY;
+                const bool thr_pos = thr > 0.f;
                 float sim_row = 0.f;
                 int newer = 0;
                 for (int J = I; J < T; ++J) {
-                    const int acc = kacc & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (kacc >> 1) & 1, s_abort));
+                    const int acc = kacc % kAccBufs;
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&acc_full[acc], (kacc / kAccBufs) & 1, s_abort));
                     if (!ok) break;
                     tc_fence_after();
                     const bool diag = (J == I);
-#pragma unroll 1
-                    for (int c = 0; c < kRows / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32cols(t_row + (uint32_t)(acc * kRows + c * 32), r);
-                        tmem_ld_wait();
-                        const float* ij = s_inv + J * kRows + c * 32;
-                        float t[32];
-                        float m = -INFINITY;
+                    uint32_t r[2][32];
+                    tmem_ld_32cols(t_row + (uint32_t)(acc * kRows), r[0]);
+                    tmem_ld_32cols(t_row + (uint32_t)(acc * kRows + 32), r[1]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(&acc_empty[acc]);  // the accumulator is in registers now
+                    ++kacc;
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            t[e] = __uint_as_float(r[e]) * ij[e];
-                            m = fmaxf(m, t[e]);
+                    for (int h = 0; h < 2; ++h) {
+                        const int chunk = J * 4 + half * 2 + h;  // 32-column chunk of the problem
+                        const int jb = chunk * 32;
+                        // column e of this chunk is the row itself (diagonal blocks)
+                        const int e_self = diag ? i - jb : -1;
+                        bool hot = !thr_pos;
+                        if (!hot) {
+                            int mb;
+                            if (diag) {
+                                uint32_t m[32];
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) m[e] = e == e_self ? 0u : r[h][e];
+                                mb = raw_max32(m);
+                            } else {
+                                mb = raw_max32(r[h]);
+                            }
+                            hot = mb > 0 && __int_as_float(mb) * invmax[chunk] > thr;
                         }
-                        if (__any_sync(0xffffffffu, diag || m > thr)) {
-                            const int jb = J * kRows + c * 32;
+                        if (__any_sync(0xffffffffu, hot)) {
+                            // exact path: S_ij > tau for the columns that exist
+                            const int e_end = min(32, N - jb);
+                            const float4* iv4 = reinterpret_cast<const float4*>(inv + jb);
+                            float v[32];
+                            uint32_t hits = 0;
+                            float row_sum = 0.f;
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                const int j = jb + e;
-                                if (t[e] > thr && j < N && j != i) {
-                                    const float s = t[e] * inv_i;
-                                    sim_row += s;
-                                    newer += (j > i);
-                                    if (!diag) atomicAdd(&s_sim[j], s);
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 w4 = iv4[e4];
+                                const float iv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int e = e4 * 4 + u;
+                                    const float t = __uint_as_float(r[h][e]) * iv[u];
+                                    const bool hit = (t > thr) && (e < e_end) && (e != e_self);
+                                    v[e] = hit ? t * inv_i : 0.f;
+                                    row_sum += v[e];
+                                    hits |= (hit ? 1u : 0u) << e;
                                 }
+                            }
+                            sim_row += row_sum;
+                            // newer similar tokens: every column of a block right
+                            // of the diagonal, and columns past the row itself
+                            const uint32_t newer_mask =
+                                !diag ? 0xffffffffu
+                                      : (e_self >= 31 ? 0u
+                                                      : (e_self < 0 ? 0xffffffffu
+                                                                    : (0xffffffffu << (e_self + 1))));
+                            newer += __popc(hits & newer_mask);
+                            if (!diag) {
+                                // column side: lane L adds column jb+L over the warp's rows
+                                const float cs = warp_column_sums(v, lane);
+                                if (cs != 0.f) atomicAdd(&s_sim[jb + lane], __float2int_rn(cs * kSimScale));
                             }
                         }
                     }
-                    tc_fence_before();
-                    mbar_arrive(&acc_empty[acc]);
-                    ++kacc;
                 }
                 if (!ok) break;
-                // all column contributions to block I are in s_sim now
-                mbar_arrive(epi_bar);
-                ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
-                ++kepi;
-                if (!ok) break;
+                // row-side partials of this half (newer saturated so that the
+                // two halves' bytes cannot carry into the next row)
                 if (valid_i) {
-                    const float sim_i = s_sim[i] + sim_row;
-                    float rr = 0.f, z = INFINITY;
-                    if (i < Cn) {
-                        const float tot = prm.sum_s[p * prm.ld_ws + i];
-                        rr = (tot - (newer < prm.beta ? sim_i : 0.f)) * inv_nm1;
-                        z = prm.lambda * prm.I[p * prm.ld_out + i] - (1.0f - prm.lambda) * rr;
-                    }
-                    if (prm.R) prm.R[p * prm.ld_out + i] = rr;
-                    prm.Z[p * prm.ld_out + i] = z;
+                    if (sim_row != 0.f) atomicAdd(&s_sim[i], __float2int_rn(sim_row * kSimScale));
+                    if (newer != 0)
+                        atomicAdd(&s_newer[i >> 2], (unsigned)min(newer, 127) << (8 * (i & 3)));
                 }
             }
             if (!ok) break;
-            // s_inv / s_sim are reset for the next problem only after every
-            // thread has read them
+            mbar_arrive(&inv_empty[ib]);
+            ++kinv;
+            // every contribution to this problem is in shared memory after this
             mbar_arrive(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
             ++kepi;
+            if (!ok) break;
+            // finalize this thread's rows, then clear exactly what it read
+            for (int i = et; i < N; i += kEpiThreads) {
+                float tot = 0.f, imp = 0.f;
+                if (i < Cn) {
+                    tot = prm.sum_s[p * prm.ld_ws + i];
+                    imp = prm.I[p * prm.ld_out + i];
+                }
+                const float sim_i = (float)s_sim[i] * (1.0f / kSimScale);
+                const int nw = (int)((s_newer[i >> 2] >> (8 * (i & 3))) & 0xffu);
+                float rr = 0.f, z = INFINITY;
+                if (i < Cn) {
+                    rr = (tot - (nw < prm.beta ? sim_i : 0.f)) * inv_nm1;
+                    z = prm.lambda * imp - (1.0f - prm.lambda) * rr;
+                }
+                if (prm.R) prm.R[p * prm.ld_out + i] = rr;
+                prm.Z[p * prm.ld_out + i] = z;
+                s_sim[i] = 0;
+            }
+            // a word of s_newer holds rows 4w..4w+3, finalized by four
+            // neighbouring lanes of one warp; the first of them clears it once
+            // all four have read it
+            __syncwarp();
+            for (int i = et; i < N; i += kEpiThreads)
+                if ((i & 3) == 0) s_newer[i >> 2] = 0u;
         }
         if (!ok) {
             *s_abort = 1;
@@ -340,7 +484,6 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ------------------------------------------------------------------ host --
 template <int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D>;
@@ -363,7 +506,9 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
 
 bool gram_tc_supported(const ScoreArgs& a) {
     return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.N >= 2 &&
-           a.N <= kMaxBlocks * kRows && a.P <= 0x7fffffff && encode_fn() != nullptr;
+           a.N <= kMaxBlocks * kRows && a.P <= 0x7fffffff && (a.ld_ws % 4) == 0 &&
+           a.beta >= 0 && a.beta <= 127 &&
+           encode_fn() != nullptr;
 }
 
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
