@@ -17,9 +17,10 @@
 //           1 / sum_j exp(l - M_c);
 //   pass 2  p = exp(l - M_c) / S_c, mean over q, max over g -> I_j.
 // Warp 0 (one lane) issues the TMA loads, warp 1 owns TMEM and one lane issues
-// the MMAs, warps 2..5 are the epilogue; one persistent CTA per SM, with a
-// five-stage ring of key blocks so the next problem's keys stream in while
-// the epilogue reduces.  All waits are bounded.
+// the MMAs, the other warps are the epilogue; one persistent CTA per SM, with
+// a five-stage ring of key blocks so the next problem's keys stream in while
+// the epilogue reduces.  All waits are bounded.  When all of a problem's
+// logits fit in TMEM the resident variant below reads the keys only once.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -63,6 +64,7 @@ struct IParams {
     int64_t P;
     int N, n_obs, G;
     float scale;
+    float scale2;  // log2(e) / sqrt(d)
     float* I;
     int64_t ld;
     DeviceStatus* status;
@@ -328,6 +330,282 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------------
+// Resident variant: when the problem's logits fit in TMEM (T * RP <= 512
+// columns), each key block is multiplied once and its logits stay in TMEM;
+// the epilogue sweeps them three times (row max, sum of exponentials,
+// probabilities) and the keys are read from memory once.  Eight epilogue
+// warps in two groups take alternate key blocks.
+constexpr int kRThreads = 64 + 256;
+constexpr int kREpi = 256;
+constexpr uint32_t kRTmemCols = 512;
+constexpr int kRMaxBlocks = 16;
+
+template <int D, int RP>
+struct RCfg {
+    static constexpr int KC = D / kChunkElems;
+    static constexpr int kBlockBytes = KC * kChunkBytes;
+    static constexpr int kQChunkBytes = RP * 128;
+    static constexpr int kStages = D == 128 ? 5 : 10;
+    static constexpr size_t kQOff = (size_t)kStages * kBlockBytes;
+    static constexpr size_t kRedOff = kQOff + (size_t)KC * kQChunkBytes;
+    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * RP;
+    static constexpr int kNumBars = 2 * kStages + 2 + kRMaxBlocks + 3;
+    static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
+};
+
+// 16 TMEM columns into r[OFF .. OFF+15] (constant indices keep r in registers)
+template <int OFF, int RP>
+RKV_DEV void tmem_ld16_at(uint32_t taddr, uint32_t (&r)[RP]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]),
+          "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]),
+          "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),
+          "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15])
+        : "r"(taddr + (uint32_t)OFF));
+}
+
+template <int RP>
+RKV_DEV void tmem_ld_row(uint32_t taddr, uint32_t (&r)[RP]) {
+    tmem_ld16_at<0, RP>(taddr, r);
+    tmem_ld16_at<16, RP>(taddr, r);
+    if constexpr (RP > 32) tmem_ld16_at<32, RP>(taddr, r);
+    tmem_ld_wait();
+}
+
+template <int D, int RP>
+__global__ void __launch_bounds__(kRThreads, 1)
+importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap qmap, const IParams prm) {
+    using C = RCfg<D, RP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sK = smem;
+    uint8_t* sQ = smem + C::kQOff;
+    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [8][RP]
+    float* redS = redM + 8 * RP;                                 // [8][RP]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = k_full + C::kStages;
+    uint64_t* q_full = k_empty + C::kStages;
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* blk_full = q_empty + 1;          // [kRMaxBlocks]
+    uint64_t* tmem_free = blk_full + kRMaxBlocks;
+    uint64_t* epi_bar = tmem_free + 1;
+    uint64_t* drain_bar = epi_bar + 1;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    __shared__ unsigned long long s_colmask[kMaxObs + 1];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = prm.N, n_obs = prm.n_obs;
+    for (int k = threadIdx.x; k <= n_obs && k <= kMaxObs; k += blockDim.x) s_colmask[k] = prm.colmask[k];
+    const int T = (N + kRows - 1) / kRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int b = 0; b < kRMaxBlocks; ++b) mbar_init(&blk_full[b], 1);
+        mbar_init(tmem_free, kREpi);
+        mbar_init(epi_bar, kREpi);
+        mbar_init(drain_bar, 1);
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, kRTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t kk = 0, kq = 0;
+            bool ok = true;
+            for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+                if (!(ok = mbar_wait(q_empty, (kq & 1) ^ 1, s_abort))) break;
+                mbar_arrive_expect_tx(q_full, C::KC * C::kQChunkBytes);
+                for (int c = 0; c < C::KC; ++c)
+                    tma_load_3d(sQ + c * C::kQChunkBytes, &qmap, q_full, c * kChunkElems, 0, (int)p);
+                ++kq;
+                for (int b = 0; b < T; ++b) {
+                    const int s = kk % C::kStages;
+                    if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort))) break;
+                    mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
+                    for (int c = 0; c < C::KC; ++c)
+                        tma_load_3d(sK + s * C::kBlockBytes + c * kChunkBytes, &kmap, &k_full[s],
+                                    c * kChunkElems, b * kRows, (int)p);
+                    ++kk;
+                }
+            }
+            if (!ok) {
+                *s_abort = 1;
+                set_error(prm.status, kDevErrTimeout, 21u);
+            }
+            volatile int never = 0;
+            for (uint32_t u = kk > (uint32_t)C::kStages ? kk - C::kStages : 0; u < kk; ++u)
+                mbar_wait(&k_full[u % C::kStages], (u / C::kStages) & 1, &never);
+            if (kq > 0) mbar_wait(q_full, (kq - 1) & 1, &never);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kRows, RP);
+            uint32_t kk = 0, kp = 0;
+            bool ok = true;
+            for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
+                if (!(ok = mbar_wait(q_full, kp & 1, s_abort))) break;
+                // the previous problem's logits have all been read
+                if (!(ok = mbar_wait(tmem_free, (kp & 1) ^ 1, s_abort))) break;
+                tc_fence_after();
+                for (int b = 0; b < T; ++b) {
+                    const int s = kk % C::kStages;
+                    if (!(ok = mbar_wait(&k_full[s], (kk / C::kStages) & 1, s_abort))) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (uint32_t)(b * RP);
+#pragma unroll
+                    for (int c = 0; c < C::KC; ++c) {
+                        const uint64_t ad = sdesc_sw128(sK + s * C::kBlockBytes + c * kChunkBytes);
+                        const uint64_t bd = sdesc_sw128(sQ + c * C::kQChunkBytes);
+#pragma unroll
+                        for (int k = 0; k < kChunkElems / 16; ++k)
+                            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (c | k) != 0);
+                    }
+                    mma_commit(&k_empty[s]);
+                    mma_commit(&blk_full[b]);
+                    ++kk;
+                }
+                if (!ok) break;
+                mma_commit(q_empty);
+            }
+            if (!ok) {
+                *s_abort = 1;
+                set_error(prm.status, kDevErrTimeout, 22u);
+            }
+            mma_commit(drain_bar);
+            volatile int never = 0;
+            mbar_wait(drain_bar, 0, &never);
+        }
+    } else {
+        const int ew = warp - 2;           // 0..7
+        const int grp = ew >> 2;           // blocks b with b % 2 == grp
+        const int qd = warp & 3;           // TMEM lane quarter
+        const int row = qd * 32 + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
+        const int lim = N - n_obs;
+        const unsigned long long lastmask = prm.lastmask;
+        const float scale2 = prm.scale2;   // log2(e) / sqrt(d)
+        uint32_t kp = 0, ke = 0;
+        bool ok = true;
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
+            float m[RP], sm[RP];
+#pragma unroll
+            for (int c = 0; c < RP; ++c) m[c] = -INFINITY;
+            // ---- sweep 1: largest raw logit per query row
+            for (int b = grp; b < T; b += 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&blk_full[b], kp & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                const int j = b * kRows + row;
+                const unsigned long long vm =
+                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                uint32_t r[RP];
+                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+#pragma unroll
+                for (int c = 0; c < RP; ++c)
+                    if ((vm >> c) & 1ull) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                const float mx = warp_max(m[c]);
+                if (lane == 0) redM[ew * RP + c] = mx;
+            }
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                float mx = redM[c];
+#pragma unroll
+                for (int w = 1; w < 8; ++w) mx = fmaxf(mx, redM[w * RP + c]);
+                m[c] = mx * scale2;  // row max in log2 units
+                sm[c] = 0.f;
+            }
+            // ---- sweep 2: sum of exponentials
+            for (int b = grp; b < T; b += 2) {
+                tc_fence_after();
+                const int j = b * kRows + row;
+                const unsigned long long vm =
+                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                uint32_t r[RP];
+                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+#pragma unroll
+                for (int c = 0; c < RP; ++c)
+                    if ((vm >> c) & 1ull) sm[c] += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                const float ws = warp_sum(sm[c]);
+                if (lane == 0) redS[ew * RP + c] = ws;
+            }
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+            // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(x - m')
+            const float log2_nobs = log2f((float)n_obs);
+#pragma unroll
+            for (int c = 0; c < RP; ++c) {
+                float t = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) t += redS[w * RP + c];
+                m[c] += log2f(t) + log2_nobs;
+            }
+            // ---- sweep 3: probabilities -> importance
+            for (int b = grp; b < T; b += 2) {
+                tc_fence_after();
+                const int j = b * kRows + row;
+                const unsigned long long vm =
+                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                uint32_t r[RP];
+                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+                float best = -INFINITY, acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < RP; ++c) {
+                    if ((vm >> c) & 1ull) acc += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
+                    if ((lastmask >> c) & 1ull) {  // last query row of a head
+                        best = fmaxf(best, acc);
+                        acc = 0.f;
+                    }
+                }
+                if (j < N) prm.I[p * prm.ld + j] = best;
+            }
+            tc_fence_before();
+            mbar_arrive(tmem_free);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            set_error(prm.status, kDevErrTimeout, 23u);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kRTmemCols);
+}
+
 template <int D, int RP>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = ICfg<D, RP>;
@@ -343,6 +621,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     prm.n_obs = a.n_obs;
     prm.G = a.G;
     prm.scale = 1.0f / sqrtf((float)D);
+    prm.scale2 = (float)(1.4426950408889634 / sqrt((double)D));
     prm.I = a.I;
     prm.ld = a.ld_out;
     prm.status = a.status;
@@ -354,12 +633,22 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     }
     for (int c = 0; c < R; ++c)
         if (c % a.n_obs == a.n_obs - 1) prm.lastmask |= 1ull << c;
+    const int64_t cap = (int64_t)sm_count();
+    const int64_t grid = a.P < cap ? a.P : cap;
+    const int T = (a.N + kRows - 1) / kRows;
+    if (T <= kRMaxBlocks && T * RP <= (int)kRTmemCols) {
+        using RC = RCfg<D, RP>;
+        auto kern = importance_tcr_kernel<D, RP>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)RC::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, prm);
+        return cudaGetLastError();
+    }
     auto kern = importance_tc_kernel<D, RP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t cap = (int64_t)sm_count();
-    const int64_t grid = a.P < cap ? a.P : cap;
     kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(kmap, qmap, prm);
     return cudaGetLastError();
 }
