@@ -9,10 +9,12 @@
 // so it costs O(N d) per problem, not O(N^2 d).  The Gram kernels then only
 // handle the thresholded part (pairs with S_ij > tau).
 //
-// One CTA per problem, 8 warps; each warp owns whole rows (d/32 values per
-// lane, coalesced 128/256-byte row reads).  Pass 1 writes inv_norm and builds
-// s in fp32 (per-warp partials, then a fixed-order sum over warps); pass 2
-// re-reads the rows (from L2) and writes sum_i.
+// One CTA of 256 threads per problem.  A row of d elements is split over
+// L = d/8 lanes (16 bytes each, so a warp reads 32 x 16 contiguous bytes);
+// every thread keeps several rows' loads in flight.  Pass 1 writes inv_norm
+// and accumulates, per thread, the partial s of its 8 columns over its rows
+// (no cross-lane traffic for s until one shared-memory reduction at the
+// end); pass 2 re-reads the rows (from L2) and writes sum_i.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 #include "../../include/rkv.h"
@@ -20,68 +22,112 @@
 namespace rkv {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // rows in flight per thread
+
+// Sum over the L lanes that share a row (L = 8 or 16, aligned groups).  The
+// mask names only those lanes: they always run the same number of row
+// iterations, the two halves of a warp need not.
+template <int L>
+RKV_DEV float group_sum(float v) {
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned mask = ((1u << L) - 1u) << (lane & ~(unsigned)(L - 1));
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1) v += __shfl_xor_sync(mask, v, o);
+    return v;
+}
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads)
 key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
                  float* __restrict__ sum_s, int64_t ld) {
-    constexpr int VPL = D / 32;  // values per lane
-    __shared__ float s_part[kWarps][D];
+    constexpr int L = D / 8;                 // lanes per row
+    constexpr int RPI = kThreads / L;        // rows per iteration of the CTA
+    __shared__ float s_part[RPI][D];
     __shared__ float s_vec[D];
     const int64_t p = blockIdx.x;
     const T* Kp = K + (size_t)p * n_cap * D;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = threadIdx.x % L;         // which 8 columns
+    const int r0 = threadIdx.x / L;          // first row of this thread
+    const int col = sub * 8;
 
-    float acc[VPL];
+    float acc[8];
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) acc[t] = 0.f;
-    for (int i = warp; i < N; i += kWarps) {
-        float v[VPL];
+    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+    // ---- pass 1: norms and the partial sums of khat
+    for (int base = r0; base < N; base += RPI * kUnroll) {
+        float v[kUnroll][8];
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) v[t] = Elem<T>::to_f(Kp[(size_t)i * D + lane * VPL + t]);
-        float n2 = 0.f;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            if (i < N) {
+                load8(Kp + (size_t)i * D + col, v[u]);
+            } else {
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) n2 = fmaf(v[t], v[t], n2);
-        n2 = warp_sum(n2);
-        const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
-        if (lane == 0) inv_norm[p * ld + i] = inv;
+                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            }
+        }
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) acc[t] = fmaf(v[t], inv, acc[t]);
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            float n2 = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) n2 = fmaf(v[u][t], v[u][t], n2);
+            n2 = group_sum<L>(n2);
+            const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
+            if (i < N) {
+                if (sub == 0) inv_norm[p * ld + i] = inv;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) acc[t] = fmaf(v[u][t], inv, acc[t]);
+            }
+        }
     }
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) s_part[warp][lane * VPL + t] = acc[t];
+    for (int t = 0; t < 8; ++t) s_part[r0][col + t] = acc[t];
     __syncthreads();
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    for (int c = threadIdx.x; c < D; c += kThreads) {
         float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += s_part[w][c];
+#pragma unroll 8
+        for (int w = 0; w < RPI; ++w) s += s_part[w][c];
         s_vec[c] = s;
     }
     __syncthreads();
-    float sv[VPL];
+    float sv[8];
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) sv[t] = s_vec[lane * VPL + t];
-    for (int i = warp; i < N; i += kWarps) {
-        float v[VPL];
+    for (int t = 0; t < 8; ++t) sv[t] = s_vec[col + t];
+    // ---- pass 2: sum_i = khat_i . s - |khat_i|^2
+    for (int base = r0; base < N; base += RPI * kUnroll) {
+        float v[kUnroll][8];
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) v[t] = Elem<T>::to_f(Kp[(size_t)i * D + lane * VPL + t]);
-        float n2 = 0.f, ds = 0.f;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            if (i < N) {
+                load8(Kp + (size_t)i * D + col, v[u]);
+            } else {
 #pragma unroll
-        for (int t = 0; t < VPL; ++t) {
-            n2 = fmaf(v[t], v[t], n2);
-            ds = fmaf(v[t], sv[t], ds);
+                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            }
         }
-        n2 = warp_sum(n2);
-        ds = warp_sum(ds);
-        const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
-        if (lane == 0) sum_s[p * ld + i] = ds * inv - (n2 * inv) * inv;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            float n2 = 0.f, ds = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                n2 = fmaf(v[u][t], v[u][t], n2);
+                ds = fmaf(v[u][t], sv[t], ds);
+            }
+            n2 = group_sum<L>(n2);
+            ds = group_sum<L>(ds);
+            const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
+            if (i < N && sub == 0) sum_s[p * ld + i] = ds * inv - (n2 * inv) * inv;
+        }
     }
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
-    key_stats_kernel<T, D><<<(unsigned)a.P, kWarps * 32, 0, s>>>(
+    key_stats_kernel<T, D><<<(unsigned)a.P, kThreads, 0, s>>>(
         static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws);
     return cudaGetLastError();
 }
