@@ -35,6 +35,39 @@ sys.path.insert(0, ROOT)
 from decode_kv_cache_02_gb300 import rkv, workloads as wl  # noqa: E402
 
 METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM roofline"
+
+# DRAM bytes (read + write) per problem measured by ncu on the Llama-8B-shaped
+# problems (profiles/kernels_llama8b_1024problems.md, 1,024 problems), with the
+# sha256 of the kernel source they were measured on; a changed source reports
+# traffic null.  Every kernel streams whole problems, so traffic scales with
+# the problem count.
+NCU_TRAFFIC = {
+    "llama8b_full": {
+        "key_stats": ("k_key_stats.cu", "189b08d86d4e77076e61e84a4d5e5248e15bbd2da565eedab0c9b70ceaf9cd75", (600.171776e6 + 11.592704e6) / 1024),
+        "importance_tc": ("k_importance_tc.cu", "574d1ff4a91bf8bb4f7f49c3e5551b7631187003ad583b1d8567a6efcf63c97b", (310.479104e6 + 6.371840e6) / 1024),
+        "gram_tc": ("k_gram_tc.cu", "2c40b7ecdf45a0285d82e9d73a99d12996ba5e808422efeac5f8ec4d088d5e50", (316.326144e6 + 6.315264e6) / 1024),
+        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", (4.742912e6 + 0.0) / 1024),
+        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", (541.108224e6 + 487.986176e6) / 1024),
+    },
+}
+
+
+def measured_traffic(workload: str, kernel: str, problems: int):
+    """ncu DRAM bytes per launch for `problems` problems, or None when no
+    capture exists for this kernel and workload or the source has changed."""
+    import hashlib
+    ent = NCU_TRAFFIC.get(workload, {}).get(kernel)
+    if ent is None:
+        return None
+    fn, sha, per_problem = ent
+    path = os.path.join(ROOT, "decode_kv_cache_02_gb300", "csrc", fn)
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != sha:
+                return None
+    except OSError:
+        return None
+    return per_problem * problems
 UNIT = "tokens/s"
 
 
@@ -156,7 +189,7 @@ def work_model(w: wl.Workload) -> dict:
     }
 
 
-def roofline(kernels: dict, model: dict, peaks: dict, steps: int) -> dict:
+def roofline(kernels: dict, model: dict, peaks: dict, steps: int, w=None) -> dict:
     """Roofline of the kernel with the largest device time."""
     name = max(kernels, key=lambda k: kernels[k]["ms"])
     ms = kernels[name]["ms"] / max(1, kernels[name]["launches"]) if kernels[name]["launches"] \
@@ -180,7 +213,7 @@ def roofline(kernels: dict, model: dict, peaks: dict, steps: int) -> dict:
              "unit": "GB/s", "peak_kind": "HBM copy (of " + peaks["source"] + ")"}
     r["frac"] = r["achieved"] / r["peak"]
     r["ms_per_launch"] = per_launch_ms
-    r["traffic"] = None  # dram bytes per launch from ncu; filled from profiles/ when current
+    r["traffic"] = measured_traffic(w.name, name, w.problems) if w is not None else None
     del ms
     return r
 
@@ -320,7 +353,7 @@ def run_ours(args, w):
         "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
         "clocks": clocks.summary(),
     }
-    line["roofline"] = roofline(kernels, model, peaks, args.steps)
+    line["roofline"] = roofline(kernels, model, peaks, args.steps, w)
     # all kernels' fractions, for the record
     line["roofline_all"] = {}
     for k, v in kernels.items():
@@ -328,7 +361,7 @@ def run_ours(args, w):
             continue
         per = v["ms"] / v["launches"] * 1e-3
         m = model[k]
-        entry = {"ms_per_launch": per * 1e3}
+        entry = {"ms_per_launch": per * 1e3, "traffic": measured_traffic(w.name, k, w.problems)}
         if "bytes" in m:
             entry["hbm_frac"] = m["bytes"] / per / 1e9 / peaks["hbm_gbs"]
         if k == "gram_tc":
