@@ -335,7 +335,9 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 // columns), each key block is multiplied once and its logits stay in TMEM;
 // the epilogue sweeps them three times (row max, sum of exponentials,
 // probabilities) and the keys are read from memory once.  Eight epilogue
-// warps in two groups take alternate key blocks.
+// warps in two groups take alternate key blocks; a block's TMEM columns are
+// released as soon as its last sweep has read them, so the next problem's
+// MMAs overlap this problem's last sweep.
 constexpr int kRThreads = 64 + 256;
 constexpr int kREpi = 256;
 constexpr uint32_t kRTmemCols = 512;
@@ -350,7 +352,7 @@ struct RCfg {
     static constexpr size_t kQOff = (size_t)kStages * kBlockBytes;
     static constexpr size_t kRedOff = kQOff + (size_t)KC * kQChunkBytes;
     static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * RP;
-    static constexpr int kNumBars = 2 * kStages + 2 + kRMaxBlocks + 3;
+    static constexpr int kNumBars = 2 * kStages + 2 + 2 * kRMaxBlocks + 2;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
 };
 
@@ -392,9 +394,9 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     uint64_t* k_empty = k_full + C::kStages;
     uint64_t* q_full = k_empty + C::kStages;
     uint64_t* q_empty = q_full + 1;
-    uint64_t* blk_full = q_empty + 1;          // [kRMaxBlocks]
-    uint64_t* tmem_free = blk_full + kRMaxBlocks;
-    uint64_t* epi_bar = tmem_free + 1;
+    uint64_t* blk_full = q_empty + 1;            // [kRMaxBlocks]
+    uint64_t* tmem_free = blk_full + kRMaxBlocks;  // [kRMaxBlocks]
+    uint64_t* epi_bar = tmem_free + kRMaxBlocks;
     uint64_t* drain_bar = epi_bar + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -412,8 +414,10 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        for (int b = 0; b < kRMaxBlocks; ++b) mbar_init(&blk_full[b], 1);
-        mbar_init(tmem_free, kREpi);
+        for (int b = 0; b < kRMaxBlocks; ++b) {
+            mbar_init(&blk_full[b], 1);
+            mbar_init(&tmem_free[b], kREpi / 2);  // the group that reads block b
+        }
         mbar_init(epi_bar, kREpi);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -464,12 +468,11 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             bool ok = true;
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
                 if (!(ok = mbar_wait(q_full, kp & 1, s_abort))) break;
-                // the previous problem's logits have all been read
-                if (!(ok = mbar_wait(tmem_free, (kp & 1) ^ 1, s_abort))) break;
-                tc_fence_after();
                 for (int b = 0; b < T; ++b) {
                     const int s = kk % C::kStages;
                     if (!(ok = mbar_wait(&k_full[s], (kk / C::kStages) & 1, s_abort))) break;
+                    // the previous problem's logits of block b have been read
+                    if (!(ok = mbar_wait(&tmem_free[b], (kp & 1) ^ 1, s_abort))) break;
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + (uint32_t)(b * RP);
 #pragma unroll
@@ -589,10 +592,10 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                         acc = 0.f;
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&tmem_free[b]);  // block b's TMEM columns may be reused
                 if (j < N) prm.I[p * prm.ld + j] = best;
             }
-            tc_fence_before();
-            mbar_arrive(tmem_free);
         }
         if (!ok) {
             *s_abort = 1;
