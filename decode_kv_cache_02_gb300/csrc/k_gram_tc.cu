@@ -73,6 +73,7 @@ constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
 constexpr int kAccBufs = 4;
 constexpr uint32_t kTmemCols = kAccBufs * kRows;  // 512: all of TMEM
 constexpr int kInvFloats = kMaxBlocks * kRows;
+constexpr int kPrefetch = 5;  // finalize rows per thread loaded at problem start (N <= 1280)
 
 template <int D>
 struct Cfg {
@@ -136,12 +137,18 @@ RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
 }
 
 // Largest of 32 raw fp32 accumulators compared as signed integers: exact for
-// the positive ones, and <= 0 when none is positive.
+// the positive ones, and <= 0 when none is positive.  A tree of 3-input
+// maxima (depth 4) rather than a chain, for latency.
 RKV_DEV int raw_max32(const uint32_t (&r)[32]) {
-    int m = __vimax3_s32((int)r[0], (int)r[1], (int)r[2]);
+    int a[11];
 #pragma unroll
-    for (int e = 3; e < 31; e += 2) m = __vimax3_s32(m, (int)r[e], (int)r[e + 1]);
-    return max(m, (int)r[31]);
+    for (int t = 0; t < 10; ++t) a[t] = __vimax3_s32((int)r[3 * t], (int)r[3 * t + 1], (int)r[3 * t + 2]);
+    a[10] = max((int)r[30], (int)r[31]);
+    const int b0 = __vimax3_s32(a[0], a[1], a[2]);
+    const int b1 = __vimax3_s32(a[3], a[4], a[5]);
+    const int b2 = __vimax3_s32(a[6], a[7], a[8]);
+    const int b3 = max(a[9], a[10]);
+    return max(__vimax3_s32(b0, b1, b2), b3);
 }
 
 // ---------------------------------------------------------------- kernel --
@@ -341,6 +348,15 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
             if (!ok) break;
             const float* inv = s_inv + ib * kInvFloats;
             float* invmax = s_invmax + ib * kMaxBlocks * 4;
+            // finalize inputs of this thread's first rows, loaded now, used
+            // after the problem's last tile
+            float pre_tot[kPrefetch], pre_imp[kPrefetch];
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u) {
+                const int i = et + u * kEpiThreads;
+                pre_tot[u] = i < Cn ? prm.sum_s[p * prm.ld_ws + i] : 0.f;
+                pre_imp[u] = i < Cn ? prm.I[p * prm.ld_out + i] : 0.f;
+            }
             for (int x = et; x < T * 4; x += kEpiThreads) {
                 float m = -INFINITY;
                 const int j_end = min(N, (x + 1) * 32);
@@ -448,12 +464,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
             ++kepi;
             if (!ok) break;
             // finalize this thread's rows, then clear exactly what it read
-            for (int i = et; i < N; i += kEpiThreads) {
-                float tot = 0.f, imp = 0.f;
-                if (i < Cn) {
-                    tot = prm.sum_s[p * prm.ld_ws + i];
-                    imp = prm.I[p * prm.ld_out + i];
-                }
+            auto finalize_row = [&](int i, float tot, float imp) {
                 const float sim_i = (float)s_sim[i] * (1.0f / kSimScale);
                 const int nw = (int)((s_newer[i >> 2] >> (8 * (i & 3))) & 0xffu);
                 float rr = 0.f, z = INFINITY;
@@ -464,6 +475,16 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                 if (prm.R) prm.R[p * prm.ld_out + i] = rr;
                 prm.Z[p * prm.ld_out + i] = z;
                 s_sim[i] = 0;
+            };
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u) {
+                const int i = et + u * kEpiThreads;
+                if (i < N) finalize_row(i, pre_tot[u], pre_imp[u]);
+            }
+            for (int i = et + kPrefetch * kEpiThreads; i < N; i += kEpiThreads) {
+                const float tot = i < Cn ? prm.sum_s[p * prm.ld_ws + i] : 0.f;
+                const float imp = i < Cn ? prm.I[p * prm.ld_out + i] : 0.f;
+                finalize_row(i, tot, imp);
             }
             // a word of s_newer holds rows 4w..4w+3, finalized by four
             // neighbouring lanes of one warp; the first of them clears it once
