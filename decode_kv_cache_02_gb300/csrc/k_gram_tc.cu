@@ -33,9 +33,9 @@
 //   * warp 1: owns all 512 TMEM columns (four 128x128 fp32 accumulators); one
 //     lane issues tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
 //     M = N = 128, K = 16 per instruction, exact products) and tcgen05.commit.
-//   * warps 2..9 (256 threads): the epilogue.  Warp w reads TMEM lanes
-//     32*(w%4).. (one accumulator row per thread) and one half of the 128
-//     columns: two tcgen05.ld of 32 columns in flight, then a filter per 32x32
+//   * warps 2..17 (512 threads, four per scheduler for latency hiding): the
+//     epilogue.  Warp w reads TMEM lanes 32*(w%4).. (one accumulator row per
+//     thread) and one 32-column quarter of the tile, then filters the 32x32
 //     sub-tile -- the largest raw accumulator (an integer max over the bits,
 //     valid for positive floats) times the largest inverse norm of the 32
 //     columns -- skips the sub-tile unless some S could exceed tau (in
@@ -44,7 +44,7 @@
 //     popc for the newer count.
 //   * Row-side partials (sum of above-tau S, count of newer similar tokens)
 //     of the two column halves meet in shared memory through atomics; the
-//     count is kept as one saturating byte per row (exact for beta <= 127), so
+//     count is kept as one saturating byte per row (exact for beta <= 63), so
 //     R and Z are written once per problem, with no barrier per row block.
 //   * Every mbarrier wait is bounded; on timeout the kernel records
 //     kDevErrTimeout in the device status, stops issuing work, waits (bounded)
@@ -67,8 +67,11 @@ constexpr int kRows = 128;                // rows (and columns) of one Gram tile
 constexpr int kChunkElems = 64;           // bf16 elements per 128-byte swizzle row
 constexpr int kChunkBytes = kRows * 128;  // one [128 x 64] bf16 TMA box
 constexpr int kMaxBlocks = 34;            // N <= 4352
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kColGroups = kEpiWarps / 4;        // warps sharing one TMEM lane quarter
+constexpr int kChunksPerWarp = 4 / kColGroups;   // 32-column chunks per warp per tile
+constexpr int kNewerCap = 255 / kColGroups;      // per-group cap of the newer count
 constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
 constexpr int kAccBufs = 4;
 constexpr uint32_t kTmemCols = kAccBufs * kRows;  // 512: all of TMEM
@@ -333,9 +336,10 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         // ------------------------------------------------------- epilogue --
         const int et = threadIdx.x - 64;      // 0..255
         const int q = warp & 3;               // TMEM lane quarter of this warp
-        const int half = (warp - 2) >> 2;     // which 64 of the 128 columns
+        const int cg = (warp - 2) >> 2;       // which column group of the 128 columns
         const int row = q * 32 + lane;        // accumulator row of this thread
-        const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        const uint32_t t_row =
+            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * 32 * kChunksPerWarp);
         const int Cn = N - prm.n_obs;
         const float inv_nm1 = 1.0f / (float)(N - 1);
         uint32_t kacc = 0, kepi = 0, kinv = 0;
@@ -382,16 +386,17 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     if (!ok) break;
                     tc_fence_after();
                     const bool diag = (J == I);
-                    uint32_t r[2][32];
-                    tmem_ld_32cols(t_row + (uint32_t)(acc * kRows), r[0]);
-                    tmem_ld_32cols(t_row + (uint32_t)(acc * kRows + 32), r[1]);
+                    uint32_t r[kChunksPerWarp][32];
+#pragma unroll
+                    for (int h = 0; h < kChunksPerWarp; ++h)
+                        tmem_ld_32cols(t_row + (uint32_t)(acc * kRows + h * 32), r[h]);
                     tmem_ld_wait();
                     tc_fence_before();
                     mbar_arrive(&acc_empty[acc]);  // the accumulator is in registers now
                     ++kacc;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int chunk = J * 4 + half * 2 + h;  // 32-column chunk of the problem
+                    for (int h = 0; h < kChunksPerWarp; ++h) {
+                        const int chunk = J * 4 + cg * kChunksPerWarp + h;  // chunk of the problem
                         const int jb = chunk * 32;
                         // column e of this chunk is the row itself (diagonal blocks)
                         const int e_self = diag ? i - jb : -1;
@@ -447,12 +452,12 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     }
                 }
                 if (!ok) break;
-                // row-side partials of this half (newer saturated so that the
-                // two halves' bytes cannot carry into the next row)
+                // row-side partials of this column group (newer capped so
+                // that the groups' bytes cannot carry into the next row)
                 if (valid_i) {
                     if (sim_row != 0.f) atomicAdd(&s_sim[i], __float2int_rn(sim_row * kSimScale));
                     if (newer != 0)
-                        atomicAdd(&s_newer[i >> 2], (unsigned)min(newer, 127) << (8 * (i & 3)));
+                        atomicAdd(&s_newer[i >> 2], (unsigned)min(newer, kNewerCap) << (8 * (i & 3)));
                 }
             }
             if (!ok) break;
@@ -528,7 +533,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
 bool gram_tc_supported(const ScoreArgs& a) {
     return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.N >= 2 &&
            a.N <= kMaxBlocks * kRows && a.P <= 0x7fffffff && (a.ld_ws % 4) == 0 &&
-           a.beta >= 0 && a.beta <= 127 &&
+           a.beta >= 0 && a.beta <= kNewerCap &&
            encode_fn() != nullptr;
 }
 
