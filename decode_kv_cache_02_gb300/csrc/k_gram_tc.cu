@@ -66,7 +66,8 @@ using namespace tc;
 constexpr int kRows = 128;                // rows (and columns) of one Gram tile
 constexpr int kChunkElems = 64;           // bf16 elements per 128-byte swizzle row
 constexpr int kChunkBytes = kRows * 128;  // one [128 x 64] bf16 TMA box
-constexpr int kMaxBlocks = 34;            // N <= 4352
+constexpr int kMaxBlocksLarge = 34;       // N <= 4352
+constexpr int kMaxBlocksSmall = 16;       // N <= 2048: room for one more B stage
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kColGroups = kEpiWarps / 4;        // warps sharing one TMEM lane quarter
@@ -75,15 +76,16 @@ constexpr int kNewerCap = 255 / kColGroups;      // per-group cap of the newer c
 constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
 constexpr int kAccBufs = 4;
 constexpr uint32_t kTmemCols = kAccBufs * kRows;  // 512: all of TMEM
-constexpr int kInvFloats = kMaxBlocks * kRows;
 constexpr int kPrefetch = 5;  // finalize rows per thread loaded at problem start (N <= 1280)
 
-template <int D>
+template <int D, int MB>
 struct Cfg {
+    static constexpr int kMaxBlocks = MB;
+    static constexpr int kInvFloats = MB * kRows;
     static constexpr int KC = D / kChunkElems;  // swizzle chunks per row block
     static constexpr int kBlockBytes = KC * kChunkBytes;
     static constexpr int kAStages = 2;
-    static constexpr int kBStages = D == 128 ? 3 : 6;
+    static constexpr int kBStages = (D == 128 ? 3 : 6) + (MB <= kMaxBlocksSmall ? (D == 128 ? 1 : 2) : 0);
     static constexpr size_t kInvOff = (size_t)(kAStages + kBStages) * kBlockBytes;
     static constexpr size_t kSimOff = kInvOff + 2 * sizeof(float) * kInvFloats;
     static constexpr size_t kNewerOff = kSimOff + sizeof(float) * kInvFloats;
@@ -155,10 +157,12 @@ RKV_DEV int raw_max32(const uint32_t (&r)[32]) {
 }
 
 // ---------------------------------------------------------------- kernel --
-template <int D>
+template <int D, int MB>
 __global__ void __launch_bounds__(kThreads, 1)
 gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
-    using C = Cfg<D>;
+    using C = Cfg<D, MB>;
+    constexpr int kMaxBlocks = C::kMaxBlocks;
+    constexpr int kInvFloats = C::kInvFloats;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -338,8 +342,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         const int q = warp & 3;               // TMEM lane quarter of this warp
         const int cg = (warp - 2) >> 2;       // which column group of the 128 columns
         const int row = q * 32 + lane;        // accumulator row of this thread
-        const uint32_t t_row =
-            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(cg * 32 * kChunksPerWarp);
+        const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
         const int Cn = N - prm.n_obs;
         const float inv_nm1 = 1.0f / (float)(N - 1);
         uint32_t kacc = 0, kepi = 0, kinv = 0;
@@ -386,17 +389,22 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     if (!ok) break;
                     tc_fence_after();
                     const bool diag = (J == I);
+                    // the warp's column group rotates with J so that the hot
+                    // sub-tiles next to the diagonal do not always land on the
+                    // same warps
+                    const int cgr = (cg + J) % kColGroups;
                     uint32_t r[kChunksPerWarp][32];
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h)
-                        tmem_ld_32cols(t_row + (uint32_t)(acc * kRows + h * 32), r[h]);
+                        tmem_ld_32cols(t_lane + (uint32_t)(acc * kRows + (cgr * kChunksPerWarp + h) * 32),
+                                       r[h]);
                     tmem_ld_wait();
                     tc_fence_before();
                     mbar_arrive(&acc_empty[acc]);  // the accumulator is in registers now
                     ++kacc;
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h) {
-                        const int chunk = J * 4 + cg * kChunksPerWarp + h;  // chunk of the problem
+                        const int chunk = J * 4 + cgr * kChunksPerWarp + h;  // chunk of the problem
                         const int jb = chunk * 32;
                         // column e of this chunk is the row itself (diagonal blocks)
                         const int e_self = diag ? i - jb : -1;
@@ -510,15 +518,15 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <int D, int MB>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
-    using C = Cfg<D>;
+    using C = Cfg<D, MB>;
     CUtensorMap map;
     if (!make_map_3d_bf16(&map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
         return cudaErrorInvalidValue;
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,
                a.sum_s,  a.ld_ws, a.I,       a.R,    a.Z,      a.ld_out, a.status};
-    auto kern = gram_tc_kernel<D>;
+    auto kern = gram_tc_kernel<D, MB>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -532,14 +540,16 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
 
 bool gram_tc_supported(const ScoreArgs& a) {
     return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.N >= 2 &&
-           a.N <= kMaxBlocks * kRows && a.P <= 0x7fffffff && (a.ld_ws % 4) == 0 &&
+           a.N <= kMaxBlocksLarge * kRows && a.P <= 0x7fffffff && (a.ld_ws % 4) == 0 &&
            a.beta >= 0 && a.beta <= kNewerCap &&
            encode_fn() != nullptr;
 }
 
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
     if (a.P == 0) return cudaSuccess;
-    return a.d == 128 ? launch_t<128>(a, s) : launch_t<64>(a, s);
+    if (a.N <= kMaxBlocksSmall * kRows)
+        return a.d == 128 ? launch_t<128, kMaxBlocksSmall>(a, s) : launch_t<64, kMaxBlocksSmall>(a, s);
+    return a.d == 128 ? launch_t<128, kMaxBlocksLarge>(a, s) : launch_t<64, kMaxBlocksLarge>(a, s);
 }
 
 }  // namespace rkv
