@@ -8,8 +8,11 @@
 //     I_j     = max_g (1/n_obs) sum_q softmax_j(l_{c,.})
 //
 // The logits of a block of 128 keys are one tcgen05.mma chain: A = the key
-// block (M = 128, K-major bf16 from TMA), B = the problem's query rows padded
-// to RP (N = RP, rows >= R zero-filled by TMA), fp32 accumulators in TMEM.
+// block (M = 128, K-major bf16 from TMA), B = the problem's R query rows
+// followed by s = sum_j khat_j as two bf16 rows (hi, lo) and zero rows, N =
+// RP = 48, fp32 accumulators in TMEM.  The s columns give k_i . s, which
+// completes the redundancy row sum sum_i = inv_i (k_i . s) - |khat_i|^2 (the
+// key-stats kernel leaves |khat_i|^2 in sum_i) without another pass over K.
 // One epilogue thread owns one key row of the block.  Two passes over the
 // problem's keys (the second is expected to hit L2):
 //   pass 1  per-thread online (max, sum of exp) per query row, then a block
@@ -43,7 +46,7 @@ constexpr int kEpi = 128;
 constexpr int kAcc = 4;            // accumulators in flight
 constexpr int kAccCols = 64;       // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 256;
-constexpr int kMaxQueryRows = 48;  // G * n_obs handled here
+constexpr int kMaxQueryRows = 46;  // G * n_obs handled here (plus the two s rows)
 
 template <int D, int RP>
 struct ICfg {
@@ -63,10 +66,16 @@ constexpr int kMaxObs = kMaxQueryRows;
 struct IParams {
     int64_t P;
     int N, n_obs, G;
+    int R;         // query rows G * n_obs; B rows R, R+1 hold s (hi, lo)
     float scale;
     float scale2;  // log2(e) / sqrt(d)
     float* I;
     int64_t ld;
+    // sum_i = inv_i (k_i . s) - |khat_i|^2: the key-stats kernel leaves
+    // |khat_i|^2 in sum_s, this kernel completes it
+    const float* inv_norm;
+    float* sum_s;
+    int64_t ld_ws;
     DeviceStatus* status;
     // bit c of colmask[k]: query row c exists and its query index c % n_obs
     // is >= k (so it sees a key k positions past N - n_obs); bit c of
@@ -88,7 +97,8 @@ RKV_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
 template <int D, int RP>
 __global__ void __launch_bounds__(kThreads, 1)
 importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap qmap, const IParams prm) {
+                     const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap smap, const IParams prm) {
     using C = ICfg<D, RP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -147,8 +157,11 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
                 if (!(ok = mbar_wait(q_empty, (kq & 1) ^ 1, s_abort))) break;
                 mbar_arrive_expect_tx(q_full, C::KC * C::kQChunkBytes);
-                for (int c = 0; c < C::KC; ++c)
+                for (int c = 0; c < C::KC; ++c) {
                     tma_load_3d(sQ + c * C::kQChunkBytes, &qmap, q_full, c * kChunkElems, 0, (int)p);
+                    tma_load_3d(sQ + c * C::kQChunkBytes + prm.R * 128, &smap, q_full,
+                                c * kChunkElems, 0, (int)p);
+                }
                 ++kq;
                 for (int pass = 0; ok && pass < 2; ++pass) {
                     for (int b = 0; b < T; ++b) {
@@ -293,7 +306,12 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int j = b * kRows + row;
                 const unsigned long long vm =
                     j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
-                float best = -INFINITY, acc = 0.f;
+                float iv = 0.f, self = 0.f;
+                if (j < N) {
+                    iv = prm.inv_norm[p * prm.ld_ws + j];
+                    self = prm.sum_s[p * prm.ld_ws + j];
+                }
+                float best = -INFINITY, acc = 0.f, dot = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < RP / 16; ++cc) {
                     uint32_t r[16];
@@ -310,12 +328,16 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                             best = fmaxf(best, acc * inv_nobs);
                             acc = 0.f;
                         }
+                        if (c == prm.R || c == prm.R + 1) dot += __uint_as_float(r[e]);
                     }
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[a]);
                 ++ka;
-                if (j < N) prm.I[p * prm.ld + j] = best;
+                if (j < N) {
+                    prm.I[p * prm.ld + j] = best;
+                    prm.sum_s[p * prm.ld_ws + j] = iv * dot - self;
+                }
             }
         }
         if (!ok) {
@@ -377,10 +399,11 @@ RKV_DEV void tmem_ld_row(uint32_t taddr, uint32_t (&r)[RP]) {
     tmem_ld_wait();
 }
 
-template <int D, int RP>
+template <int D, int RP, int QP>
 __global__ void __launch_bounds__(kRThreads, 1)
 importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap qmap, const IParams prm) {
+                      const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap smap, const IParams prm) {
     using C = RCfg<D, RP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -439,8 +462,11 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
                 if (!(ok = mbar_wait(q_empty, (kq & 1) ^ 1, s_abort))) break;
                 mbar_arrive_expect_tx(q_full, C::KC * C::kQChunkBytes);
-                for (int c = 0; c < C::KC; ++c)
+                for (int c = 0; c < C::KC; ++c) {
                     tma_load_3d(sQ + c * C::kQChunkBytes, &qmap, q_full, c * kChunkElems, 0, (int)p);
+                    tma_load_3d(sQ + c * C::kQChunkBytes + prm.R * 128, &smap, q_full,
+                                c * kChunkElems, 0, (int)p);
+                }
                 ++kq;
                 for (int b = 0; b < T; ++b) {
                     const int s = kk % C::kStages;
@@ -510,9 +536,11 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
         uint32_t kp = 0, ke = 0;
         bool ok = true;
         for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
-            float m[RP], sm[RP];
+            // softmax state for the QP query columns (the rows of s are at
+            // columns R, R+1 and only read in sweep 3)
+            float m[QP], sm[QP];
 #pragma unroll
-            for (int c = 0; c < RP; ++c) m[c] = -INFINITY;
+            for (int c = 0; c < QP; ++c) m[c] = -INFINITY;
             // ---- sweep 1: largest raw logit per query row
             for (int b = grp; b < T; b += 2) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&blk_full[b], kp & 1, s_abort));
@@ -521,15 +549,15 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int j = b * kRows + row;
                 const unsigned long long vm =
                     j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
-                uint32_t r[RP];
-                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+                uint32_t r[QP];
+                tmem_ld_row<QP>(t_row + (uint32_t)(b * RP), r);
 #pragma unroll
-                for (int c = 0; c < RP; ++c)
+                for (int c = 0; c < QP; ++c)
                     if ((vm >> c) & 1ull) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
             }
             if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < RP; ++c) {
+            for (int c = 0; c < QP; ++c) {
                 const float mx = warp_max(m[c]);
                 if (lane == 0) redM[ew * RP + c] = mx;
             }
@@ -538,7 +566,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             ++ke;
             if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < RP; ++c) {
+            for (int c = 0; c < QP; ++c) {
                 float mx = redM[c];
 #pragma unroll
                 for (int w = 1; w < 8; ++w) mx = fmaxf(mx, redM[w * RP + c]);
@@ -551,14 +579,14 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int j = b * kRows + row;
                 const unsigned long long vm =
                     j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
-                uint32_t r[RP];
-                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+                uint32_t r[QP];
+                tmem_ld_row<QP>(t_row + (uint32_t)(b * RP), r);
 #pragma unroll
-                for (int c = 0; c < RP; ++c)
+                for (int c = 0; c < QP; ++c)
                     if ((vm >> c) & 1ull) sm[c] += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
             }
 #pragma unroll
-            for (int c = 0; c < RP; ++c) {
+            for (int c = 0; c < QP; ++c) {
                 const float ws = warp_sum(sm[c]);
                 if (lane == 0) redS[ew * RP + c] = ws;
             }
@@ -569,7 +597,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(x - m')
             const float log2_nobs = log2f((float)n_obs);
 #pragma unroll
-            for (int c = 0; c < RP; ++c) {
+            for (int c = 0; c < QP; ++c) {
                 float t = 0.f;
 #pragma unroll
                 for (int w = 0; w < 8; ++w) t += redS[w * RP + c];
@@ -581,20 +609,39 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 const int j = b * kRows + row;
                 const unsigned long long vm =
                     j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                float iv = 0.f, self = 0.f;
+                if (j < N) {
+                    iv = prm.inv_norm[p * prm.ld_ws + j];
+                    self = prm.sum_s[p * prm.ld_ws + j];
+                }
                 uint32_t r[RP];
-                tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
-                float best = -INFINITY, acc = 0.f;
+                if constexpr (QP < RP) {
+                    // query columns, then the 16 columns that start with s
+                    tmem_ld16_at<0, RP>(t_row + (uint32_t)(b * RP), r);
+                    tmem_ld16_at<16, RP>(t_row + (uint32_t)(b * RP), r);
+                    tmem_ld16_at<32, RP>(t_row + (uint32_t)(b * RP), r);
+                    tmem_ld_wait();
+                } else {
+                    tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
+                }
+                float best = -INFINITY, acc = 0.f, dot = 0.f;
 #pragma unroll
                 for (int c = 0; c < RP; ++c) {
-                    if ((vm >> c) & 1ull) acc += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
-                    if ((lastmask >> c) & 1ull) {  // last query row of a head
-                        best = fmaxf(best, acc);
-                        acc = 0.f;
+                    if (c < QP) {
+                        if ((vm >> c) & 1ull) acc += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
+                        if ((lastmask >> c) & 1ull) {  // last query row of a head
+                            best = fmaxf(best, acc);
+                            acc = 0.f;
+                        }
                     }
+                    if (c == prm.R || c == prm.R + 1) dot += __uint_as_float(r[c]);
                 }
                 tc_fence_before();
                 mbar_arrive(&tmem_free[b]);  // block b's TMEM columns may be reused
-                if (j < N) prm.I[p * prm.ld + j] = best;
+                if (j < N) {
+                    prm.I[p * prm.ld + j] = best;
+                    prm.sum_s[p * prm.ld_ws + j] = iv * dot - self;
+                }
             }
         }
         if (!ok) {
@@ -612,21 +659,27 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
 template <int D, int RP>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = ICfg<D, RP>;
-    CUtensorMap kmap, qmap;
+    CUtensorMap kmap, qmap, smap;
     const int R = a.G * a.n_obs;
     if (!make_map_3d_bf16(&kmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
         return cudaErrorInvalidValue;
-    if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, RP))
+    if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
+        return cudaErrorInvalidValue;
+    if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, RP - R))
         return cudaErrorInvalidValue;
     IParams prm{};
     prm.P = a.P;
     prm.N = a.N;
     prm.n_obs = a.n_obs;
     prm.G = a.G;
+    prm.R = R;
     prm.scale = 1.0f / sqrtf((float)D);
     prm.scale2 = (float)(1.4426950408889634 / sqrt((double)D));
     prm.I = a.I;
     prm.ld = a.ld_out;
+    prm.inv_norm = a.inv_norm;
+    prm.sum_s = a.sum_s;
+    prm.ld_ws = a.ld_ws;
     prm.status = a.status;
     for (int k = 0; k <= a.n_obs && k <= kMaxObs; ++k) {
         unsigned long long m = 0;
@@ -641,32 +694,32 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     const int T = (a.N + kRows - 1) / kRows;
     if (T <= kRMaxBlocks && T * RP <= (int)kRTmemCols) {
         using RC = RCfg<D, RP>;
-        auto kern = importance_tcr_kernel<D, RP>;
+        auto kern = R <= 32 ? importance_tcr_kernel<D, RP, 32> : importance_tcr_kernel<D, RP, 48>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)RC::kSmemBytes);
         if (e != cudaSuccess) return e;
-        kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, prm);
+        kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, smap, prm);
         return cudaGetLastError();
     }
     auto kern = importance_tc_kernel<D, RP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(kmap, qmap, prm);
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(kmap, qmap, smap, prm);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const ScoreArgs& a, cudaStream_t s) {
-    const int R = a.G * a.n_obs;
-    if (R <= 32) return launch_t<D, 32>(a, s);
+    // the query rows plus the two rows of s, padded to the MMA's N step of 16
     return launch_t<D, 48>(a, s);
 }
 
 }  // namespace
 
 bool importance_tc_supported(const ScoreArgs& a) {
-    return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.G * a.n_obs <= kMaxQueryRows &&
+    return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) &&
+           a.G * a.n_obs <= kMaxQueryRows && (a.G * a.n_obs) % 8 == 0 &&
            a.N >= 2 && a.P <= 0x7fffffff && encode_fn() != nullptr;
 }
 

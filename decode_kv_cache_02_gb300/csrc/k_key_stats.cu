@@ -14,7 +14,10 @@
 // every thread keeps several rows' loads in flight.  Pass 1 writes inv_norm
 // and accumulates, per thread, the partial s of its 8 columns over its rows
 // (no cross-lane traffic for s until one shared-memory reduction at the
-// end); pass 2 re-reads the rows (from L2) and writes sum_i.
+// end); pass 2 re-reads the rows (from L2) and writes sum_i.  When the
+// tensor-core importance kernel runs, only pass 1 is needed: it writes
+// |khat_i|^2 into sum_i and s as bf16 rows (hi, lo) that the importance MMA
+// multiplies with every key block anyway, which completes sum_i there.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 #include "../../include/rkv.h"
@@ -24,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;  // rows in flight per thread
+constexpr int kSRows = 16;  // rows of the s block handed to the importance MMA
 
 // Sum over the L lanes that share a row (L = 8 or 16, aligned groups).  The
 // mask names only those lanes: they always run the same number of row
@@ -40,7 +44,8 @@ RKV_DEV float group_sum(float v) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
-                 float* __restrict__ sum_s, int64_t ld) {
+                 float* __restrict__ sum_s, int64_t ld, bool two_pass,
+                 __nv_bfloat16* __restrict__ s_rows) {
     constexpr int L = D / 8;                 // lanes per row
     constexpr int RPI = kThreads / L;        // rows per iteration of the CTA
     __shared__ float s_part[RPI][D];
@@ -76,7 +81,11 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
             n2 = group_sum<L>(n2);
             const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
             if (i < N) {
-                if (sub == 0) inv_norm[p * ld + i] = inv;
+                if (sub == 0) {
+                    inv_norm[p * ld + i] = inv;
+                    // |khat_i|^2, completed to sum_i by the importance kernel
+                    if (!two_pass) sum_s[p * ld + i] = (n2 * inv) * inv;
+                }
 #pragma unroll
                 for (int t = 0; t < 8; ++t) acc[t] = fmaf(v[u][t], inv, acc[t]);
             }
@@ -90,7 +99,17 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
 #pragma unroll 8
         for (int w = 0; w < RPI; ++w) s += s_part[w][c];
         s_vec[c] = s;
+        if (!two_pass) {
+            // s as two bf16 rows (s ~= hi + lo to 2^-16), then 14 zero rows:
+            // extra B rows of the importance MMA, which then yields k_i . s
+            __nv_bfloat16* sr = s_rows + (size_t)p * kSRows * D;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(s);
+            sr[c] = hi;
+            sr[D + c] = __float2bfloat16_rn(s - __bfloat162float(hi));
+            for (int r = 2; r < kSRows; ++r) sr[r * D + c] = __float2bfloat16_rn(0.f);
+        }
     }
+    if (!two_pass) return;
     __syncthreads();
     float sv[8];
 #pragma unroll
@@ -128,7 +147,8 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
 template <typename T, int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     key_stats_kernel<T, D><<<(unsigned)a.P, kThreads, 0, s>>>(
-        static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws);
+        static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
+        static_cast<__nv_bfloat16*>(a.s_rows));
     return cudaGetLastError();
 }
 

@@ -84,6 +84,7 @@ struct Workspace {
     float* sum_s;
     float* I;
     float* Z;
+    void* s_rows;
     int64_t ld;
     size_t bytes;
 };
@@ -107,6 +108,8 @@ Workspace carve(void* base, int64_t P, int n) {
     off += arr;
     w.Z = reinterpret_cast<float*>(b + off);
     off += arr;
+    w.s_rows = b + off;
+    off += align_up(2 * (size_t)P * 16 * 128);
     w.bytes = off;
     return w;
 }
@@ -167,21 +170,25 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.tau = tau;
     a.inv_norm = w.inv_norm;
     a.sum_s = w.sum_s;
+    a.s_rows = w.s_rows;
     a.ld_ws = w.ld;
     a.I = I;
     a.R = R;
     a.Z = Z;
     a.ld_out = ld_out;
     a.status = w.status;
+    const bool gram_tc = rkv::gram_tc_supported(a);
+    const bool imp_tc = rkv::importance_tc_supported(a);
+    a.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
     cudaError_t e = timed(kKeyStats, s, [&] { return rkv::launch_key_stats(a, s); });
     if (e == cudaSuccess) {
-        if (rkv::importance_tc_supported(a))
+        if (imp_tc)
             e = timed(kImportanceTc, s, [&] { return rkv::launch_importance_tc(a, s); });
         else
             e = timed(kImportance, s, [&] { return rkv::launch_importance(a, s); });
     }
     if (e == cudaSuccess) {
-        if (rkv::gram_tc_supported(a))
+        if (gram_tc)
             e = timed(kGramTc, s, [&] { return rkv::launch_gram_tc(a, s); });
         else
             e = timed(kGramSimt, s, [&] { return rkv::launch_gram_simt(a, s); });

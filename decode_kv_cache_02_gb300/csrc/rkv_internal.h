@@ -19,6 +19,8 @@ struct ScoreArgs {
     // workspace rows (stride ld_ws floats per problem)
     float* inv_norm;     // 1 / max(|k_i|, eps)
     float* sum_s;        // sum_{j != i} S_ij
+    void* s_rows;        // [P, 16, d] bf16: s = sum_j khat_j as (hi, lo, 0...)
+    bool stats_sum;      // key stats write sum_s (else importance completes it)
     int64_t ld_ws;
     // outputs (stride ld_out floats per problem); R may be null
     float* I;

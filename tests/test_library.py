@@ -52,8 +52,9 @@ def _desc(P=4, G=4, d=128, n_cap=1152, dtype=0):
 def test_workspace_size(lib):
     d = _desc()
     n = lib.rkv_workspace_size(ctypes.byref(d), 1152, 8)
-    # status block + four fp32 [P, N] arrays, each rounded to 256 bytes
-    assert n == 256 + 4 * ((4 * 1152 * 4 + 255) // 256 * 256)
+    # status block + four fp32 [P, N] arrays + the [P, 16, 128] bf16 s rows,
+    # each rounded to 256 bytes
+    assert n == 256 + 4 * ((4 * 1152 * 4 + 255) // 256 * 256) + (2 * 4 * 16 * 128 + 255) // 256 * 256
     assert lib.rkv_workspace_size(None, 1152, 8) == 0
     bad = _desc(d=96)
     assert lib.rkv_workspace_size(ctypes.byref(bad), 1152, 8) == 0
