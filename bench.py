@@ -43,11 +43,11 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "189b08d86d4e77076e61e84a4d5e5248e15bbd2da565eedab0c9b70ceaf9cd75", (600.171776e6 + 11.592704e6) / 1024),
-        "importance_tc": ("k_importance_tc.cu", "574d1ff4a91bf8bb4f7f49c3e5551b7631187003ad583b1d8567a6efcf63c97b", (310.479104e6 + 6.371840e6) / 1024),
-        "gram_tc": ("k_gram_tc.cu", "2c40b7ecdf45a0285d82e9d73a99d12996ba5e808422efeac5f8ec4d088d5e50", (316.326144e6 + 6.315264e6) / 1024),
-        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", (4.742912e6 + 0.0) / 1024),
-        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", (541.108224e6 + 487.986176e6) / 1024),
+        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314681344 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "0b1e9411925fea548bd6ec7ae002d2f47619c1c43e4fddcbf028e91152f9f228", 332675072 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "edfbc516d5ac99deb85aed8e6077c11b9a0b9e549cc8a8f7ae709909a0191c70", 322827776 / 1024),
+        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", 4742912 / 1024),
+        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", 1029194496 / 1024),
     },
 }
 
