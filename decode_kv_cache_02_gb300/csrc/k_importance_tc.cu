@@ -82,6 +82,7 @@ struct IParams {
     // lastmask: c is the last query row of its head.
     unsigned long long colmask[kMaxObs + 1];
     unsigned long long lastmask;
+    int ns, nd;  // resident variant: logit slots and dot slots in TMEM
 };
 
 RKV_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
@@ -353,29 +354,44 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 }
 
 // ------------------------------------------------------------------------
-// Resident variant: when the problem's logits fit in TMEM (T * RP <= 512
-// columns), each key block is multiplied once and its logits stay in TMEM;
-// the epilogue sweeps them three times (row max, sum of exponentials,
-// probabilities) and the keys are read from memory once.  Eight epilogue
-// warps in two groups take alternate key blocks; a block's TMEM columns are
-// released as soon as its last sweep has read them, so the next problem's
-// MMAs overlap this problem's last sweep.
+// Resident variant: when a problem's logits fit in TMEM, each key block is
+// multiplied once and its logits stay in TMEM while the epilogue sweeps them
+// three times (row max, sum of exponentials, probabilities); the keys are
+// read from memory once.  TMEM is split into a ring of NS logit slots of SC
+// columns (the query rows) and a ring of ND dot slots of 16 columns (k . s_hi,
+// k . s_lo from a second N = 16 MMA).  Sweep 1 releases a block's dot slot and
+// sweep 3 its logit slot, so the MMAs of the next problem run while this one
+// is swept and the key stream keeps going.  NS >= T keeps the ring free of
+// deadlock (a problem never waits for one of its own logit slots); so does
+// ND >= 1 (sweep 1 of a block needs that block's MMA only).  The query rows
+// are double-buffered.  Eight epilogue warps in two groups take alternate key
+// blocks.
 constexpr int kRThreads = 64 + 256;
 constexpr int kREpi = 256;
 constexpr uint32_t kRTmemCols = 512;
-constexpr int kRMaxBlocks = 16;
+constexpr int kRMaxSlots = 16;
+constexpr int kRMaxDots = 32;
+constexpr int kDotCols = 16;
+constexpr size_t kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
 
-template <int D, int RP>
+template <int D, int SC>
 struct RCfg {
     static constexpr int KC = D / kChunkElems;
     static constexpr int kBlockBytes = KC * kChunkBytes;
-    static constexpr int kQChunkBytes = RP * 128;
-    static constexpr int kStages = D == 128 ? 5 : 10;
-    static constexpr size_t kQOff = (size_t)kStages * kBlockBytes;
-    static constexpr size_t kRedOff = kQOff + (size_t)KC * kQChunkBytes;
-    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * RP;
-    static constexpr int kNumBars = 2 * kStages + 2 + 2 * kRMaxBlocks + 2;
+    static constexpr int kQChunkBytes = SC * 128;
+    static constexpr int kSChunkBytes = kDotCols * 128;
+    static constexpr int kBBytes = KC * (kQChunkBytes + kSChunkBytes);  // one problem's B operands
+    static constexpr int kFixedBars = 4 + 2 * kRMaxSlots + kRMaxDots + 2;
+    static constexpr size_t kFixed =
+        1024 + 2 * (size_t)kBBytes + sizeof(float) * 16 * SC + 8 * kFixedBars + 16;
+    static constexpr int kFit = (int)((kSmemLimit - kFixed) / (kBlockBytes + 16));
+    static constexpr int kStages = kFit < 12 ? kFit : 12;
+    static constexpr size_t kBOff = (size_t)kStages * kBlockBytes;
+    static constexpr size_t kRedOff = kBOff + 2 * (size_t)kBBytes;
+    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * SC;
+    static constexpr int kNumBars = 2 * kStages + kFixedBars;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
+    static_assert(kStages >= 4 && kSmemBytes <= kSmemLimit, "shared memory plan");
 };
 
 // 16 TMEM columns into r[OFF .. OFF+15] (constant indices keep r in registers)
@@ -391,35 +407,124 @@ RKV_DEV void tmem_ld16_at(uint32_t taddr, uint32_t (&r)[RP]) {
         : "r"(taddr + (uint32_t)OFF));
 }
 
-template <int RP>
-RKV_DEV void tmem_ld_row(uint32_t taddr, uint32_t (&r)[RP]) {
-    tmem_ld16_at<0, RP>(taddr, r);
-    tmem_ld16_at<16, RP>(taddr, r);
-    if constexpr (RP > 32) tmem_ld16_at<32, RP>(taddr, r);
-    tmem_ld_wait();
+RKV_DEV void tmem_ld_2cols(uint32_t taddr, uint32_t& a, uint32_t& b) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                 : "=r"(a), "=r"(b)
+                 : "r"(taddr));
 }
 
-template <int D, int RP, int QP>
+// the SC query columns of one key row (no wait)
+template <int SC>
+RKV_DEV void tmem_ld_row_nowait(uint32_t taddr, uint32_t (&r)[SC]) {
+    tmem_ld16_at<0, SC>(taddr, r);
+    tmem_ld16_at<16, SC>(taddr, r);
+    if constexpr (SC > 32) tmem_ld16_at<32, SC>(taddr, r);
+}
+
+RKV_DEV float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+RKV_DEV float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+struct OpMax {
+    RKV_DEV float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpAdd {
+    RKV_DEV float operator()(float a, float b) const { return a + b; }
+};
+
+// Warp reduce-scatter of v[OFF .. OFF+NV) (NV = 16 or 32): rounds of halving
+// width, each lane keeping the half its lane bit selects and folding in the
+// partner's other half.  On return lane l holds the reduction over the warp of
+// column OFF + (l mod NV); v is clobbered.
+template <int OFF, int NV, int SC, class Op>
+RKV_DEV float warp_reduce_scatter(float (&v)[SC], Op op) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = NV / 2; h >= 1; h >>= 1) {
+        const bool up = (lane & h) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[OFF + i] : v[OFF + i + h];
+            const float keep = up ? v[OFF + i + h] : v[OFF + i];
+            v[OFF + i] = op(keep, __shfl_xor_sync(0xffffffffu, send, h));
+        }
+    }
+    float r = v[OFF];
+#pragma unroll
+    for (int h = NV; h < 32; h <<= 1) r = op(r, __shfl_xor_sync(0xffffffffu, r, h));
+    return r;
+}
+
+// Row statistics over the eight epilogue warps: each warp reduce-scatters its
+// per-thread partials, lane l posts column l (and 32 + l mod 16 when SC = 48),
+// and after the barrier every lane folds its column over the warps.
+template <int SC, class Op>
+RKV_DEV void post_partials(float (&v)[SC], float* red, int ew, Op op) {
+    const int lane = threadIdx.x & 31;
+    const float lo = warp_reduce_scatter<0, 32, SC>(v, op);
+    red[ew * SC + lane] = lo;
+    if constexpr (SC > 32) {
+        const float hi = warp_reduce_scatter<32, SC - 32, SC>(v, op);
+        if (lane < SC - 32) red[ew * SC + 32 + lane] = hi;
+    }
+}
+
+template <int SC, class Op>
+RKV_DEV void fold_partials(const float* red, float& lo, float& hi, Op op) {
+    const int lane = threadIdx.x & 31;
+    lo = red[lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) lo = op(lo, red[w * SC + lane]);
+    hi = 0.f;
+    if constexpr (SC > 32) {
+        const int c = 32 + (lane & (SC - 33));
+        hi = red[c];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) hi = op(hi, red[w * SC + c]);
+    }
+}
+
+// every lane gets all SC column values back from the lanes that own them
+template <int SC>
+RKV_DEV void broadcast_columns(float (&v)[SC], float lo, float hi) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = __shfl_sync(0xffffffffu, lo, c);
+#pragma unroll
+    for (int c = 32; c < SC; ++c) v[c] = __shfl_sync(0xffffffffu, hi, c - 32);
+}
+
+// HEAD > 0: the query rows form SC / HEAD heads of HEAD rows (R == SC), so a
+// head's last row is known at compile time; HEAD == 0 reads it from lastmask.
+template <int D, int SC, int HEAD>
 __global__ void __launch_bounds__(kRThreads, 1)
 importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap smap, const IParams prm) {
-    using C = RCfg<D, RP>;
+    using C = RCfg<D, SC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sK = smem;
-    uint8_t* sQ = smem + C::kQOff;
-    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [8][RP]
-    float* redS = redM + 8 * RP;                                 // [8][RP]
+    uint8_t* sB = smem + C::kBOff;  // [2][ KC query chunks | KC s chunks ]
+    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [8][SC]
+    float* redS = redM + 8 * SC;                                 // [8][SC]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* k_full = bars;
     uint64_t* k_empty = k_full + C::kStages;
-    uint64_t* q_full = k_empty + C::kStages;
-    uint64_t* q_empty = q_full + 1;
-    uint64_t* blk_full = q_empty + 1;            // [kRMaxBlocks]
-    uint64_t* tmem_free = blk_full + kRMaxBlocks;  // [kRMaxBlocks]
-    uint64_t* epi_bar = tmem_free + kRMaxBlocks;
+    uint64_t* q_full = k_empty + C::kStages;    // [2]
+    uint64_t* q_empty = q_full + 2;             // [2]
+    uint64_t* blk_full = q_empty + 2;           // [kRMaxSlots]
+    uint64_t* tmem_free = blk_full + kRMaxSlots;  // [kRMaxSlots]
+    uint64_t* dot_free = tmem_free + kRMaxSlots;  // [kRMaxDots]
+    uint64_t* epi_bar = dot_free + kRMaxDots;
     uint64_t* drain_bar = epi_bar + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -427,20 +532,36 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N, n_obs = prm.n_obs;
+    const uint32_t NS = (uint32_t)prm.ns, ND = (uint32_t)prm.nd;
     for (int k = threadIdx.x; k <= n_obs && k <= kMaxObs; k += blockDim.x) s_colmask[k] = prm.colmask[k];
     const int T = (N + kRows - 1) / kRows;
 
+    // query rows R .. SC-1 of both B buffers are never loaded: zero them once
+    // (their logit columns are masked, zeros keep them finite)
+    if (prm.R < SC) {
+        const int pad = (SC - prm.R) * 128;
+        for (int i = threadIdx.x; i < 2 * C::KC * pad / 16; i += blockDim.x) {
+            const int chunk = i / (pad / 16), off = i % (pad / 16);
+            const int buf = chunk / C::KC, c = chunk % C::KC;
+            *reinterpret_cast<uint4*>(sB + buf * C::kBBytes + c * C::kQChunkBytes + prm.R * 128 +
+                                      off * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
         }
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        for (int b = 0; b < kRMaxBlocks; ++b) {
-            mbar_init(&blk_full[b], 1);
-            mbar_init(&tmem_free[b], kREpi / 2);  // the group that reads block b
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&q_full[q], 1);
+            mbar_init(&q_empty[q], 1);
         }
+        for (int b = 0; b < kRMaxSlots; ++b) {
+            mbar_init(&blk_full[b], 1);
+            mbar_init(&tmem_free[b], kREpi / 2);  // the group that reads the block
+        }
+        for (int b = 0; b < kRMaxDots; ++b) mbar_init(&dot_free[b], kREpi / 2);
         mbar_init(epi_bar, kREpi);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -454,18 +575,23 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    const uint32_t tmem_dots = tmem + NS * (uint32_t)SC;
 
     if (warp == 0) {
         if (lane == 0) {
             uint32_t kk = 0, kq = 0;
             bool ok = true;
+            const uint32_t q_tx = (uint32_t)(C::KC * (prm.R * 128 + C::kSChunkBytes));
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
-                if (!(ok = mbar_wait(q_empty, (kq & 1) ^ 1, s_abort))) break;
-                mbar_arrive_expect_tx(q_full, C::KC * C::kQChunkBytes);
+                const int qb = kq & 1;
+                if (!(ok = mbar_wait(&q_empty[qb], ((kq >> 1) & 1) ^ 1, s_abort))) break;
+                mbar_arrive_expect_tx(&q_full[qb], q_tx);
+                uint8_t* b_buf = sB + qb * C::kBBytes;
                 for (int c = 0; c < C::KC; ++c) {
-                    tma_load_3d(sQ + c * C::kQChunkBytes, &qmap, q_full, c * kChunkElems, 0, (int)p);
-                    tma_load_3d(sQ + c * C::kQChunkBytes + prm.R * 128, &smap, q_full,
-                                c * kChunkElems, 0, (int)p);
+                    tma_load_3d(b_buf + c * C::kQChunkBytes, &qmap, &q_full[qb], c * kChunkElems, 0,
+                                (int)p);
+                    tma_load_3d(b_buf + C::KC * C::kQChunkBytes + c * C::kSChunkBytes, &smap,
+                                &q_full[qb], c * kChunkElems, 0, (int)p);
                 }
                 ++kq;
                 for (int b = 0; b < T; ++b) {
@@ -482,39 +608,50 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 *s_abort = 1;
                 set_error(prm.status, kDevErrTimeout, 21u);
             }
+            // let every copy this warp started land before the CTA exits
             volatile int never = 0;
             for (uint32_t u = kk > (uint32_t)C::kStages ? kk - C::kStages : 0; u < kk; ++u)
                 mbar_wait(&k_full[u % C::kStages], (u / C::kStages) & 1, &never);
-            if (kq > 0) mbar_wait(q_full, (kq - 1) & 1, &never);
+            for (uint32_t u = kq > 2u ? kq - 2u : 0u; u < kq; ++u)
+                mbar_wait(&q_full[u & 1], (u >> 1) & 1, &never);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kRows, RP);
-            uint32_t kk = 0, kp = 0;
+            constexpr uint32_t idesc_q = idesc_bf16(kRows, SC);
+            constexpr uint32_t idesc_s = idesc_bf16(kRows, kDotCols);
+            uint32_t u = 0, kp = 0;
             bool ok = true;
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
-                if (!(ok = mbar_wait(q_full, kp & 1, s_abort))) break;
-                for (int b = 0; b < T; ++b) {
-                    const int s = kk % C::kStages;
-                    if (!(ok = mbar_wait(&k_full[s], (kk / C::kStages) & 1, s_abort))) break;
-                    // the previous problem's logits of block b have been read
-                    if (!(ok = mbar_wait(&tmem_free[b], (kp & 1) ^ 1, s_abort))) break;
+                const int qb = kp & 1;
+                if (!(ok = mbar_wait(&q_full[qb], (kp >> 1) & 1, s_abort))) break;
+                const uint8_t* b_buf = sB + qb * C::kBBytes;
+                for (int b = 0; b < T; ++b, ++u) {
+                    const int s = u % C::kStages;
+                    if (!(ok = mbar_wait(&k_full[s], (u / C::kStages) & 1, s_abort))) break;
+                    const uint32_t slot = u % NS, ds = u % ND;
+                    // the logit slot's and the dot slot's previous blocks have been read
+                    if (!(ok = mbar_wait(&tmem_free[slot], ((u / NS) & 1) ^ 1, s_abort))) break;
+                    if (!(ok = mbar_wait(&dot_free[ds], ((u / ND) & 1) ^ 1, s_abort))) break;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(b * RP);
+                    const uint32_t d_q = tmem + slot * (uint32_t)SC;
+                    const uint32_t d_s = tmem_dots + ds * (uint32_t)kDotCols;
 #pragma unroll
                     for (int c = 0; c < C::KC; ++c) {
                         const uint64_t ad = sdesc_sw128(sK + s * C::kBlockBytes + c * kChunkBytes);
-                        const uint64_t bd = sdesc_sw128(sQ + c * C::kQChunkBytes);
+                        const uint64_t bq = sdesc_sw128(b_buf + c * C::kQChunkBytes);
+                        const uint64_t bs =
+                            sdesc_sw128(b_buf + C::KC * C::kQChunkBytes + c * C::kSChunkBytes);
 #pragma unroll
-                        for (int k = 0; k < kChunkElems / 16; ++k)
-                            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (c | k) != 0);
+                        for (int k = 0; k < kChunkElems / 16; ++k) {
+                            mma_bf16(d_q, ad + 2 * k, bq + 2 * k, idesc_q, (c | k) != 0);
+                            mma_bf16(d_s, ad + 2 * k, bs + 2 * k, idesc_s, (c | k) != 0);
+                        }
                     }
                     mma_commit(&k_empty[s]);
-                    mma_commit(&blk_full[b]);
-                    ++kk;
+                    mma_commit(&blk_full[slot]);
                 }
                 if (!ok) break;
-                mma_commit(q_empty);
+                mma_commit(&q_empty[qb]);
             }
             if (!ok) {
                 *s_abort = 1;
@@ -529,119 +666,138 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
         const int grp = ew >> 2;           // blocks b with b % 2 == grp
         const int qd = warp & 3;           // TMEM lane quarter
         const int row = qd * 32 + lane;
-        const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
         const int lim = N - n_obs;
+        // blocks whose rows all lie at or before N - n_obs: every query row
+        // sees every key there, no mask.  Columns R .. SC-1 (zero query rows)
+        // need none either: they never reach a head's mean.
+        const int full_blocks = (lim + 1) / kRows;
         const unsigned long long lastmask = prm.lastmask;
         const float scale2 = prm.scale2;   // log2(e) / sqrt(d)
-        uint32_t kp = 0, ke = 0;
+        const float log2_nobs = lg2_approx((float)n_obs);
+        uint32_t ub = 0, ke = 0;           // ub: ring index of the problem's block 0
         bool ok = true;
-        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
-            // softmax state for the QP query columns (the rows of s are at
-            // columns R, R+1 and only read in sweep 3)
-            float m[QP], sm[QP];
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ub += (uint32_t)T) {
+            float m[SC];
 #pragma unroll
-            for (int c = 0; c < QP; ++c) m[c] = -INFINITY;
-            // ---- sweep 1: largest raw logit per query row
+            for (int c = 0; c < SC; ++c) m[c] = -INFINITY;
+            // ---- sweep 1: largest raw logit per query row; the dot columns
+            // complete sum_i and free their slot
             for (int b = grp; b < T; b += 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&blk_full[b], kp & 1, s_abort));
-                if (!ok) break;
-                tc_fence_after();
+                const uint32_t u = ub + (uint32_t)b;
+                const uint32_t slot = u % NS, ds = u % ND;
                 const int j = b * kRows + row;
-                const unsigned long long vm =
-                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
-                uint32_t r[QP];
-                tmem_ld_row<QP>(t_row + (uint32_t)(b * RP), r);
-#pragma unroll
-                for (int c = 0; c < QP; ++c)
-                    if ((vm >> c) & 1ull) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
-            }
-            if (!ok) break;
-#pragma unroll
-            for (int c = 0; c < QP; ++c) {
-                const float mx = warp_max(m[c]);
-                if (lane == 0) redM[ew * RP + c] = mx;
-            }
-            mbar_arrive(epi_bar);
-            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
-            ++ke;
-            if (!ok) break;
-#pragma unroll
-            for (int c = 0; c < QP; ++c) {
-                float mx = redM[c];
-#pragma unroll
-                for (int w = 1; w < 8; ++w) mx = fmaxf(mx, redM[w * RP + c]);
-                m[c] = mx * scale2;  // row max in log2 units
-                sm[c] = 0.f;
-            }
-            // ---- sweep 2: sum of exponentials
-            for (int b = grp; b < T; b += 2) {
-                tc_fence_after();
-                const int j = b * kRows + row;
-                const unsigned long long vm =
-                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
-                uint32_t r[QP];
-                tmem_ld_row<QP>(t_row + (uint32_t)(b * RP), r);
-#pragma unroll
-                for (int c = 0; c < QP; ++c)
-                    if ((vm >> c) & 1ull) sm[c] += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
-            }
-#pragma unroll
-            for (int c = 0; c < QP; ++c) {
-                const float ws = warp_sum(sm[c]);
-                if (lane == 0) redS[ew * RP + c] = ws;
-            }
-            mbar_arrive(epi_bar);
-            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
-            ++ke;
-            if (!ok) break;
-            // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(x - m')
-            const float log2_nobs = log2f((float)n_obs);
-#pragma unroll
-            for (int c = 0; c < QP; ++c) {
-                float t = 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) t += redS[w * RP + c];
-                m[c] += log2f(t) + log2_nobs;
-            }
-            // ---- sweep 3: probabilities -> importance
-            for (int b = grp; b < T; b += 2) {
-                tc_fence_after();
-                const int j = b * kRows + row;
-                const unsigned long long vm =
-                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
                 float iv = 0.f, self = 0.f;
                 if (j < N) {
                     iv = prm.inv_norm[p * prm.ld_ws + j];
                     self = prm.sum_s[p * prm.ld_ws + j];
                 }
-                uint32_t r[RP];
-                if constexpr (QP < RP) {
-                    // query columns, then the 16 columns that start with s
-                    tmem_ld16_at<0, RP>(t_row + (uint32_t)(b * RP), r);
-                    tmem_ld16_at<16, RP>(t_row + (uint32_t)(b * RP), r);
-                    tmem_ld16_at<32, RP>(t_row + (uint32_t)(b * RP), r);
-                    tmem_ld_wait();
-                } else {
-                    tmem_ld_row<RP>(t_row + (uint32_t)(b * RP), r);
-                }
-                float best = -INFINITY, acc = 0.f, dot = 0.f;
+                ok = __all_sync(0xffffffffu, mbar_wait(&blk_full[slot], (u / NS) & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t r[SC], d_hi, d_lo;
+                tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
+                tmem_ld_2cols(tmem_dots + lane_off + ds * (uint32_t)kDotCols, d_hi, d_lo);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&dot_free[ds]);
+                if (b < full_blocks) {
 #pragma unroll
-                for (int c = 0; c < RP; ++c) {
-                    if (c < QP) {
-                        if ((vm >> c) & 1ull) acc += exp2f(__uint_as_float(r[c]) * scale2 - m[c]);
-                        if ((lastmask >> c) & 1ull) {  // last query row of a head
+                    for (int c = 0; c < SC; ++c) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
+                } else {
+                    const unsigned long long vm =
+                        j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+#pragma unroll
+                    for (int c = 0; c < SC; ++c)
+                        if ((vm >> c) & 1ull) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
+                }
+                if (j < N)
+                    prm.sum_s[p * prm.ld_ws + j] =
+                        iv * (__uint_as_float(d_hi) + __uint_as_float(d_lo)) - self;
+            }
+            if (!ok) break;
+            post_partials<SC>(m, redM, ew, OpMax{});
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+            float mlo, mhi;  // this lane's columns: row max in log2 units
+            fold_partials<SC>(redM, mlo, mhi, OpMax{});
+            mlo *= scale2;
+            mhi *= scale2;
+            broadcast_columns<SC>(m, mlo, mhi);
+            // ---- sweep 2: sum of exponentials
+            float sm[SC];
+#pragma unroll
+            for (int c = 0; c < SC; ++c) sm[c] = 0.f;
+            for (int b = grp; b < T; b += 2) {
+                const uint32_t slot = (ub + (uint32_t)b) % NS;
+                tc_fence_after();
+                uint32_t r[SC];
+                tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
+                tmem_ld_wait();
+                if (b < full_blocks) {
+#pragma unroll
+                    for (int c = 0; c < SC; ++c)
+                        sm[c] += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                } else {
+                    const int j = b * kRows + row;
+                    const unsigned long long vm =
+                        j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+#pragma unroll
+                    for (int c = 0; c < SC; ++c)
+                        if ((vm >> c) & 1ull)
+                            sm[c] += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                }
+            }
+            post_partials<SC>(sm, redS, ew, OpAdd{});
+            mbar_arrive(epi_bar);
+            ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
+            ++ke;
+            if (!ok) break;
+            // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(x - m')
+            {
+                float slo, shi;
+                fold_partials<SC>(redS, slo, shi, OpAdd{});
+                mlo += lg2_approx(slo) + log2_nobs;
+                if constexpr (SC > 32) mhi += lg2_approx(shi) + log2_nobs;
+                broadcast_columns<SC>(m, mlo, mhi);
+            }
+            // ---- sweep 3: probabilities -> importance; frees the logit slot
+            for (int b = grp; b < T; b += 2) {
+                const uint32_t slot = (ub + (uint32_t)b) % NS;
+                tc_fence_after();
+                const int j = b * kRows + row;
+                uint32_t r[SC];
+                tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&tmem_free[slot]);
+                const unsigned long long vm =
+                    b < full_blocks ? ~0ull
+                                    : (j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull));
+                float best = -INFINITY, acc = 0.f;
+                if (b < full_blocks) {
+#pragma unroll
+                    for (int c = 0; c < SC; ++c) {
+                        acc += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                        if (HEAD > 0 ? (c % (HEAD > 0 ? HEAD : 1) == HEAD - 1) : ((lastmask >> c) & 1ull)) {
+                            best = fmaxf(best, acc);  // last query row of a head
+                            acc = 0.f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < SC; ++c) {
+                        if ((vm >> c) & 1ull)
+                            acc += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                        if ((lastmask >> c) & 1ull) {
                             best = fmaxf(best, acc);
                             acc = 0.f;
                         }
                     }
-                    if (c == prm.R || c == prm.R + 1) dot += __uint_as_float(r[c]);
                 }
-                tc_fence_before();
-                mbar_arrive(&tmem_free[b]);  // block b's TMEM columns may be reused
-                if (j < N) {
-                    prm.I[p * prm.ld + j] = best;
-                    prm.sum_s[p * prm.ld_ws + j] = iv * dot - self;
-                }
+                if (j < N) prm.I[p * prm.ld + j] = best;
             }
         }
         if (!ok) {
@@ -656,17 +812,25 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     if (warp == 1) tmem_dealloc(tmem, kRTmemCols);
 }
 
+// Ring sizes of the resident variant for T key blocks and SC logit columns:
+// at least T logit slots (and a few more, so the next problem's first MMAs
+// fit beside this problem's logits), the rest of the 512 columns as dot slots.
+// Returns false when a problem does not fit.
+bool resident_rings(int T, int SC, int* ns, int* nd) {
+    const int reserve = 128;  // dot columns kept when T leaves room
+    int n = (int)(kRTmemCols - reserve) / SC;
+    if (n < T) n = T;
+    const int d = ((int)kRTmemCols - n * SC) / kDotCols;
+    if (n > kRMaxSlots || d < 1) return false;
+    *ns = n;
+    *nd = d < kRMaxDots ? d : kRMaxDots;
+    return true;
+}
+
 template <int D, int RP>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = ICfg<D, RP>;
-    CUtensorMap kmap, qmap, smap;
     const int R = a.G * a.n_obs;
-    if (!make_map_3d_bf16(&kmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
-        return cudaErrorInvalidValue;
-    if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
-        return cudaErrorInvalidValue;
-    if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, RP - R))
-        return cudaErrorInvalidValue;
     IParams prm{};
     prm.P = a.P;
     prm.N = a.N;
@@ -692,15 +856,37 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     const int64_t cap = (int64_t)sm_count();
     const int64_t grid = a.P < cap ? a.P : cap;
     const int T = (a.N + kRows - 1) / kRows;
-    if (T <= kRMaxBlocks && T * RP <= (int)kRTmemCols) {
-        using RC = RCfg<D, RP>;
-        auto kern = R <= 32 ? importance_tcr_kernel<D, RP, 32> : importance_tcr_kernel<D, RP, 48>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)RC::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, smap, prm);
+    CUtensorMap kmap, qmap, smap;
+    if (!make_map_3d_bf16(&kmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
+        return cudaErrorInvalidValue;
+    if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
+        return cudaErrorInvalidValue;
+    const int SC = R <= 32 ? 32 : 48;
+    if (resident_rings(T, SC, &prm.ns, &prm.nd)) {
+        // s rows: hi, lo and 14 zero rows -> the N = 16 dot MMA
+        if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, kDotCols))
+            return cudaErrorInvalidValue;
+        if (SC == 32) {
+            using RC = RCfg<D, 32>;
+            auto kern = (R == 32 && a.n_obs == 8) ? importance_tcr_kernel<D, 32, 8>
+                                                  : importance_tcr_kernel<D, 32, 0>;
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)RC::kSmemBytes);
+            if (e != cudaSuccess) return e;
+            kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, smap, prm);
+        } else {
+            using RC = RCfg<D, 48>;
+            auto kern = importance_tcr_kernel<D, 48, 0>;
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)RC::kSmemBytes);
+            if (e != cudaSuccess) return e;
+            kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, smap, prm);
+        }
         return cudaGetLastError();
     }
+    // two-pass variant: the query rows, then s (hi, lo) and zeros up to RP rows
+    if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, RP - R))
+        return cudaErrorInvalidValue;
     auto kern = importance_tc_kernel<D, RP>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
