@@ -82,7 +82,7 @@ struct IParams {
     // lastmask: c is the last query row of its head.
     unsigned long long colmask[kMaxObs + 1];
     unsigned long long lastmask;
-    int ns, nd;  // resident variant: logit slots and dot slots in TMEM
+    int ns;  // resident variant: logit slots in TMEM
 };
 
 RKV_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
@@ -357,21 +357,25 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 // Resident variant: when a problem's logits fit in TMEM, each key block is
 // multiplied once and its logits stay in TMEM while the epilogue sweeps them
 // three times (row max, sum of exponentials, probabilities); the keys are
-// read from memory once.  TMEM is split into a ring of NS logit slots of SC
-// columns (the query rows) and a ring of ND dot slots of 16 columns (k . s_hi,
-// k . s_lo from a second N = 16 MMA).  Sweep 1 releases a block's dot slot and
-// sweep 3 its logit slot, so the MMAs of the next problem run while this one
-// is swept and the key stream keeps going.  NS >= T keeps the ring free of
-// deadlock (a problem never waits for one of its own logit slots); so does
-// ND >= 1 (sweep 1 of a block needs that block's MMA only).  The query rows
-// are double-buffered.  Eight epilogue warps in two groups take alternate key
-// blocks.
-constexpr int kRThreads = 64 + 256;
+// read from memory once.  TMEM is a ring of NS slots of SC columns (the query
+// rows, padded); sweep 3 releases a block's slot, so the MMAs of the next
+// problem run while this one is swept and the key stream keeps going.
+// NS >= T keeps the ring free of deadlock (a problem never waits for one of
+// its own slots).  The query rows are double-buffered.
+//
+// The tensor pipe takes about as long for one M = 128 MMA of N = 16 as of
+// N = 128, so k_i . s (which completes sum_i) is not a second MMA per K step:
+// two dot warps read each key block from shared memory, take the dot product
+// with s in fp32, and release the stage together with the MMA.
+//
+// Warps: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..9 the epilogue in
+// two groups taking alternate key blocks, 10..11 the dot warps.
 constexpr int kREpi = 256;
+constexpr int kRDotWarps = 4;
+constexpr int kRThreads = 64 + kREpi + 32 * kRDotWarps;
 constexpr uint32_t kRTmemCols = 512;
 constexpr int kRMaxSlots = 16;
-constexpr int kRMaxDots = 32;
-constexpr int kDotCols = 16;
+constexpr int kSRows = 2;  // s_hi, s_lo: the rows of s the dot warps read
 constexpr size_t kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
 
 template <int D, int SC>
@@ -379,16 +383,16 @@ struct RCfg {
     static constexpr int KC = D / kChunkElems;
     static constexpr int kBlockBytes = KC * kChunkBytes;
     static constexpr int kQChunkBytes = SC * 128;
-    static constexpr int kSChunkBytes = kDotCols * 128;
+    static constexpr int kSChunkBytes = 1024;  // kSRows rows used; 1024-byte aligned
     static constexpr int kBBytes = KC * (kQChunkBytes + kSChunkBytes);  // one problem's B operands
-    static constexpr int kFixedBars = 4 + 2 * kRMaxSlots + kRMaxDots + 2;
-    static constexpr size_t kFixed =
-        1024 + 2 * (size_t)kBBytes + sizeof(float) * 16 * SC + 8 * kFixedBars + 16;
+    static constexpr int kFixedBars = 4 + 2 * kRMaxSlots + 2;
+    static constexpr size_t kRedBytes = sizeof(float) * (16 * SC + kRDotWarps * D);
+    static constexpr size_t kFixed = 1024 + 2 * (size_t)kBBytes + kRedBytes + 8 * kFixedBars + 16;
     static constexpr int kFit = (int)((kSmemLimit - kFixed) / (kBlockBytes + 16));
     static constexpr int kStages = kFit < 12 ? kFit : 12;
     static constexpr size_t kBOff = (size_t)kStages * kBlockBytes;
     static constexpr size_t kRedOff = kBOff + 2 * (size_t)kBBytes;
-    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * SC;
+    static constexpr size_t kBarOff = kRedOff + kRedBytes;
     static constexpr int kNumBars = 2 * kStages + kFixedBars;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
     static_assert(kStages >= 4 && kSmemBytes <= kSmemLimit, "shared memory plan");
@@ -405,12 +409,6 @@ RKV_DEV void tmem_ld16_at(uint32_t taddr, uint32_t (&r)[RP]) {
           "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]),
           "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15])
         : "r"(taddr + (uint32_t)OFF));
-}
-
-RKV_DEV void tmem_ld_2cols(uint32_t taddr, uint32_t& a, uint32_t& b) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-                 : "=r"(a), "=r"(b)
-                 : "r"(taddr));
 }
 
 // the SC query columns of one key row (no wait)
@@ -501,6 +499,50 @@ RKV_DEV void broadcast_columns(float (&v)[SC], float lo, float hi) {
     for (int c = 32; c < SC; ++c) v[c] = __shfl_sync(0xffffffffu, hi, c - 32);
 }
 
+// Eight bf16 of a 128-byte-swizzled K-major tile: 16-byte unit u of row r
+// sits at unit u ^ (r mod 8) of the row (the TMA 128-byte swizzle).
+RKV_DEV uint4 swizzled_unit(const uint8_t* tile, int r, int u) {
+    return *reinterpret_cast<const uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// the two bf16 of a 32-bit word as a packed fp32 pair (low element first)
+RKV_DEV unsigned long long bf16x2_to_f32x2(uint32_t w) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+
+// acc.xy += a.xy * b.xy on packed fp32 pairs
+RKV_DEV void fma_f32x2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+RKV_DEV float f32x2_sum(unsigned long long v) {
+    return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+}
+
+// k . s over the D elements of row r of a key block (KC swizzled chunks of
+// 64), s in fp32; four packed accumulators keep the FMA chains short
+template <int KC>
+RKV_DEV float row_dot(const uint8_t* blk, int r, const float* s32) {
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < KC; ++c) {
+        const uint8_t* tile = blk + c * kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint4 k = swizzled_unit(tile, r, u);
+            const ulonglong2 s01 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8);
+            const ulonglong2 s23 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8 + 4);
+            fma_f32x2(acc[0], bf16x2_to_f32x2(k.x), s01.x);
+            fma_f32x2(acc[1], bf16x2_to_f32x2(k.y), s01.y);
+            fma_f32x2(acc[2], bf16x2_to_f32x2(k.z), s23.x);
+            fma_f32x2(acc[3], bf16x2_to_f32x2(k.w), s23.y);
+        }
+    }
+    return (f32x2_sum(acc[0]) + f32x2_sum(acc[1])) + (f32x2_sum(acc[2]) + f32x2_sum(acc[3]));
+}
+
 // HEAD > 0: the query rows form SC / HEAD heads of HEAD rows (R == SC), so a
 // head's last row is known at compile time; HEAD == 0 reads it from lastmask.
 template <int D, int SC, int HEAD>
@@ -516,6 +558,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     uint8_t* sB = smem + C::kBOff;  // [2][ KC query chunks | KC s chunks ]
     float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [8][SC]
     float* redS = redM + 8 * SC;                                 // [8][SC]
+    float* sDot = redS + 8 * SC;                                 // [kRDotWarps][D]: s in fp32
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* k_full = bars;
     uint64_t* k_empty = k_full + C::kStages;
@@ -523,8 +566,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     uint64_t* q_empty = q_full + 2;             // [2]
     uint64_t* blk_full = q_empty + 2;           // [kRMaxSlots]
     uint64_t* tmem_free = blk_full + kRMaxSlots;  // [kRMaxSlots]
-    uint64_t* dot_free = tmem_free + kRMaxSlots;  // [kRMaxDots]
-    uint64_t* epi_bar = dot_free + kRMaxDots;
+    uint64_t* epi_bar = tmem_free + kRMaxSlots;
     uint64_t* drain_bar = epi_bar + 1;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -532,12 +574,12 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N, n_obs = prm.n_obs;
-    const uint32_t NS = (uint32_t)prm.ns, ND = (uint32_t)prm.nd;
+    const uint32_t NS = (uint32_t)prm.ns;
     for (int k = threadIdx.x; k <= n_obs && k <= kMaxObs; k += blockDim.x) s_colmask[k] = prm.colmask[k];
     const int T = (N + kRows - 1) / kRows;
 
     // query rows R .. SC-1 of both B buffers are never loaded: zero them once
-    // (their logit columns are masked, zeros keep them finite)
+    // (their logit columns are never used, zeros keep them finite)
     if (prm.R < SC) {
         const int pad = (SC - prm.R) * 128;
         for (int i = threadIdx.x; i < 2 * C::KC * pad / 16; i += blockDim.x) {
@@ -551,17 +593,16 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], 1 + kRDotWarps);  // the MMAs' commit and each dot warp
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(&q_full[q], 1);
-            mbar_init(&q_empty[q], 1);
+            mbar_init(&q_empty[q], 1 + kRDotWarps);
         }
         for (int b = 0; b < kRMaxSlots; ++b) {
             mbar_init(&blk_full[b], 1);
             mbar_init(&tmem_free[b], kREpi / 2);  // the group that reads the block
         }
-        for (int b = 0; b < kRMaxDots; ++b) mbar_init(&dot_free[b], kREpi / 2);
         mbar_init(epi_bar, kREpi);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
@@ -575,13 +616,12 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t tmem_dots = tmem + NS * (uint32_t)SC;
 
     if (warp == 0) {
         if (lane == 0) {
             uint32_t kk = 0, kq = 0;
             bool ok = true;
-            const uint32_t q_tx = (uint32_t)(C::KC * (prm.R * 128 + C::kSChunkBytes));
+            const uint32_t q_tx = (uint32_t)(C::KC * (prm.R + kSRows) * 128);
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
                 const int qb = kq & 1;
                 if (!(ok = mbar_wait(&q_empty[qb], ((kq >> 1) & 1) ^ 1, s_abort))) break;
@@ -618,7 +658,6 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_q = idesc_bf16(kRows, SC);
-            constexpr uint32_t idesc_s = idesc_bf16(kRows, kDotCols);
             uint32_t u = 0, kp = 0;
             bool ok = true;
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
@@ -628,24 +667,18 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 for (int b = 0; b < T; ++b, ++u) {
                     const int s = u % C::kStages;
                     if (!(ok = mbar_wait(&k_full[s], (u / C::kStages) & 1, s_abort))) break;
-                    const uint32_t slot = u % NS, ds = u % ND;
-                    // the logit slot's and the dot slot's previous blocks have been read
+                    const uint32_t slot = u % NS;
+                    // the slot's previous block has been swept
                     if (!(ok = mbar_wait(&tmem_free[slot], ((u / NS) & 1) ^ 1, s_abort))) break;
-                    if (!(ok = mbar_wait(&dot_free[ds], ((u / ND) & 1) ^ 1, s_abort))) break;
                     tc_fence_after();
                     const uint32_t d_q = tmem + slot * (uint32_t)SC;
-                    const uint32_t d_s = tmem_dots + ds * (uint32_t)kDotCols;
 #pragma unroll
                     for (int c = 0; c < C::KC; ++c) {
                         const uint64_t ad = sdesc_sw128(sK + s * C::kBlockBytes + c * kChunkBytes);
                         const uint64_t bq = sdesc_sw128(b_buf + c * C::kQChunkBytes);
-                        const uint64_t bs =
-                            sdesc_sw128(b_buf + C::KC * C::kQChunkBytes + c * C::kSChunkBytes);
 #pragma unroll
-                        for (int k = 0; k < kChunkElems / 16; ++k) {
+                        for (int k = 0; k < kChunkElems / 16; ++k)
                             mma_bf16(d_q, ad + 2 * k, bq + 2 * k, idesc_q, (c | k) != 0);
-                            mma_bf16(d_s, ad + 2 * k, bs + 2 * k, idesc_s, (c | k) != 0);
-                        }
                     }
                     mma_commit(&k_empty[s]);
                     mma_commit(&blk_full[slot]);
@@ -660,6 +693,85 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             mma_commit(drain_bar);
             volatile int never = 0;
             mbar_wait(drain_bar, 0, &never);
+        }
+    } else if (warp >= 2 + kREpi / 32) {
+        // ---- dot warps: sum_i = inv_i (k_i . s) - |khat_i|^2 (the key-stats
+        // kernel leaves |khat_i|^2 in sum_s), rows dw * 64 + lane and + 32 of
+        // every key block.  inv_i and |khat_i|^2 are loaded two blocks ahead
+        // (a cursor over (problem, block) pairs) so that no store waits on them.
+        const int dw = warp - (2 + kREpi / 32);
+        const int r0 = dw * 32 + lane;
+        float* s32 = sDot + dw * D;
+        auto fetch = [&](int64_t q, int c, float (&v)[2]) {
+            const int j0 = c * kRows + r0;
+            v[0] = v[1] = 0.f;
+            if (q < prm.P && j0 < N) {
+                v[0] = prm.inv_norm[q * prm.ld_ws + j0];
+                v[1] = prm.sum_s[q * prm.ld_ws + j0];
+            }
+        };
+        auto advance = [&](int64_t& q, int& c) {
+            if (++c == T) {
+                c = 0;
+                q += gridDim.x;
+            }
+        };
+        int64_t p = blockIdx.x, fq = blockIdx.x;
+        int b = 0, fc = 0;
+        uint32_t kk = 0, kp = 0;
+        bool ok = true;
+        float va[2], vb[2];
+        fetch(fq, fc, va);
+        advance(fq, fc);
+        fetch(fq, fc, vb);
+        advance(fq, fc);
+        // one key block of problem p with its prefetched inv / |khat|^2
+        auto dot_block = [&](float (&v)[2]) {
+            if (b == 0) {
+                // s = s_hi + s_lo in fp32: rows 0 and 1 of each s chunk (row
+                // r's 16-byte unit u at unit u ^ r)
+                const int qb = kp & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&q_full[qb], (kp >> 1) & 1, s_abort));
+                if (!ok) return;
+                const uint8_t* s_buf = sB + qb * C::kBBytes + C::KC * C::kQChunkBytes;
+                __syncwarp();  // the previous problem's reads of s32 are done
+                for (int e = lane; e < D; e += 32) {
+                    const int c = e / kChunkElems, x = e % kChunkElems, u = x >> 3, w = x & 7;
+                    const uint8_t* ch = s_buf + c * C::kSChunkBytes;
+                    const __nv_bfloat16 hi =
+                        reinterpret_cast<const __nv_bfloat16*>(ch + ((u ^ 0) << 4))[w];
+                    const __nv_bfloat16 lo =
+                        reinterpret_cast<const __nv_bfloat16*>(ch + 128 + ((u ^ 1) << 4))[w];
+                    s32[e] = __bfloat162float(hi) + __bfloat162float(lo);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_empty[qb]);
+            }
+            const int st = kk % C::kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(&k_full[st], (kk / C::kStages) & 1, s_abort));
+            if (!ok) return;
+            const uint8_t* blk = sK + st * C::kBlockBytes;
+            const float d0 = row_dot<C::KC>(blk, r0, s32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&k_empty[st]);
+            const int j0 = b * kRows + r0;
+            if (j0 < N) prm.sum_s[p * prm.ld_ws + j0] = v[0] * d0 - v[1];
+            ++kk;
+            if (b + 1 == T) ++kp;
+            advance(p, b);
+        };
+        while (ok && p < prm.P) {
+            dot_block(va);
+            fetch(fq, fc, va);
+            advance(fq, fc);
+            if (!ok || p >= prm.P) break;
+            dot_block(vb);
+            fetch(fq, fc, vb);
+            advance(fq, fc);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            set_error(prm.status, kDevErrTimeout, 24u);
         }
     } else {
         const int ew = warp - 2;           // 0..7
@@ -681,26 +793,17 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             float m[SC];
 #pragma unroll
             for (int c = 0; c < SC; ++c) m[c] = -INFINITY;
-            // ---- sweep 1: largest raw logit per query row; the dot columns
-            // complete sum_i and free their slot
+            // ---- sweep 1: largest raw logit per query row
             for (int b = grp; b < T; b += 2) {
                 const uint32_t u = ub + (uint32_t)b;
-                const uint32_t slot = u % NS, ds = u % ND;
+                const uint32_t slot = u % NS;
                 const int j = b * kRows + row;
-                float iv = 0.f, self = 0.f;
-                if (j < N) {
-                    iv = prm.inv_norm[p * prm.ld_ws + j];
-                    self = prm.sum_s[p * prm.ld_ws + j];
-                }
                 ok = __all_sync(0xffffffffu, mbar_wait(&blk_full[slot], (u / NS) & 1, s_abort));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t r[SC], d_hi, d_lo;
+                uint32_t r[SC];
                 tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
-                tmem_ld_2cols(tmem_dots + lane_off + ds * (uint32_t)kDotCols, d_hi, d_lo);
                 tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&dot_free[ds]);
                 if (b < full_blocks) {
 #pragma unroll
                     for (int c = 0; c < SC; ++c) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
@@ -711,9 +814,6 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                     for (int c = 0; c < SC; ++c)
                         if ((vm >> c) & 1ull) m[c] = fmaxf(m[c], __uint_as_float(r[c]));
                 }
-                if (j < N)
-                    prm.sum_s[p * prm.ld_ws + j] =
-                        iv * (__uint_as_float(d_hi) + __uint_as_float(d_lo)) - self;
             }
             if (!ok) break;
             post_partials<SC>(m, redM, ew, OpMax{});
@@ -763,7 +863,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 if constexpr (SC > 32) mhi += lg2_approx(shi) + log2_nobs;
                 broadcast_columns<SC>(m, mlo, mhi);
             }
-            // ---- sweep 3: probabilities -> importance; frees the logit slot
+            // ---- sweep 3: probabilities -> importance; frees the slot
             for (int b = grp; b < T; b += 2) {
                 const uint32_t slot = (ub + (uint32_t)b) % NS;
                 tc_fence_after();
@@ -812,18 +912,13 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
     if (warp == 1) tmem_dealloc(tmem, kRTmemCols);
 }
 
-// Ring sizes of the resident variant for T key blocks and SC logit columns:
-// at least T logit slots (and a few more, so the next problem's first MMAs
-// fit beside this problem's logits), the rest of the 512 columns as dot slots.
-// Returns false when a problem does not fit.
-bool resident_rings(int T, int SC, int* ns, int* nd) {
-    const int reserve = 128;  // dot columns kept when T leaves room
-    int n = (int)(kRTmemCols - reserve) / SC;
-    if (n < T) n = T;
-    const int d = ((int)kRTmemCols - n * SC) / kDotCols;
-    if (n > kRMaxSlots || d < 1) return false;
+// Ring size of the resident variant for T key blocks of SC logit columns:
+// as many slots as TMEM holds; false when a problem does not fit.
+bool resident_ring(int T, int SC, int* ns) {
+    int n = (int)kRTmemCols / SC;
+    if (n > kRMaxSlots) n = kRMaxSlots;
+    if (T > n) return false;
     *ns = n;
-    *nd = d < kRMaxDots ? d : kRMaxDots;
     return true;
 }
 
@@ -862,9 +957,9 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
         return cudaErrorInvalidValue;
     const int SC = R <= 32 ? 32 : 48;
-    if (resident_rings(T, SC, &prm.ns, &prm.nd)) {
-        // s rows: hi, lo and 14 zero rows -> the N = 16 dot MMA
-        if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, kDotCols))
+    if (resident_ring(T, SC, &prm.ns)) {
+        // s rows hi, lo for the dot warps
+        if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, kSRows))
             return cudaErrorInvalidValue;
         if (SC == 32) {
             using RC = RCfg<D, 32>;
