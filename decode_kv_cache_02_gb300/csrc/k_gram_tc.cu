@@ -117,20 +117,21 @@ constexpr uint32_t kIdesc = idesc_bf16(kRows, kRows);
 // at most 2^-19.
 constexpr float kSimScale = 262144.0f;
 
-// Reduce-scatter over the warp: on return, lane L holds in v[0] the sum over
+// Reduce-scatter over the warp of fp32 values kept as bits in v (the raw
+// accumulator registers, reused): on return, lane L holds in v[0] the sum over
 // all lanes of their v[L].
-RKV_DEV float warp_column_sums(float (&v)[32], int lane) {
+RKV_DEV float warp_column_sums_bits(uint32_t (&v)[32], int lane) {
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) {
         const bool upper = (lane & w) != 0;
 #pragma unroll
         for (int k = 0; k < w; ++k) {
-            const float send = upper ? v[k] : v[k + w];
-            const float keep = upper ? v[k + w] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            const float send = __uint_as_float(upper ? v[k] : v[k + w]);
+            const float keep = __uint_as_float(upper ? v[k + w] : v[k]);
+            v[k] = __float_as_uint(keep + __shfl_xor_sync(0xffffffffu, send, w));
         }
     }
-    return v[0];
+    return __uint_as_float(v[0]);
 }
 
 RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -344,6 +345,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         const int row = q * 32 + lane;        // accumulator row of this thread
         const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16);
         const int Cn = N - prm.n_obs;
+        const bool tau_pos = prm.tau > 0.f;
         const float inv_nm1 = 1.0f / (float)(N - 1);
         uint32_t kacc = 0, kepi = 0, kinv = 0;
         bool ok = true;
@@ -379,7 +381,6 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                 const bool valid_i = i < N;
                 const float inv_i = valid_i ? inv[i] : 0.f;
                 const float thr = valid_i ? prm.tau / inv_i : INFINITY;
-                const bool thr_pos = thr > 0.f;
                 float sim_row = 0.f;
                 int newer = 0;
                 for (int J = I; J < T; ++J) {
@@ -404,28 +405,86 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     ++kacc;
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h) {
-                        const int chunk = J * 4 + cgr * kChunksPerWarp + h;  // chunk of the problem
+                        const int cq = cgr * kChunksPerWarp + h;  // 32-column chunk within the tile
+                        const int chunk = J * 4 + cq;             // chunk of the problem
                         const int jb = chunk * 32;
-                        // column e of this chunk is the row itself (diagonal blocks)
-                        const int e_self = diag ? i - jb : -1;
-                        bool hot = !thr_pos;
-                        if (!hot) {
-                            int mb;
-                            if (diag) {
-                                uint32_t m[32];
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) m[e] = e == e_self ? 0u : r[h][e];
-                                mb = raw_max32(m);
-                            } else {
-                                mb = raw_max32(r[h]);
+                        if (tau_pos) {
+                            // tau > 0: key rows past N are zero (TMA fill), so
+                            // their S is 0 and never passes; only the row's own
+                            // column needs excluding, and it lies in the chunk of
+                            // a diagonal tile that matches the warp's lane
+                            // quarter, at column e = lane
+                            const bool self_chunk = diag && cq == q;
+                            bool hot = self_chunk;  // S_ii > tau there anyway
+                            if (!hot) {
+                                const int mb = raw_max32(r[h]);
+                                hot = mb > 0 && __int_as_float(mb) * invmax[chunk] > thr;
                             }
-                            hot = mb > 0 && __int_as_float(mb) * invmax[chunk] > thr;
-                        }
-                        if (__any_sync(0xffffffffu, hot)) {
-                            // exact path: S_ij > tau for the columns that exist
+                            if (__any_sync(0xffffffffu, hot)) {
+                                const float4* iv4 = reinterpret_cast<const float4*>(inv + jb);
+                                uint32_t hits = 0;
+                                float rs = 0.f;  // the row's hits before inv_i
+                                if (!diag) {
+#pragma unroll
+                                    for (int e4 = 0; e4 < 8; ++e4) {
+                                        const float4 w4 = iv4[e4];
+                                        const float iv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                        for (int u = 0; u < 4; ++u) {
+                                            const int e = e4 * 4 + u;
+                                            const float t = __uint_as_float(r[h][e]) * iv[u];
+                                            const bool hit = t > thr;
+                                            rs += hit ? t : 0.f;
+                                            hits |= hit ? (1u << e) : 0u;
+                                            // S_ij of the hits, in the registers of the raw values
+                                            r[h][e] = __float_as_uint(hit ? t * inv_i : 0.f);
+                                        }
+                                    }
+                                    // column side: lane L adds column jb+L over the warp's rows
+                                    const float cs = warp_column_sums_bits(r[h], lane);
+                                    if (cs != 0.f)
+                                        atomicAdd(&s_sim[jb + lane], __float2int_rn(cs * kSimScale));
+                                    newer += __popc(hits);  // every column is newer
+                                } else if (self_chunk) {
+#pragma unroll
+                                    for (int e4 = 0; e4 < 8; ++e4) {
+                                        const float4 w4 = iv4[e4];
+                                        const float iv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                        for (int u = 0; u < 4; ++u) {
+                                            const int e = e4 * 4 + u;
+                                            const float t = __uint_as_float(r[h][e]) * iv[u];
+                                            const bool hit = t > thr && e != lane;
+                                            rs += hit ? t : 0.f;
+                                            hits |= hit ? (1u << e) : 0u;
+                                        }
+                                    }
+                                    newer += __popc(hits & (lane == 31 ? 0u : (0xffffffffu << (lane + 1))));
+                                } else {
+#pragma unroll
+                                    for (int e4 = 0; e4 < 8; ++e4) {
+                                        const float4 w4 = iv4[e4];
+                                        const float iv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                        for (int u = 0; u < 4; ++u) {
+                                            const int e = e4 * 4 + u;
+                                            const float t = __uint_as_float(r[h][e]) * iv[u];
+                                            const bool hit = t > thr;
+                                            rs += hit ? t : 0.f;
+                                            hits |= hit ? (1u << e) : 0u;
+                                        }
+                                    }
+                                    // chunks right of the row's own chunk hold newer tokens
+                                    if (cq > q) newer += __popc(hits);
+                                }
+                                sim_row += rs * inv_i;
+                            }
+                        } else {
+                            // tau <= 0: every existing pair counts; columns past N
+                            // and the row's own column are excluded one by one
+                            const int e_self = diag ? i - jb : -1;
                             const int e_end = min(32, N - jb);
                             const float4* iv4 = reinterpret_cast<const float4*>(inv + jb);
-                            float v[32];
                             uint32_t hits = 0;
                             float row_sum = 0.f;
 #pragma unroll
@@ -437,14 +496,13 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                                     const int e = e4 * 4 + u;
                                     const float t = __uint_as_float(r[h][e]) * iv[u];
                                     const bool hit = (t > thr) && (e < e_end) && (e != e_self);
-                                    v[e] = hit ? t * inv_i : 0.f;
-                                    row_sum += v[e];
+                                    const float v = hit ? t * inv_i : 0.f;
+                                    row_sum += v;
                                     hits |= (hit ? 1u : 0u) << e;
+                                    r[h][e] = __float_as_uint(v);
                                 }
                             }
                             sim_row += row_sum;
-                            // newer similar tokens: every column of a block right
-                            // of the diagonal, and columns past the row itself
                             const uint32_t newer_mask =
                                 !diag ? 0xffffffffu
                                       : (e_self >= 31 ? 0u
@@ -452,8 +510,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                                                                     : (0xffffffffu << (e_self + 1))));
                             newer += __popc(hits & newer_mask);
                             if (!diag) {
-                                // column side: lane L adds column jb+L over the warp's rows
-                                const float cs = warp_column_sums(v, lane);
+                                const float cs = warp_column_sums_bits(r[h], lane);
                                 if (cs != 0.f) atomicAdd(&s_sim[jb + lane], __float2int_rn(cs * kSimScale));
                             }
                         }
