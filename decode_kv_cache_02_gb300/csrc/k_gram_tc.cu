@@ -205,13 +205,13 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
         }
         for (int s = 0; s < kAccBufs; ++s) {
             mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], kEpiThreads);
+            mbar_init(&acc_empty[s], kEpiWarps);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&inv_full[s], 1);
-            mbar_init(&inv_empty[s], kEpiThreads);
+            mbar_init(&inv_empty[s], kEpiWarps);
         }
-        mbar_init(epi_bar, kEpiThreads);
+        mbar_init(epi_bar, kEpiWarps);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -373,7 +373,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                 invmax[x] = m;
             }
             // the previous problem's s_sim / s_newer entries are zero again
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
             ++kepi;
             for (int I = 0; ok && I < T; ++I) {
@@ -401,7 +401,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                                        r[h]);
                     tmem_ld_wait();
                     tc_fence_before();
-                    mbar_arrive(&acc_empty[acc]);  // the accumulator is in registers now
+                    mbar_arrive_warp(&acc_empty[acc]);  // the accumulator is in registers now
                     ++kacc;
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h) {
@@ -526,10 +526,10 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                 }
             }
             if (!ok) break;
-            mbar_arrive(&inv_empty[ib]);
+            mbar_arrive_warp(&inv_empty[ib]);
             ++kinv;
             // every contribution to this problem is in shared memory after this
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
             ++kepi;
             if (!ok) break;

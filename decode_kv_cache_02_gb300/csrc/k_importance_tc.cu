@@ -135,9 +135,9 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         mbar_init(q_empty, 1);
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], kEpi);
+            mbar_init(&acc_empty[a], kEpi / 32);
         }
-        mbar_init(epi_bar, kEpi);
+        mbar_init(epi_bar, kEpi / 32);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -269,7 +269,7 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&acc_empty[a]);
+                mbar_arrive_warp(&acc_empty[a]);
                 ++ka;
             }
             if (!ok) break;
@@ -279,7 +279,7 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 const float mx = warp_max(m[c]);
                 if (lane == 0) redM[qd * RP + c] = mx;
             }
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
@@ -291,7 +291,7 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 if (lane == 0) redS[qd * RP + c] = ws;
                 m[c] = M;
             }
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
@@ -333,7 +333,7 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&acc_empty[a]);
+                mbar_arrive_warp(&acc_empty[a]);
                 ++ka;
                 if (j < N) {
                     prm.I[p * prm.ld + j] = best;
@@ -601,9 +601,9 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         for (int b = 0; b < kRMaxSlots; ++b) {
             mbar_init(&blk_full[b], 1);
-            mbar_init(&tmem_free[b], kREpi / 2);  // the group that reads the block
+            mbar_init(&tmem_free[b], kREpi / 64);  // the group (its warps) that reads the block
         }
-        mbar_init(epi_bar, kREpi);
+        mbar_init(epi_bar, kREpi / 32);
         mbar_init(drain_bar, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -817,7 +817,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             if (!ok) break;
             post_partials<SC>(m, redM, ew, OpMax{});
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
@@ -851,7 +851,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 }
             }
             post_partials<SC>(sm, redS, ew, OpAdd{});
-            mbar_arrive(epi_bar);
+            mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
@@ -872,7 +872,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&tmem_free[slot]);
+                mbar_arrive_warp(&tmem_free[slot]);
                 const unsigned long long vm =
                     b < full_blocks ? ~0ull
                                     : (j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull));

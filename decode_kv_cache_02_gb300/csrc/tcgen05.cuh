@@ -26,6 +26,13 @@ RKV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
 RKV_DEV void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// One arrival for the whole (converged) warp, after every lane has reached
+// this point: barriers counted in warps instead of threads take 32 times fewer
+// shared-memory arrive operations.
+RKV_DEV void mbar_arrive_warp(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 RKV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
