@@ -43,11 +43,11 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314681344 / 1024),
-        "importance_tc": ("k_importance_tc.cu", "0b1e9411925fea548bd6ec7ae002d2f47619c1c43e4fddcbf028e91152f9f228", 332675072 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "edfbc516d5ac99deb85aed8e6077c11b9a0b9e549cc8a8f7ae709909a0191c70", 322827776 / 1024),
-        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", 4742912 / 1024),
-        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", 1029194496 / 1024),
+        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314742272 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329688576 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "eeaa8967c0375109597e28a0d1551d3d4f828759628e6dc952721b0a140b9836", 324689664 / 1024),
+        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", 4743168 / 1024),
+        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", 1029158400 / 1024),
     },
 }
 
