@@ -74,24 +74,33 @@ constexpr int kColGroups = kEpiWarps / 4;        // warps sharing one TMEM lane 
 constexpr int kChunksPerWarp = 4 / kColGroups;   // 32-column chunks per warp per tile
 constexpr int kNewerCap = 255 / kColGroups;      // per-group cap of the newer count
 constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
-constexpr int kAccBufs = 4;
-constexpr uint32_t kTmemCols = kAccBufs * kRows;  // 512: all of TMEM
+constexpr uint32_t kTmemCols = 512;  // all of TMEM: 4 accumulators of 128 columns or 2 of 256
 constexpr int kPrefetch = 5;  // finalize rows per thread loaded at problem start (N <= 1280)
 
-template <int D, int MB>
+// W: column blocks per tile.  A tile multiplies row block I with W column
+// blocks J0 .. J0+W-1 at once (one MMA of N = 128 W), so the MMA issuer's
+// fixed cost per tile -- barrier waits and commits between tiles, during which
+// the tensor pipe idles because issuing an MMA blocks until the pipe takes it
+// -- is spread over W blocks.
+template <int D, int MB, int W>
 struct Cfg {
     static constexpr int kMaxBlocks = MB;
     static constexpr int kInvFloats = MB * kRows;
     static constexpr int KC = D / kChunkElems;  // swizzle chunks per row block
     static constexpr int kBlockBytes = KC * kChunkBytes;
+    static constexpr int kAccBufs = 4 / W;      // accumulators of 128 W columns
     static constexpr int kAStages = 2;
-    static constexpr int kBStages = (D == 128 ? 3 : 6) + (MB <= kMaxBlocksSmall ? (D == 128 ? 1 : 2) : 0);
-    static constexpr size_t kInvOff = (size_t)(kAStages + kBStages) * kBlockBytes;
+    // B stages of W blocks each (the same shared memory as 3 or 4 single blocks)
+    static constexpr int kBStages =
+        ((D == 128 ? 3 : 6) + (MB <= kMaxBlocksSmall ? (D == 128 ? 1 : 2) : 0)) / W;
+    static constexpr int kBStageBytes = W * kBlockBytes;
+    static constexpr int kBChunkBytes = W * kChunkBytes;  // one chunk of W blocks
+    static constexpr size_t kInvOff = (size_t)kAStages * kBlockBytes + (size_t)kBStages * kBStageBytes;
     static constexpr size_t kSimOff = kInvOff + 2 * sizeof(float) * kInvFloats;
     static constexpr size_t kNewerOff = kSimOff + sizeof(float) * kInvFloats;
     static constexpr size_t kInvMaxOff = kNewerOff + kInvFloats;  // one byte per row
     static constexpr size_t kBarOff = kInvMaxOff + 2 * sizeof(float) * kMaxBlocks * 4;
-    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kAccBufs + 4 + 2;
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * 4 + 4 + 2;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
 };
 
@@ -110,6 +119,7 @@ struct Params {
 };
 
 constexpr uint32_t kIdesc = idesc_bf16(kRows, kRows);
+constexpr uint32_t kIdesc2 = idesc_bf16(kRows, 2 * kRows);
 
 // Fixed-point scale of the shared-memory similarity sums (integer atomics are
 // native in shared memory): a similarity is stored in units of 2^-18, so a row
@@ -158,10 +168,12 @@ RKV_DEV int raw_max32(const uint32_t (&r)[32]) {
 }
 
 // ---------------------------------------------------------------- kernel --
-template <int D, int MB>
+template <int D, int MB, int W>
 __global__ void __launch_bounds__(kThreads, 1)
-gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
-    using C = Cfg<D, MB>;
+gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap bmap,
+               const Params prm) {
+    using C = Cfg<D, MB, W>;
+    constexpr int kAccBufs = C::kAccBufs;
     constexpr int kMaxBlocks = C::kMaxBlocks;
     constexpr int kInvFloats = C::kInvFloats;
     extern __shared__ uint8_t smem_raw[];
@@ -249,13 +261,15 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                         tma_load_3d(sA + sa * C::kBlockBytes + c * kChunkBytes, &tmap, &a_full[sa],
                                     c * kChunkElems, I * kRows, (int)p);
                     ++ka;
-                    for (int J = I + 1; ok && J < T; ++J) {
+                    // the column blocks of the row's tiles: J > I one at a time (the
+                    // diagonal tile reuses block I), or W at a time from J = I
+                    for (int J = W == 1 ? I + 1 : I; ok && J < T; J += W) {
                         const int sb = kb % C::kBStages;
                         if (!(ok = mbar_wait(&b_empty[sb], ((kb / C::kBStages) & 1) ^ 1, s_abort)))
                             break;
-                        mbar_arrive_expect_tx(&b_full[sb], C::kBlockBytes);
+                        mbar_arrive_expect_tx(&b_full[sb], C::kBStageBytes);
                         for (int c = 0; c < C::KC; ++c)
-                            tma_load_3d(sB + sb * C::kBlockBytes + c * kChunkBytes, &tmap,
+                            tma_load_3d(sB + sb * C::kBStageBytes + c * C::kBChunkBytes, &bmap,
                                         &b_full[sb], c * kChunkElems, J * kRows, (int)p);
                         ++kb;
                     }
@@ -294,27 +308,28 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     const int sa = ka % C::kAStages;
                     if (!(ok = mbar_wait(&a_full[sa], (ka / C::kAStages) & 1, s_abort))) break;
                     const uint8_t* a_base = sA + sa * C::kBlockBytes;
-                    for (int J = I; ok && J < T; ++J) {
+                    for (int J = I; ok && J < T; J += W) {
                         const uint8_t* b_base = a_base;
                         int sb = -1;
-                        if (J > I) {
+                        if (W > 1 || J > I) {
                             sb = kb % C::kBStages;
                             if (!(ok = mbar_wait(&b_full[sb], (kb / C::kBStages) & 1, s_abort)))
                                 break;
-                            b_base = sB + sb * C::kBlockBytes;
+                            b_base = sB + sb * C::kBStageBytes;
                         }
                         const int acc = kacc % kAccBufs;
                         if (!(ok = mbar_wait(&acc_empty[acc], ((kacc / kAccBufs) & 1) ^ 1, s_abort)))
                             break;
                         tc_fence_after();
-                        const uint32_t d_tmem = tmem + (uint32_t)(acc * kRows);
+                        const uint32_t d_tmem = tmem + (uint32_t)(acc * W * kRows);
 #pragma unroll
                         for (int c = 0; c < C::KC; ++c) {
                             const uint64_t ad = sdesc_sw128(a_base + c * kChunkBytes);
-                            const uint64_t bd = sdesc_sw128(b_base + c * kChunkBytes);
+                            const uint64_t bd = sdesc_sw128(b_base + c * (W > 1 ? C::kBChunkBytes : kChunkBytes));
 #pragma unroll
                             for (int k = 0; k < kChunkElems / 16; ++k)
-                                mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, kIdesc, (c | k) != 0);
+                                mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, W > 1 ? kIdesc2 : kIdesc,
+                                         (c | k) != 0);
                         }
                         mma_commit(&acc_full[acc]);
                         if (sb >= 0) {
@@ -383,13 +398,17 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                 const float thr = valid_i ? prm.tau / inv_i : INFINITY;
                 float sim_row = 0.f;
                 int newer = 0;
-                for (int J = I; J < T; ++J) {
-                    const int acc = kacc % kAccBufs;
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&acc_full[acc], (kacc / kAccBufs) & 1, s_abort));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const bool diag = (J == I);
+                for (int J0 = I; J0 < T; J0 += W) {
+                  const int acc = kacc % kAccBufs;
+                  ok = __all_sync(0xffffffffu,
+                                  mbar_wait(&acc_full[acc], (kacc / kAccBufs) & 1, s_abort));
+                  if (!ok) break;
+                  tc_fence_after();
+                  ++kacc;
+                  // the tile's column blocks one after another, with one
+                  // register buffer; the accumulator is released after the last
+                  for (int w = 0; w < W; ++w) {
+                    const int J = J0 + w;
                     // the warp's column group rotates with J so that the hot
                     // sub-tiles next to the diagonal do not always land on the
                     // same warps
@@ -397,12 +416,16 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                     uint32_t r[kChunksPerWarp][32];
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h)
-                        tmem_ld_32cols(t_lane + (uint32_t)(acc * kRows + (cgr * kChunksPerWarp + h) * 32),
+                        tmem_ld_32cols(t_lane + (uint32_t)(acc * W * kRows + w * kRows +
+                                                           (cgr * kChunksPerWarp + h) * 32),
                                        r[h]);
                     tmem_ld_wait();
-                    tc_fence_before();
-                    mbar_arrive_warp(&acc_empty[acc]);  // the accumulator is in registers now
-                    ++kacc;
+                    if (w == W - 1) {
+                        tc_fence_before();
+                        mbar_arrive_warp(&acc_empty[acc]);  // the accumulator is in registers now
+                    }
+                    if (J >= T) continue;  // past the problem's last block (zero keys)
+                    const bool diag = (J == I);
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h) {
                         const int cq = cgr * kChunksPerWarp + h;  // 32-column chunk within the tile
@@ -515,6 +538,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
                             }
                         }
                     }
+                  }
                 }
                 if (!ok) break;
                 // row-side partials of this column group (newer capped so
@@ -575,21 +599,23 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, int MB>
+template <int D, int MB, int W>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
-    using C = Cfg<D, MB>;
-    CUtensorMap map;
+    using C = Cfg<D, MB, W>;
+    CUtensorMap map, bmap;
     if (!make_map_3d_bf16(&map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
+        return cudaErrorInvalidValue;
+    if (!make_map_3d_bf16(&bmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, W * kRows))
         return cudaErrorInvalidValue;
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,
                a.sum_s,  a.ld_ws, a.I,       a.R,    a.Z,      a.ld_out, a.status};
-    auto kern = gram_tc_kernel<D, MB>;
+    auto kern = gram_tc_kernel<D, MB, W>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t sms = sm_count();
     const int64_t grid = a.P < sms ? a.P : sms;
-    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(map, prm);
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(map, bmap, prm);
     return cudaGetLastError();
 }
 
@@ -605,8 +631,9 @@ bool gram_tc_supported(const ScoreArgs& a) {
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
     if (a.P == 0) return cudaSuccess;
     if (a.N <= kMaxBlocksSmall * kRows)
-        return a.d == 128 ? launch_t<128, kMaxBlocksSmall>(a, s) : launch_t<64, kMaxBlocksSmall>(a, s);
-    return a.d == 128 ? launch_t<128, kMaxBlocksLarge>(a, s) : launch_t<64, kMaxBlocksLarge>(a, s);
+        return a.d == 128 ? launch_t<128, kMaxBlocksSmall, 2>(a, s)
+                          : launch_t<64, kMaxBlocksSmall, 2>(a, s);
+    return a.d == 128 ? launch_t<128, kMaxBlocksLarge, 1>(a, s) : launch_t<64, kMaxBlocksLarge, 1>(a, s);
 }
 
 }  // namespace rkv
