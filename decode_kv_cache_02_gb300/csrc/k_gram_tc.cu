@@ -381,11 +381,14 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                 pre_tot[u] = i < Cn ? prm.sum_s[p * prm.ld_ws + i] : 0.f;
                 pre_imp[u] = i < Cn ? prm.I[p * prm.ld_out + i] : 0.f;
             }
-            for (int x = et; x < T * 4; x += kEpiThreads) {
-                float m = -INFINITY;
-                const int j_end = min(N, (x + 1) * 32);
-                for (int j = x * 32; j < j_end; ++j) m = fmaxf(m, inv[j]);
-                invmax[x] = m;
+            // largest inverse norm of each 32-column chunk: one warp per chunk
+            // (a lane per column), chunks spread over the epilogue warps
+            for (int x = (warp - 2); x < T * 4; x += kEpiWarps) {
+                const int j = x * 32 + lane;
+                float m = j < N ? inv[j] : -INFINITY;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) invmax[x] = m;
             }
             // the previous problem's s_sim / s_newer entries are zero again
             mbar_arrive_warp(epi_bar);
