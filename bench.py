@@ -43,11 +43,10 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314742272 / 1024),
-        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329688576 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "eeaa8967c0375109597e28a0d1551d3d4f828759628e6dc952721b0a140b9836", 324689664 / 1024),
-        "select": ("k_select.cu", "df2e1ce993f9ba4c3b9cc9ef8210460c65e83db3ccb056b0fe5308d1dddd8ca8", 4743168 / 1024),
-        "gather": ("k_gather.cu", "0318d761cf59b5ba2fccaebea8b2a23a57c315b0084024b32f385e7d4e6d24f8", 1029158400 / 1024),
+        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314486528 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329739008 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "0e195e5262769e197b8a0cad98677843c90d80e7d43bf5e88cfbc76f19f9e083", 324261888 / 1024),
+        "compact": ("k_compact.cu", "924b4134c31ad01bd24c4d198adc79e4302ddbef89325cbe6f37f3ce347f30f0", 1034703616 / 1024),
     },
 }
 
@@ -186,6 +185,8 @@ def work_model(w: wl.Workload) -> dict:
         "gram_simt": {"flops": 2 * P * N * N * d, "bytes": k_bytes + 3 * P * N * 4},
         "select": {"bytes": P * (N - n_obs) * 4 + P * B * 4},
         "gather": {"bytes": 4 * P * B * d * es + P * B * 4},
+        # select + gather in one pass: Z read once, idx written, kept K, V moved
+        "compact": {"bytes": P * (N - n_obs) * 4 + P * B * 4 + 4 * P * B * d * es},
     }
 
 

@@ -1,0 +1,360 @@
+// k_compact.cu -- top-k selection and compaction of the kept K/V rows, fused.
+//
+// R-KV review (yoonschallenge.tistory.com/1236), opening notes (the newest 8
+// tokens always stay; the other tokens are scored and the best ones that fit
+// the budget are kept), question 2, cause 3 (top-k over the scores, then the
+// kept KV rows copied into the compacted cache) and cause 4 (re-layout of the
+// KV tensor).  Ties in Z
+// go to the larger (more recent) index; the kept candidates follow in
+// ascending order, then the n_obs observation tokens.
+//
+// One CTA per problem does both steps, so the selection's latency hides behind
+// the other CTAs' row copies and Z is read once:
+//   select  the scores as order-preserving keys in shared memory; a histogram
+//           of 256 buckets linear in the score between the problem's extremes
+//           (bucket(z) never decreases with z, so every score in a higher
+//           bucket is larger); only the bucket holding the k-th largest score
+//           is ranked exactly (directly for up to 32 keys, else radix passes
+//           over its compacted keys); a block scan in index order places each
+//           kept index.
+//   copy    16-byte vectors, several in flight per thread.  In place, rows
+//           before the first evicted token are skipped and the rest move in
+//           ascending chunks, each read completely before any of it is written
+//           (kept indices are ascending and idx[r] >= r).
+#include "rkv_common.cuh"
+#include "rkv_internal.h"
+#include "../../include/rkv.h"
+
+namespace rkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCopyVecs = 8;  // vectors per thread per tensor in flight
+
+RKV_DEV float from_orderable(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// Exclusive scan of one int per thread over the block; returns the thread's
+// prefix and the block total.
+__device__ int block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kWarps ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kWarps) s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int base = warp > 0 ? s_warp[warp - 1] : 0;
+    *total = s_warp[kWarps - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// The bin of the krem-th largest key in hist[0..255] (one warp): the digit,
+// the rank left inside the bin and the bin's count, in every lane.
+RKV_DEV void find_bin(const uint32_t* hist, uint32_t& krem, uint32_t& digit, uint32_t& bin_count) {
+    const int lane = threadIdx.x & 31;
+    uint32_t h[8], tot = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        h[b] = hist[lane * 8 + b];
+        tot += h[b];
+    }
+    uint32_t incl = tot;  // keys in the bins of lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+    }
+    uint32_t above = incl - tot;
+    uint32_t d = 0, kn = 0, c = 0;
+    const bool mine = above < krem && krem <= incl;
+    if (mine) {
+#pragma unroll
+        for (int b = 7; b >= 0; --b) {
+            if (above + h[b] >= krem) {
+                d = (uint32_t)(lane * 8 + b);
+                kn = krem - above;
+                c = h[b];
+                break;
+            }
+            above += h[b];
+        }
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    digit = __shfl_sync(0xffffffffu, d, src);
+    krem = __shfl_sync(0xffffffffu, kn, src);
+    bin_count = __shfl_sync(0xffffffffu, c, src);
+}
+
+RKV_DEV int bucket_of(float z, float zmin, float scale) {
+    return min(255, max(0, (int)((z - zmin) * scale)));
+}
+
+__global__ void __launch_bounds__(kThreads)
+compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
+               int32_t* __restrict__ idx, const uint4* a_src, const uint4* b_src, uint4* a_dst,
+               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st) {
+    extern __shared__ uint32_t s_dyn[];
+    const int C = N - n_obs, k = budget - n_obs;
+    uint32_t* keys = s_dyn;                                         // [C]
+    uint32_t* list = keys + C;                                      // [C]
+    int32_t* sidx = reinterpret_cast<int32_t*>(list + C);           // [budget]
+    __shared__ uint32_t s_hist[256];
+    __shared__ float s_red[2][kWarps];
+    __shared__ int s_warp[kWarps];
+    __shared__ uint32_t s_m, s_uk, s_eq, s_need;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t p = blockIdx.x;
+
+    // ---------------------------------------------------------- select --
+    float zmin = INFINITY, zmax = -INFINITY;
+    for (int i = tid; i < C; i += kThreads) {
+        const float z = Z[p * ldz + i];
+        keys[i] = orderable(z);
+        zmin = fminf(zmin, z);
+        zmax = fmaxf(zmax, z);
+    }
+    for (int b = tid; b < 256; b += kThreads) s_hist[b] = 0u;
+    if (tid == 0) s_m = 0u;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        zmin = fminf(zmin, __shfl_xor_sync(0xffffffffu, zmin, o));
+        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    }
+    if (lane == 0) {
+        s_red[0][warp] = zmin;
+        s_red[1][warp] = zmax;
+    }
+    __syncthreads();
+    zmin = s_red[0][0];
+    zmax = s_red[1][0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+        zmin = fminf(zmin, s_red[0][w]);
+        zmax = fmaxf(zmax, s_red[1][w]);
+    }
+    const float range = zmax - zmin;
+    const float scale = range > 0.f ? 255.5f / range : 0.f;
+    for (int i = tid; i < C; i += kThreads) atomicAdd(&s_hist[bucket_of(from_orderable(keys[i]), zmin, scale)], 1u);
+    __syncthreads();
+    uint32_t krem = (uint32_t)(k > 0 ? k : 1), bucket = 0, m = 0;
+    if (warp == 0) find_bin(s_hist, krem, bucket, m);
+    if (tid == 0) s_uk = bucket;
+    __syncthreads();
+    bucket = s_uk;
+    for (int i = tid; i < C; i += kThreads) {
+        const uint32_t u = keys[i];
+        if ((uint32_t)bucket_of(from_orderable(u), zmin, scale) == bucket) list[atomicAdd(&s_m, 1u)] = u;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // the krem-th largest of the m keys in the bucket: uk, how many keys
+        // equal it and how many of those are kept
+        m = s_m;
+        uint32_t uk, eq_count, need_eq;
+        if (m <= 32) {
+            const uint32_t mine = lane < (int)m ? list[lane] : 0u;
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t x = 0; x < m; ++x) {
+                const uint32_t o = __shfl_sync(0xffffffffu, mine, x);
+                gt += o > mine;
+                eq += o == mine;
+            }
+            const bool it = lane < (int)m && gt < krem && krem <= gt + eq;
+            const int src = __ffs(__ballot_sync(0xffffffffu, it)) - 1;
+            uk = __shfl_sync(0xffffffffu, mine, src);
+            eq_count = __shfl_sync(0xffffffffu, eq, src);
+            need_eq = krem - __shfl_sync(0xffffffffu, gt, src);
+        } else {
+            // radix passes over the bucket's keys, from the highest bit where
+            // they differ
+            uint32_t lmin = 0xffffffffu, lmax = 0u;
+            for (uint32_t x = lane; x < m; x += 32) {
+                lmin = min(lmin, list[x]);
+                lmax = max(lmax, list[x]);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                lmin = min(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+                lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            }
+            int top = lmin == lmax ? 0 : 32 - __clz(lmin ^ lmax);
+            uint32_t prefix = top == 32 ? 0u : lmax & ~((1u << top) - 1u);
+            eq_count = m;
+            while (top > 0) {
+                const int sh = top >= 8 ? top - 8 : 0;
+                const uint32_t dm = top >= 8 ? 255u : ((1u << top) - 1u);
+                const uint32_t pm = top == 32 ? 0u : ~((1u << top) - 1u);
+                __syncwarp();
+#pragma unroll
+                for (int b = 0; b < 8; ++b) s_hist[lane * 8 + b] = 0u;
+                __syncwarp();
+                for (uint32_t x = lane; x < m; x += 32) {
+                    const uint32_t u = list[x];
+                    if ((u & pm) == prefix) atomicAdd(&s_hist[(u >> sh) & dm], 1u);
+                }
+                __syncwarp();
+                uint32_t dg;
+                find_bin(s_hist, krem, dg, eq_count);
+                prefix |= dg << sh;
+                top = sh;
+            }
+            uk = prefix;
+            need_eq = krem;
+        }
+        if (lane == 0) {
+            s_uk = uk;
+            s_eq = eq_count;
+            s_need = need_eq;
+        }
+    }
+    __syncthreads();
+    const uint32_t uk = s_uk;
+    const uint32_t eq_cut = s_eq - s_need;  // equal keys of rank >= eq_cut are kept
+    // kept candidates in index order: contiguous ranges per thread, block scans
+    const int ipt = (C + kThreads - 1) / kThreads;
+    const int lo = min(C, tid * ipt), hi = min(C, lo + ipt);
+    int eq_before = 0;
+    if (eq_cut > 0) {
+        int n_eq = 0;
+        for (int i = lo; i < hi; ++i) n_eq += (keys[i] == uk);
+        int eq_total;
+        eq_before = block_scan(n_eq, s_warp, &eq_total);
+    }
+    int n_keep = 0;
+    {
+        int e = eq_before;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t u = keys[i];
+            if (u > uk) ++n_keep;
+            else if (u == uk) { n_keep += (e >= (int)eq_cut); ++e; }
+        }
+    }
+    int keep_total;
+    int pos = block_scan(n_keep, s_warp, &keep_total);
+    if (k > 0) {
+        int e = eq_before;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t u = keys[i];
+            bool keep = false;
+            if (u > uk) keep = true;
+            else if (u == uk) { keep = (e >= (int)eq_cut); ++e; }
+            if (keep && pos < k) sidx[pos++] = i;
+        }
+    }
+    for (int r = tid; r < n_obs; r += kThreads) sidx[k + r] = C + r;
+    __syncthreads();
+    int32_t* out = idx + p * (int64_t)budget;
+    for (int r = tid; r < budget; r += kThreads) out[r] = sidx[r];
+
+    // ------------------------------------------------------------ copy --
+    const int64_t base = (int64_t)p * n_cap * vpr;
+    if (!in_place) {
+        const int total = budget * vpr;
+        for (int e0 = tid; e0 < total; e0 += kThreads * kCopyVecs) {
+            uint4 va[kCopyVecs], vb[kCopyVecs];
+            int dst[kCopyVecs];
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                const int e = e0 + t * kThreads;
+                dst[t] = -1;
+                if (e < total) {
+                    const int r = e / vpr, v = e % vpr;
+                    const int s = sidx[r];
+                    if (s >= 0 && s < n_cap) {
+                        dst[t] = r * vpr + v;
+                        va[t] = __ldg(a_src + base + (int64_t)s * vpr + v);
+                        if (b_src) vb[t] = __ldg(b_src + base + (int64_t)s * vpr + v);
+                    } else if (st) {
+                        set_error(st, kDevErrIndex, (unsigned)r);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                if (dst[t] >= 0) {
+                    a_dst[base + dst[t]] = va[t];
+                    if (b_dst) b_dst[base + dst[t]] = vb[t];
+                }
+            }
+        }
+    } else {
+        // first row r0 with sidx[r0] != r0 (sidx[r] == r holds exactly on a prefix)
+        int l = 0, h = budget;
+        while (l < h) {
+            const int mid = (l + h) >> 1;
+            if (sidx[mid] == mid) l = mid + 1;
+            else h = mid;
+        }
+        const int rows_per_chunk = kThreads * kCopyVecs / vpr;
+        for (int c0 = l; c0 < budget; c0 += rows_per_chunk) {
+            uint4 va[kCopyVecs], vb[kCopyVecs];
+            int dst[kCopyVecs];
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                const int e = t * kThreads + tid;  // vector within the chunk
+                const int r = c0 + e / vpr, v = e % vpr;
+                dst[t] = -1;
+                if (r < budget) {
+                    const int s = sidx[r];
+                    if (s >= 0 && s < n_cap) {
+                        dst[t] = r * vpr + v;
+                        va[t] = a_dst[base + (int64_t)s * vpr + v];
+                        if (b_dst) vb[t] = b_dst[base + (int64_t)s * vpr + v];
+                    } else if (st) {
+                        set_error(st, kDevErrIndex, (unsigned)r);
+                    }
+                }
+            }
+            __syncthreads();  // every source row of the chunk has been read
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                if (dst[t] >= 0) {
+                    a_dst[base + dst[t]] = va[t];
+                    if (b_dst) b_dst[base + dst[t]] = vb[t];
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace
+
+size_t compact_smem_bytes(int N, int n_obs, int budget) {
+    const int C = N - n_obs;
+    return sizeof(uint32_t) * (size_t)(2 * (C > 0 ? C : 1)) + sizeof(int32_t) * (size_t)budget;
+}
+
+cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
+                           int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
+                           void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
+                           cudaStream_t s) {
+    if (P == 0 || budget == 0) return cudaSuccess;
+    const size_t smem = compact_smem_bytes(N, n_obs, budget);
+    cudaError_t e =
+        cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    compact_kernel<<<(unsigned)P, kThreads, smem, s>>>(
+        Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(src_a),
+        static_cast<const uint4*>(src_b), static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), n_cap,
+        row_bytes / 16, in_place ? 1 : 0, st);
+    return cudaGetLastError();
+}
+
+}  // namespace rkv

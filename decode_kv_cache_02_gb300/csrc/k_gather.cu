@@ -1,7 +1,7 @@
 // k_gather.cu -- copy the kept K/V rows into the compacted cache.
 //
-// R-KV review (yoonschallenge.tistory.com/1236), question 2, cause 3 ("copy
-// the selected KV into the new cache") and cause 4 (pruning forces a re-layout
+// R-KV review (yoonschallenge.tistory.com/1236), question 2, cause 3 (the
+// kept KV rows are copied into the compacted cache) and cause 4 (pruning forces a re-layout
 // of the KV tensor; allocating a new cache costs memory management).  The
 // copy is byte-exact and can run in place, so no second cache is needed.
 //

@@ -1,8 +1,8 @@
 // k_select.cu -- per-problem top-k of the combined score, ascending indices.
 //
-// R-KV review (yoonschallenge.tistory.com/1236), opening notes ("keep the
-// newest 8, score the rest, select only the top tokens that fit the
-// budget") and question 2, cause 3 ("top-k token selection").  Ties in Z go to
+// R-KV review (yoonschallenge.tistory.com/1236), opening notes (the newest 8
+// tokens always stay; the other tokens are scored and the best ones that fit
+// the budget are kept) and question 2, cause 3 (top-k over the scores).  Ties in Z go to
 // the larger (more recent) index; the output is the kept candidates in
 // ascending order followed by the n_obs observation tokens.
 //

@@ -34,11 +34,12 @@ enum KernelId {
     kSelect,
     kGather,
     kIdentity,
+    kCompact,
     kNumKernels
 };
 const char* const kKernelNames[kNumKernels] = {
     "key_stats", "importance", "importance_tc", "gram_tc", "gram_simt", "select", "gather",
-    "identity_idx"};
+    "identity_idx", "compact"};
 
 // ---------------------------------------------------------------- timing --
 struct TimedLaunch {
@@ -76,6 +77,9 @@ cudaError_t timed(int kernel, cudaStream_t s, F&& launch) {
 
 // ------------------------------------------------------------ workspace --
 constexpr size_t kAlign = 256;
+// the fused select + gather keeps a problem's scores, bucket keys and kept
+// indices in shared memory; larger problems take the separate kernels
+constexpr size_t kCompactSmemMax = 160 * 1024;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Workspace {
@@ -270,14 +274,23 @@ int rkv_compress(const rkv_desc* desc, const void* K, const void* V, const void*
     rc = run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I, nullptr, w.Z, w.ld,
                     w, s);
     if (rc) return rc;
-    cudaError_t e = timed(kSelect, s, [&] {
-        return rkv::launch_select(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.status, s);
-    });
-    if (e == cudaSuccess)
-        e = timed(kGather, s, [&] {
-            return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, budget,
-                                      row_bytes, in_place, w.status, s);
+    cudaError_t e;
+    if (rkv::compact_smem_bytes(n_cached, n_obs, budget) <= kCompactSmemMax) {
+        // selection and compaction in one pass per problem
+        e = timed(kCompact, s, [&] {
+            return rkv::launch_compact(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, K, V, out_K,
+                                       out_V, desc->n_capacity, row_bytes, in_place, w.status, s);
         });
+    } else {
+        e = timed(kSelect, s, [&] {
+            return rkv::launch_select(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.status, s);
+        });
+        if (e == cudaSuccess)
+            e = timed(kGather, s, [&] {
+                return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, budget,
+                                          row_bytes, in_place, w.status, s);
+            });
+    }
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 

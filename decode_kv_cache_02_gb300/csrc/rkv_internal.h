@@ -49,5 +49,11 @@ cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, voi
 
 // idx rows = 0..n-1 then -1 (nothing evicted).
 cudaError_t launch_identity_idx(int64_t P, int n, int budget, int32_t* idx, cudaStream_t s);
+// select + gather fused (one CTA per problem); dynamic shared memory it needs
+size_t compact_smem_bytes(int N, int n_obs, int budget);
+cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
+                           int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
+                           void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
+                           cudaStream_t s);
 
 }  // namespace rkv

@@ -99,6 +99,18 @@ def test_ragged_and_capacity(cuda_ok):
         _full_check(w, K, V, Q, list(range(w.problems)))
 
 
+@pytest.mark.parametrize("n_cached,budget", [(13000, 12000), (14000, 13000)])
+def test_long_context_selection_paths(cuda_ok, n_cached, budget):
+    """Long contexts on both sides of the fused select + gather's shared-memory
+    limit (scores, sort keys and kept indices of one problem): the first size
+    runs the fused kernel with ~150 KB of shared memory, the second the
+    separate select and gather kernels."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(head_dim=64, n_cached=n_cached, budget=budget,
+                                           layers=1, batch=1, kv_heads=1)
+    K, V, Q = wl.make_inputs(w, device=DEV)
+    _full_check(w, K, V, Q, [0])
+
+
 def test_parameter_variants(cuda_ok):
     """lambda in {0, 1}, beta in {0, 1, 5}, tau in {0.5, 0.99}."""
     base = wl.BY_NAME["llama8b_layer"].scaled(n_cached=640, budget=512, kv_heads=2)
