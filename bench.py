@@ -187,6 +187,8 @@ def work_model(w: wl.Workload) -> dict:
         "gather": {"bytes": 4 * P * B * d * es + P * B * 4},
         # select + gather in one pass: Z read once, idx written, kept K, V moved
         "compact": {"bytes": P * (N - n_obs) * 4 + P * B * 4 + 4 * P * B * d * es},
+        # scoring variant: read I and R, write Z
+        "variant": {"bytes": 3 * P * N * 4},
     }
 
 
@@ -290,6 +292,87 @@ def _config(w, **extra):
     return c
 
 
+def _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, softmax=False, window=1):
+    """One compression step of workload `w` (with a scoring variant if asked)."""
+    if softmax or window != 1:
+        def step():
+            rkv.rkv_compress_ex(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
+                                redundancy_softmax=softmax, pool_window=window, out_K=out_K,
+                                out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
+    else:
+        def step():
+            rkv.rkv_compress(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
+                             out_K=out_K, out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
+    return step
+
+
+def _time_steps(step, steps, warmup, ws, stream, local, world):
+    """W untimed steps, then K steps between CUDA events on the launching
+    stream with a barrier and a synchronize on both sides and the clocks
+    sampled meanwhile.  Returns (elapsed ms, per-kernel totals, clocks)."""
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error during warm-up")
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rkv.rkv_timing_read(reset=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        _barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        rkv.rkv_timing_enable(True)
+        for _ in range(steps):
+            step()
+        rkv.rkv_timing_enable(False)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+    elapsed = start.elapsed_time(stop)
+    timing = rkv.rkv_timing_read(reset=True)
+    kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in timing.items() if v[1] > 0}
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error in the timed region")
+    return elapsed, kernels, clocks.summary()
+
+
+# lambda / beta / tau swept one at a time around the page's setting, and the
+# scoring variants (beta above 63 would switch to the CUDA-core Gram)
+SWEEP = ([{"lam": v} for v in (0.0, 0.5, 1.0)] + [{"beta": v} for v in (0, 1, 8, 63)]
+         + [{"tau": v} for v in (0.5, 0.7, 0.8, 0.95, 0.99)]
+         + [{"softmax": True}, {"window": 7}, {"softmax": True, "window": 7}])
+
+
+def run_sweep(args, w):
+    """One JSON line per setting of SWEEP on the workload (device-timed step
+    and per-kernel split; no end-to-end or CPU legs)."""
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rkv.load()
+    K, V, Q = wl.make_inputs(w, device=dev, seed=w.seed + rank)
+    out_K, out_V = torch.empty_like(K), torch.empty_like(V)
+    idx = torch.empty((w.problems, w.budget), dtype=torch.int32, device=dev)
+    ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
+    stream = torch.cuda.current_stream()
+    for setting in [{}] + SWEEP:
+        ws_ = w.scaled(**{k: v for k, v in setting.items() if k in ("lam", "beta", "tau")})
+        step = _step_fn(ws_, K, V, Q, out_K, out_V, idx, ws, stream,
+                        setting.get("softmax", False), setting.get("window", 1))
+        elapsed, kernels, clocks = _time_steps(step, args.steps, args.warmup, ws, stream, local,
+                                               world)
+        line = {"sweep": {"lambda": ws_.lam, "beta": ws_.beta, "tau": ws_.tau,
+                          "redundancy_softmax": setting.get("softmax", False),
+                          "pool_window": setting.get("window", 1)},
+                "workload": w.name, "steps": args.steps, "ms_per_step": elapsed / args.steps,
+                "value": args.steps * w.problems * w.n_cached / (elapsed * 1e-3), "unit": UNIT,
+                "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
+                "clocks": clocks}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+
+
 def run_ours(args, w):
     world, rank, local = _dist()
     if world > 1:
@@ -304,37 +387,11 @@ def run_ours(args, w):
     idx = torch.empty((w.problems, w.budget), dtype=torch.int32, device=dev)
     ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
     stream = torch.cuda.current_stream()
-
-    def step():
-        rkv.rkv_compress(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
-                         out_K=out_K, out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    if rkv.rkv_get_device_status(ws) != 0:
-        raise RuntimeError("a kernel reported a device error during warm-up")
-
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    rkv.rkv_timing_read(reset=True)
-    with ClockSampler(local) as clocks:
-        time.sleep(0.3)
-        _barrier(world)
-        torch.cuda.synchronize()
-        start.record(stream)
-        rkv.rkv_timing_enable(True)
-        for _ in range(args.steps):
-            step()
-        rkv.rkv_timing_enable(False)
-        stop.record(stream)
-        torch.cuda.synchronize()
-        _barrier(world)
-    elapsed = start.elapsed_time(stop)
-    timing = rkv.rkv_timing_read(reset=True)
-    kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in timing.items() if v[1] > 0}
+    step = _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, args.redundancy_softmax,
+                    args.pool_window)
+    elapsed, kernels, clock_summary = _time_steps(step, args.steps, args.warmup, ws, stream,
+                                                  local, world)
     launches = sum(v["launches"] for v in kernels.values())
-    if rkv.rkv_get_device_status(ws) != 0:
-        raise RuntimeError("a kernel reported a device error in the timed region")
 
     units = args.steps * w.problems * w.n_cached
     t_max, u_sum = aggregate(elapsed, units, world)
@@ -352,8 +409,11 @@ def run_ours(args, w):
         / (t_max * 1e-3),
         "gpu_launches": launches,
         "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
-        "clocks": clocks.summary(),
+        "clocks": clock_summary,
     }
+    if args.redundancy_softmax or args.pool_window != 1:
+        line["config"]["variant"] = {"redundancy_softmax": args.redundancy_softmax,
+                                     "pool_window": args.pool_window}
     line["roofline"] = roofline(kernels, model, peaks, args.steps, w)
     # all kernels' fractions, for the record
     line["roofline_all"] = {}
@@ -419,8 +479,10 @@ def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world):
         stream.wait_event(e_in)
         if done_d2h[sl] is not None:
             stream.wait_event(done_d2h[sl])  # slot's outputs copied out
-        rkv.rkv_compress(dK, dV, dQ, w.n_cached, B, w.n_obs, w.lam, w.beta, w.tau, out_K=dOK,
-                         out_V=dOV, out_idx=dI, workspace=ws, stream=stream)
+        rkv.rkv_compress_ex(dK, dV, dQ, w.n_cached, B, w.n_obs, w.lam, w.beta, w.tau,
+                            redundancy_softmax=args.redundancy_softmax,
+                            pool_window=args.pool_window, out_K=dOK, out_V=dOV, out_idx=dI,
+                            workspace=ws, stream=stream)
         e_c = ev()
         e_c.record(stream)
         done_compute[sl] = e_c
@@ -541,12 +603,20 @@ def main():
     ap.add_argument("--problems", type=int, default=0,
                     help="override the problem count (smaller copies for profiling; "
                          "such a run is not the workload's bench line)")
+    ap.add_argument("--redundancy-softmax", action="store_true",
+                    help="scoring variant: softmax of the redundancy over the candidates")
+    ap.add_argument("--pool-window", type=int, default=1,
+                    help="scoring variant: odd max-pooling window on the importance")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the step over a lambda/beta/tau/variant sweep, one line each")
     args = ap.parse_args()
     w = wl.BY_NAME[args.workload]
     if args.problems:
         w = w.scaled(layers=1, batch=1, kv_heads=args.problems)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.sweep:
+        run_sweep(args, w)
     elif w.gen_tokens:
         run_stream(args, w)
     else:

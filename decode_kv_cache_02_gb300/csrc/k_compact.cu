@@ -23,6 +23,7 @@
 //           (kept indices are ascending and idx[r] >= r).
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
+#include "rkv_variant.cuh"
 #include "../../include/rkv.h"
 
 namespace rkv {
@@ -108,7 +109,7 @@ RKV_DEV int bucket_of(float z, float zmin, float scale) {
 __global__ void __launch_bounds__(kThreads)
 compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
                int32_t* __restrict__ idx, const uint4* a_src, const uint4* b_src, uint4* a_dst,
-               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st) {
+               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st, VariantIn var) {
     extern __shared__ uint32_t s_dyn[];
     const int C = N - n_obs, k = budget - n_obs;
     uint32_t* keys = s_dyn;                                         // [C]
@@ -123,11 +124,35 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
 
     // ---------------------------------------------------------- select --
     float zmin = INFINITY, zmax = -INFINITY;
-    for (int i = tid; i < C; i += kThreads) {
-        const float z = Z[p * ldz + i];
-        keys[i] = orderable(z);
-        zmin = fminf(zmin, z);
-        zmax = fmaxf(zmax, z);
+    if (var.I == nullptr) {
+        for (int i = tid; i < C; i += kThreads) {
+            const float z = Z[p * ldz + i];
+            keys[i] = orderable(z);
+            zmin = fminf(zmin, z);
+            zmax = fmaxf(zmax, z);
+        }
+    } else {
+        // scoring variant: Z from the base I and R rows, staged in the two
+        // key arrays (I in `list`, R in `keys`, each entry of `keys` then
+        // replaced by its own Z key)
+        float* sI = reinterpret_cast<float*>(list);
+        float* sR = reinterpret_cast<float*>(keys);
+        for (int i = tid; i < C; i += kThreads) {
+            sI[i] = var.I[p * var.ld + i];
+            sR[i] = var.R[p * var.ld + i];
+        }
+        __syncthreads();
+        SoftmaxStats sm{0.f, 1.f};
+        if (var.softmax) sm = softmax_stats<kThreads>(sR, C, s_red[0]);
+        for (int i = tid; i < C; i += kThreads) {
+            const float r = sR[i];
+            const float z = variant_z(var.lambda, pooled_importance(sI, i, C, var.half),
+                                      var.softmax ? softmax_term(r, sm) : r);
+            keys[i] = orderable(z);
+            zmin = fminf(zmin, z);
+            zmax = fmaxf(zmax, z);
+        }
+        __syncthreads();  // `list` is reused for the bucket's keys below
     }
     for (int b = tid; b < 256; b += kThreads) s_hist[b] = 0u;
     if (tid == 0) s_m = 0u;
@@ -344,7 +369,7 @@ size_t compact_smem_bytes(int N, int n_obs, int budget) {
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
                            void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
-                           cudaStream_t s) {
+                           cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
     const size_t smem = compact_smem_bytes(N, n_obs, budget);
     cudaError_t e =
@@ -353,7 +378,7 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
     compact_kernel<<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(src_a),
         static_cast<const uint4*>(src_b), static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), n_cap,
-        row_bytes / 16, in_place ? 1 : 0, st);
+        row_bytes / 16, in_place ? 1 : 0, st, var);
     return cudaGetLastError();
 }
 

@@ -35,11 +35,12 @@ enum KernelId {
     kGather,
     kIdentity,
     kCompact,
+    kVariant,
     kNumKernels
 };
 const char* const kKernelNames[kNumKernels] = {
     "key_stats", "importance", "importance_tc", "gram_tc", "gram_simt", "select", "gather",
-    "identity_idx", "compact"};
+    "identity_idx", "compact", "variant"};
 
 // ---------------------------------------------------------------- timing --
 struct TimedLaunch {
@@ -87,6 +88,7 @@ struct Workspace {
     float* inv_norm;
     float* sum_s;
     float* I;
+    float* R;
     float* Z;
     void* s_rows;
     int64_t ld;
@@ -109,6 +111,8 @@ Workspace carve(void* base, int64_t P, int n) {
     w.sum_s = reinterpret_cast<float*>(b + off);
     off += arr;
     w.I = reinterpret_cast<float*>(b + off);
+    off += arr;
+    w.R = reinterpret_cast<float*>(b + off);
     off += arr;
     w.Z = reinterpret_cast<float*>(b + off);
     off += arr;
@@ -140,6 +144,17 @@ bool partial_overlap(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// A variant's fields; *active = whether it changes anything.
+int check_variant(const rkv_variant* v, bool* active) {
+    *active = false;
+    if (!v) return RKV_OK;
+    if (v->redundancy_softmax != 0 && v->redundancy_softmax != 1) return RKV_ERR_INVALID_ARG;
+    if (v->pool_window < 1 || v->pool_window > RKV_MAX_POOL_WINDOW || (v->pool_window & 1) == 0)
+        return RKV_ERR_INVALID_ARG;
+    *active = v->redundancy_softmax != 0 || v->pool_window > 1;
+    return RKV_OK;
+}
+
 int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                  void* ws, size_t ws_bytes) {
     int rc = check_desc(d);
@@ -159,6 +174,7 @@ int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, 
 int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
                const Workspace& w, cudaStream_t s) {
+    // I, R, Z as defined on the page (R may be null: not stored)
     ScoreArgs a{};
     a.K = K;
     a.Q = Q;
@@ -200,6 +216,21 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
+// The scores with a variant: the base scores into the workspace, then I', R'
+// and Z into the given rows (I_out, R_out may be null).
+int run_scores_variant(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
+                       float lambda, int beta, float tau, const rkv_variant& v, float* I_out,
+                       float* R_out, float* Z, int64_t ld_out, const Workspace& w,
+                       cudaStream_t s) {
+    int rc = run_scores(d, K, Q, n_cached, n_obs, lambda, beta, tau, w.I, w.R, w.Z, w.ld, w, s);
+    if (rc) return rc;
+    cudaError_t e = timed(kVariant, s, [&] {
+        return rkv::launch_variant(d->num_problems, n_cached, n_obs, lambda, v.redundancy_softmax,
+                                   v.pool_window, w.I, w.R, w.ld, Z, I_out, R_out, ld_out, s);
+    });
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -210,24 +241,50 @@ size_t rkv_workspace_size(const rkv_desc* desc, int n_cached, int n_obs) {
     return carve(nullptr, desc->num_problems, n_cached).bytes;
 }
 
-int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cached, int n_obs,
-              float lambda, int beta, float tau, float* out_I, float* out_R, float* out_Z,
-              void* workspace, size_t workspace_bytes, void* stream) {
-    int rc = check_scores(desc, K, Q_obs, n_cached, n_obs, workspace, workspace_bytes);
+int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cached,
+                 int n_obs, float lambda, int beta, float tau, const rkv_variant* variant,
+                 float* out_I, float* out_R, float* out_Z, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    bool var_on = false;
+    int rc = check_variant(variant, &var_on);
+    if (rc) return rc;
+    rc = check_scores(desc, K, Q_obs, n_cached, n_obs, workspace, workspace_bytes);
     if (rc) return rc;
     if (beta < 0) return RKV_ERR_INVALID_ARG;
     if (desc->num_problems == 0) return RKV_OK;
     if (!out_I || !out_R || !out_Z) return RKV_ERR_INVALID_ARG;
     const Workspace w = carve(workspace, desc->num_problems, n_cached);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (var_on)
+        return run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
+                                  out_I, out_R, out_Z, n_cached, w, s);
     return run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, out_I, out_R, out_Z,
-                      n_cached, w, static_cast<cudaStream_t>(stream));
+                      n_cached, w, s);
+}
+
+int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cached, int n_obs,
+              float lambda, int beta, float tau, float* out_I, float* out_R, float* out_Z,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    return rkv_score_ex(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, nullptr, out_I, out_R,
+                        out_Z, workspace, workspace_bytes, stream);
 }
 
 int rkv_compress(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
                  int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                  void* out_K, void* out_V, int32_t* out_idx, void* workspace,
                  size_t workspace_bytes, void* stream) {
-    int rc = check_desc(desc);
+    return rkv_compress_ex(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau, nullptr,
+                           out_K, out_V, out_idx, workspace, workspace_bytes, stream);
+}
+
+int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                    int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                    const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    bool var_on = false;
+    int rc = check_variant(variant, &var_on);
+    if (rc) return rc;
+    rc = check_desc(desc);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t P = desc->num_problems;
@@ -271,15 +328,31 @@ int rkv_compress(const rkv_desc* desc, const void* K, const void* V, const void*
     if (rc) return rc;
     if (P == 0) return RKV_OK;
     const Workspace w = carve(workspace, P, n_cached);
-    rc = run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I, nullptr, w.Z, w.ld,
-                    w, s);
+    const bool fused = rkv::compact_smem_bytes(n_cached, n_obs, budget) <= kCompactSmemMax;
+    if (var_on && !fused)
+        rc = run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
+                                nullptr, nullptr, w.Z, w.ld, w, s);
+    else
+        rc = run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
+                        var_on ? w.R : nullptr, w.Z, w.ld, w, s);
     if (rc) return rc;
     cudaError_t e;
-    if (rkv::compact_smem_bytes(n_cached, n_obs, budget) <= kCompactSmemMax) {
-        // selection and compaction in one pass per problem
+    if (fused) {
+        // selection and compaction in one pass per problem (a variant's Z is
+        // formed there from I and R)
+        rkv::VariantIn vin;
+        if (var_on) {
+            vin.I = w.I;
+            vin.R = w.R;
+            vin.ld = w.ld;
+            vin.lambda = lambda;
+            vin.softmax = variant->redundancy_softmax;
+            vin.half = (variant->pool_window - 1) / 2;
+        }
         e = timed(kCompact, s, [&] {
             return rkv::launch_compact(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, K, V, out_K,
-                                       out_V, desc->n_capacity, row_bytes, in_place, w.status, s);
+                                       out_V, desc->n_capacity, row_bytes, in_place, w.status, s,
+                                       vin);
         });
     } else {
         e = timed(kSelect, s, [&] {

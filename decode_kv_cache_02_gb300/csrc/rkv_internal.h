@@ -49,11 +49,29 @@ cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, voi
 
 // idx rows = 0..n-1 then -1 (nothing evicted).
 cudaError_t launch_identity_idx(int64_t P, int n, int budget, int32_t* idx, cudaStream_t s);
+// A scoring variant applied inside the fused select + gather: Z is computed
+// from the base I and R rows (stride ld) instead of read.  I == nullptr: read Z.
+struct VariantIn {
+    const float* I = nullptr;
+    const float* R = nullptr;
+    int64_t ld = 0;
+    float lambda = 0.f;
+    int softmax = 0;
+    int half = 0;  // (pool window - 1) / 2
+};
+
 // select + gather fused (one CTA per problem); dynamic shared memory it needs
 size_t compact_smem_bytes(int N, int n_obs, int budget);
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
                            void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
-                           cudaStream_t s);
+                           cudaStream_t s, const VariantIn& var = VariantIn{});
+
+// Variant scores (redundancy softmax, importance pooling window) from the
+// base I and R rows (stride ld_in): Z, and I', R' when I_out / R_out are given
+// (stride ld_out).
+cudaError_t launch_variant(int64_t P, int N, int n_obs, float lambda, int softmax, int window,
+                           const float* I, const float* R, int64_t ld_in, float* Z, float* I_out,
+                           float* R_out, int64_t ld_out, cudaStream_t s);
 
 }  // namespace rkv

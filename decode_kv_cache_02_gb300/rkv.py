@@ -25,8 +25,10 @@ RKV_MAX_TOKENS = 32768
 EXPORTED = [
     "rkv_workspace_size", "rkv_compress", "rkv_score", "rkv_select", "rkv_gather",
     "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
-    "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc",
+    "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
+    "rkv_score_ex",
 ]
+RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_TOO_LARGE = 7
 
 
@@ -40,6 +42,10 @@ class _Desc(ctypes.Structure):
     _fields_ = [("num_problems", ctypes.c_int64), ("gqa_group", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_capacity", ctypes.c_int32),
                 ("dtype", ctypes.c_int32)]
+
+
+class _Variant(ctypes.Structure):
+    _fields_ = [("redundancy_softmax", ctypes.c_int32), ("pool_window", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -68,6 +74,13 @@ def load(path: str | None = None):
         lib.rkv_compress.restype = i32
         lib.rkv_score.argtypes = [dp, vp, vp, i32, i32, f32, i32, f32, vp, vp, vp, vp, sz, vp]
         lib.rkv_score.restype = i32
+        vr = ctypes.POINTER(_Variant)
+        lib.rkv_compress_ex.argtypes = [dp, vp, vp, vp, i32, i32, i32, f32, i32, f32, vr, vp, vp,
+                                        vp, vp, sz, vp]
+        lib.rkv_compress_ex.restype = i32
+        lib.rkv_score_ex.argtypes = [dp, vp, vp, i32, i32, f32, i32, f32, vr, vp, vp, vp, vp, sz,
+                                     vp]
+        lib.rkv_score_ex.restype = i32
         lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
         lib.rkv_select.restype = i32
         lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
@@ -142,12 +155,7 @@ def alloc_workspace(K: torch.Tensor, gqa_group: int, n_cached: int, n_obs: int) 
     return torch.zeros(n, dtype=torch.uint8, device=K.device)
 
 
-def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
-                 beta: int = 2, tau: float = 0.9, out_K=None, out_V=None, out_idx=None,
-                 workspace=None, stream=None):
-    """One compression round of every problem in K/V [P, n_cap, d] with
-    Q_obs [P, G, n_obs, d].  Returns (out_K, out_V, out_idx); pass
-    out_K=K, out_V=V to compact in place."""
+def _compress_args(K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, workspace):
     for t, n in ((K, "K"), (V, "V"), (Q_obs, "Q_obs")):
         _cuda(t, n)
     if V.shape != K.shape or V.dtype != K.dtype or Q_obs.dtype != K.dtype:
@@ -170,11 +178,41 @@ def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: f
     if out_K.shape != K.shape or out_V.shape != K.shape or out_idx.shape != (K.shape[0], budget) \
             or out_idx.dtype != torch.int32:
         raise ValueError("output shapes")
+    return desc, out_K, out_V, out_idx, workspace
+
+
+def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
+                 beta: int = 2, tau: float = 0.9, out_K=None, out_V=None, out_idx=None,
+                 workspace=None, stream=None):
+    """One compression round of every problem in K/V [P, n_cap, d] with
+    Q_obs [P, G, n_obs, d].  Returns (out_K, out_V, out_idx); pass
+    out_K=K, out_V=V to compact in place."""
+    desc, out_K, out_V, out_idx, workspace = _compress_args(
+        K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, workspace)
     rc = load().rkv_compress(ctypes.byref(desc), K.data_ptr(), V.data_ptr(), Q_obs.data_ptr(),
                              int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
                              float(tau), out_K.data_ptr(), out_V.data_ptr(), out_idx.data_ptr(),
                              workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _check(rc, "rkv_compress")
+    return out_K, out_V, out_idx
+
+
+def rkv_compress_ex(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
+                    beta: int = 2, tau: float = 0.9, redundancy_softmax: bool = False,
+                    pool_window: int = 1, out_K=None, out_V=None, out_idx=None, workspace=None,
+                    stream=None):
+    """rkv_compress with a scoring variant: redundancy_softmax turns R into a
+    softmax over the candidates, pool_window (odd) max-pools I over that many
+    neighbouring positions."""
+    desc, out_K, out_V, out_idx, workspace = _compress_args(
+        K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, workspace)
+    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
+    rc = load().rkv_compress_ex(ctypes.byref(desc), K.data_ptr(), V.data_ptr(), Q_obs.data_ptr(),
+                                int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
+                                float(tau), ctypes.byref(var), out_K.data_ptr(), out_V.data_ptr(),
+                                out_idx.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                _stream_ptr(stream))
+    _check(rc, "rkv_compress_ex")
     return out_K, out_V, out_idx
 
 
@@ -204,9 +242,7 @@ def rkv_compress_noalloc(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8
     return out_K, out_V, out_idx
 
 
-def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
-              tau: float = 0.9, workspace=None, stream=None):
-    """(I, R, Z), each fp32 [P, n_cached]."""
+def _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, variant, workspace, stream):
     _cuda(K, "K")
     _cuda(Q_obs, "Q_obs")
     G = Q_obs.shape[1]
@@ -217,12 +253,32 @@ def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: i
     Z = torch.empty_like(I)
     if workspace is None:
         workspace = alloc_workspace(K, G, n_cached, n_obs)
-    rc = load().rkv_score(ctypes.byref(desc), K.data_ptr(), Q_obs.data_ptr(), int(n_cached),
-                          int(n_obs), float(lam), int(beta), float(tau), I.data_ptr(),
-                          R.data_ptr(), Z.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                          _stream_ptr(stream))
-    _check(rc, "rkv_score")
+    args = (int(n_cached), int(n_obs), float(lam), int(beta), float(tau))
+    outs = (I.data_ptr(), R.data_ptr(), Z.data_ptr(), workspace.data_ptr(), workspace.numel(),
+            _stream_ptr(stream))
+    if variant is None:
+        rc = load().rkv_score(ctypes.byref(desc), K.data_ptr(), Q_obs.data_ptr(), *args, *outs)
+        _check(rc, "rkv_score")
+    else:
+        rc = load().rkv_score_ex(ctypes.byref(desc), K.data_ptr(), Q_obs.data_ptr(), *args,
+                                 ctypes.byref(variant), *outs)
+        _check(rc, "rkv_score_ex")
     return I, R, Z
+
+
+def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
+              tau: float = 0.9, workspace=None, stream=None):
+    """(I, R, Z), each fp32 [P, n_cached]."""
+    return _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, None, workspace, stream)
+
+
+def rkv_score_ex(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
+                 tau: float = 0.9, redundancy_softmax: bool = False, pool_window: int = 1,
+                 workspace=None, stream=None):
+    """(I', R', Z), each fp32 [P, n_cached], for a scoring variant (see
+    rkv_compress_ex); I' and R' are the terms that enter Z."""
+    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
+    return _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, var, workspace, stream)
 
 
 def rkv_select(Z, n_obs: int, budget: int, out_idx=None, stream=None):

@@ -114,6 +114,39 @@ int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cach
               float* out_I, float* out_R, float* out_Z,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Variants of the scoring (both off: the step above).
+ *   redundancy_softmax  the R-KV review, question 2, cause 3, lists a softmax
+ *                       of the redundancy among the operations of a
+ *                       compression round.  1: the candidates' redundancy
+ *                       becomes R'_i = exp(R_i) / sum_{j<C} exp(R_j) (R_i as
+ *                       above, C = n_cached - n_obs candidates), so it sums
+ *                       to 1 over the candidates; 0: R as above.
+ *   pool_window         w, odd, 1..RKV_MAX_POOL_WINDOW.  A SnapKV-style
+ *                       pooling of the importance over positions (SnapKV is
+ *                       the attention-only method the review compares
+ *                       against): I'_i = max of I_j over the candidates j
+ *                       with |j - i| <= (w-1)/2 (the window is cut at the
+ *                       candidates' ends).  1: no pooling.
+ * Z_i = lambda*I'_i - (1-lambda)*R'_i; observation tokens keep their I, get
+ * R = 0 and Z = +inf as before.  A NULL variant is both off. */
+typedef struct {
+    int32_t redundancy_softmax; /* 0 or 1 */
+    int32_t pool_window;        /* odd, 1 .. RKV_MAX_POOL_WINDOW */
+} rkv_variant;
+#define RKV_MAX_POOL_WINDOW 255
+
+/* rkv_compress / rkv_score with a variant (invalid variant fields:
+ * RKV_ERR_INVALID_ARG).  rkv_score_ex's out_I and out_R are the I' and R'
+ * that enter Z. */
+int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                    int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                    const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
+                    void* workspace, size_t workspace_bytes, void* stream);
+int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cached,
+                 int n_obs, float lambda, int beta, float tau, const rkv_variant* variant,
+                 float* out_I, float* out_R, float* out_Z,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* The selection alone: for scores Z [P, n] (fp32), out_idx [P, budget] as
  * rkv_compress would produce it (top budget-n_obs of the candidates
  * 0..n-n_obs-1 by Z, ties to the larger index, then the n_obs observation
@@ -144,8 +177,9 @@ int rkv_get_device_status(void* workspace, void* stream);
  * the scratch is a static array of RKV_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads it until exit.  Requests whose
  * rkv_workspace_size() exceeds it return RKV_ERR_TOO_LARGE before anything is
- * enqueued (16 MiB holds the scratch of about one million token slots, e.g.
- * one Llama-8B layer at batch 64 with N = 1152, or 240 problems of 4096).  Never allocates or frees device memory.
+ * enqueued (16 MiB holds the scratch of about 700 thousand token slots, e.g.
+ * one Llama-8B layer at batch 64 with N = 1152, or 195 problems of 4096).
+ * Never allocates or frees device memory.
  * The first call on each device, made with that device current, looks up the
  * array's device address (cudaGetSymbolAddress) and caches it; make that first
  * call before any stream capture.  All calls share the array (its error word

@@ -10,12 +10,14 @@ independent problems); this module only marshals numpy arrays through ctypes.
 Every function follows the R-KV review page (yoonschallenge.tistory.com/1236):
 the opening notes and the summary-table rows "Decoding-time compression
 scheme", "importance", "redundancy" and "final selection criterion", and
-question 2, cause 3 (the steps of one compression round).  The readings of the
+question 2, cause 3 (the steps of one compression round, which include a
+softmax of the redundancy: the variant ``variant()`` applies it, together with
+a SnapKV-style pooling window on the importance).  The readings of the
 points those passages leave open are listed at the top of ``rkv_oracle.c``.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, brute force over subsets, library routines, invariants).  What
-no pin can decide is whether readings R1-R9 are what the R-KV authors ran: the
+no pin can decide is whether readings R1-R11 are what the R-KV authors ran: the
 pages print no value that could settle it.
 """
 from __future__ import annotations
@@ -77,6 +79,10 @@ def _load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                 i32p, ctypes.c_int, ctypes.c_void_p]
             lib.rkv_oracle_gather_bytes.restype = None
+            lib.rkv_oracle_variant.argtypes = [
+                dp, dp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_int, ctypes.c_int, dp, dp, dp]
+            lib.rkv_oracle_variant.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -158,6 +164,25 @@ def select(Z, n_obs: int, budget: int) -> np.ndarray:
     return idx
 
 
+def variant(sc: dict, n_obs: int, lam: float, redundancy_softmax: bool = False,
+            pool_window: int = 1) -> dict:
+    """The scores of a variant (readings R10, R11) from the base scores
+    ``sc`` of ``score()``: a copy of ``sc`` whose I, R, Z are I pooled over
+    ``pool_window`` positions, R softmaxed over the candidates, and their
+    combination."""
+    I, R = _f64(sc["I"]), _f64(sc["R"])
+    P, N = I.shape
+    out = dict(sc)
+    out["I"], out["R"], out["Z"] = (np.empty((P, N), dtype=np.float64) for _ in range(3))
+    rc = _load().rkv_oracle_variant(
+        _ptr(I, ctypes.c_double), _ptr(R, ctypes.c_double), P, N, n_obs, float(lam),
+        1 if redundancy_softmax else 0, int(pool_window), _ptr(out["I"], ctypes.c_double),
+        _ptr(out["R"], ctypes.c_double), _ptr(out["Z"], ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle variant: invalid sizes")
+    return out
+
+
 def gather(src: np.ndarray, idx: np.ndarray) -> np.ndarray:
     """out[p, r] = src[p, idx[p, r]] for the budget rows, bytes copied
     exactly; src [P, n_cap, ...] of any dtype.  Rows past budget are zero."""
@@ -173,7 +198,8 @@ def gather(src: np.ndarray, idx: np.ndarray) -> np.ndarray:
 
 
 def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
-             beta: int, tau: float, nthreads: int | None = None) -> dict:
+             beta: int, tau: float, nthreads: int | None = None,
+             redundancy_softmax: bool = False, pool_window: int = 1) -> dict:
     """Scores and selection of one compression round of P problems.
     K [P, n_cap, d] (rows >= n_cached ignored), Q [P, G, n_obs, d].  Returns
     dict(idx, scores); the kept rows themselves are ``gather(src, idx)``.
@@ -187,5 +213,7 @@ def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
         sc = None
     else:
         sc = score(_f64(K)[:, :n_cached], Q, n_obs, lam, beta, tau, nthreads)
+        if redundancy_softmax or pool_window != 1:
+            sc = variant(sc, n_obs, lam, redundancy_softmax, pool_window)
         idx = select(sc["Z"], n_obs, budget)
     return {"idx": idx, "scores": sc}

@@ -10,8 +10,9 @@
  *
  * Sources (the pages the method is taken from):
  *   [notes]      R-KV review (yoonschallenge.tistory.com/1236), opening notes:
- *                B_budget / B_buffer, "keep the newest 8, score the rest, keep
- *                the top ones, evict, generate 128 more".
+ *                B_budget / B_buffer; the newest 8 tokens always stay, the
+ *                others are scored, the best that fit the budget are kept,
+ *                the rest evicted, and 128 more tokens are generated.
  *   [scheme]     same page, summary table, row "Decoding-time compression
  *                scheme": merge cache and buffer, always keep some recent
  *                observation tokens, prune the rest by score; buffer 128,
@@ -30,7 +31,11 @@
  *                Z = lambda * I - (1 - lambda) * R.
  *   [cause3]     same page, question 2, cause 3: the steps of one compression
  *                round (attention importance, key normalisation, all-pairs
- *                cosine similarity, combine, top-k, copy the kept KV).
+ *                cosine similarity, a softmax of the redundancy, combine,
+ *                top-k, copy the kept KV).
+ *   [snapkv]     same page, summary table: SnapKV, the attention-only method
+ *                R-KV is compared with; its importance is pooled over
+ *                neighbouring positions.
  *
  * Readings of points the pages leave open (each is stated where it is used):
  *   R1  importance: mean over the n_obs observation queries of the softmax
@@ -43,12 +48,19 @@
  *       than beta tokens newer than i are similar to it; a protected token
  *       drops its above-tau similarities from its redundancy sum.
  *   R5  zero-norm key: norms are clamped to eps = 1e-12, so S = 0.
- *   R6  no softmax over redundancy (the cause-3 list names one, but the
- *       redundancy is a mean cosine similarity; identical keys give R = 1).
+ *   R6  by default no softmax over redundancy (the cause-3 list names one,
+ *       but the redundancy is a mean cosine similarity; identical keys give
+ *       R = 1).  The softmax is variant R10.
  *   R7  ties in Z: the larger (more recent) index wins.
  *   R8  kept indices are returned in ascending order; the n_obs observation
  *       tokens are always the last n_obs of them.
  *   R9  n_cached <= budget: nothing is evicted (identity).
+ *   R10 variant, redundancy softmax: R'_i = exp(R_i) / sum_{j<C} exp(R_j)
+ *       over the C = N - n_obs candidates (temperature 1); observation
+ *       tokens are not candidates.
+ *   R11 variant, importance pooling: I'_i = max of I_j over the candidates j
+ *       with |j - i| <= (w-1)/2 for an odd window w, the window cut at the
+ *       candidates' ends; applied to I after the max over query heads.
  *
  * Layouts (row-major, contiguous, fp64):
  *   K  [P, N, d]          keys of the merged cache (budget rows, then buffer)
@@ -323,6 +335,48 @@ int rkv_oracle_select(const double* Z, int64_t P, int N, int n_obs, int budget, 
         for (int r = 0; r < n_obs; ++r) out[k + r] = C + r;
     }
     free(buf);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* scoring variants [cause3: redundancy softmax] [snapkv: pooling]     */
+/* ------------------------------------------------------------------ */
+
+/* From one call's base scores I, R [P, N], the variant scores: I_out = I
+ * pooled over a window of w positions (R11; w = 1 leaves I as it is), R_out =
+ * the softmax of R over the candidates (R10) when softmax != 0 (else R), and
+ * Z = lambda * I_out - (1 - lambda) * R_out.  Observation tokens keep I,
+ * get R = 0 and Z = +inf.  Returns 0, or -1 for invalid sizes. */
+int rkv_oracle_variant(const double* I, const double* R, int64_t P, int N, int n_obs,
+                       double lambda, int softmax, int window, double* I_out, double* R_out,
+                       double* Z) {
+    if (P < 0 || N < 1 || n_obs < 0 || n_obs >= N || window < 1 || window % 2 == 0) return -1;
+    const int C = N - n_obs, h = (window - 1) / 2;
+    for (int64_t p = 0; p < P; ++p) {
+        const double* ip = I + p * (int64_t)N;
+        const double* rp = R + p * (int64_t)N;
+        double* io = I_out + p * (int64_t)N;
+        double* ro = R_out + p * (int64_t)N;
+        double* z = Z + p * (int64_t)N;
+        double m = -INFINITY, total = 0.0;
+        if (softmax) {
+            for (int j = 0; j < C; ++j) m = rp[j] > m ? rp[j] : m;
+            for (int j = 0; j < C; ++j) total += exp(rp[j] - m);
+        }
+        for (int i = 0; i < C; ++i) {
+            const int lo = i - h < 0 ? 0 : i - h, hi = i + h > C - 1 ? C - 1 : i + h;
+            double best = ip[lo];
+            for (int j = lo + 1; j <= hi; ++j) best = ip[j] > best ? ip[j] : best;
+            io[i] = best;
+            ro[i] = softmax ? exp(rp[i] - m) / total : rp[i];
+            z[i] = lambda * io[i] - (1.0 - lambda) * ro[i];
+        }
+        for (int i = C; i < N; ++i) {
+            io[i] = ip[i];
+            ro[i] = 0.0;
+            z[i] = INFINITY;
+        }
+    }
     return 0;
 }
 

@@ -4,7 +4,9 @@ Tolerances (the target fixed for this method): scores I, R, Z within 2e-3
 absolute; kept sets identical except tokens whose oracle score lies within
 2e-3 of the k-th largest oracle score, or whose protection/similarity depends
 on a threshold-borderline pair (|S_ij - tau| < 1e-5); gathered rows
-bit-exact for the GPU's own indices.
+bit-exact for the GPU's own indices.  Scoring variants (the redundancy
+softmax puts R near 1/C) take the same 2e-3 relative to each problem's scale
+max_i |X*_i|, which is never looser than the absolute bound there.
 """
 from __future__ import annotations
 
@@ -27,6 +29,24 @@ def score_errors(gpu: dict, sc: dict, C: int) -> dict:
     return out
 
 
+def scaled_score_errors(gpu: dict, sc: dict, C: int) -> dict:
+    """Max over problems of the error of I, R, Z over the candidates relative
+    to the problem's scale max_i |X*_i| (for scoring variants whose values
+    are ~1/C, where an absolute 2e-3 would compare nothing)."""
+    out = {}
+    for name in ("I", "R", "Z"):
+        g = gpu[name].detach().cpu().double().numpy()[:, :C]
+        ref = sc[name][:, :C]
+        scale = np.maximum(np.abs(ref).max(axis=1), 1e-300)
+        out[name] = float((np.abs(g - ref).max(axis=1) / scale).max())
+    return out
+
+
+def scaled_band(sc: dict, C: int, rel: float = KEPT_BAND) -> np.ndarray:
+    """Per-problem tie band rel * max_i |Z*_i| over the candidates."""
+    return rel * np.abs(sc["Z"][:, :C]).max(axis=1)
+
+
 def check_observation_scores(gpu: dict, C: int):
     R = gpu["R"].detach().cpu().numpy()
     Z = gpu["Z"].detach().cpu().numpy()
@@ -42,8 +62,9 @@ def check_idx_valid(idx: np.ndarray, N: int, budget: int, n_obs: int):
 
 
 def kept_mismatches(idx_gpu: np.ndarray, sc: dict, budget: int, n_obs: int,
-                    band: float = KEPT_BAND) -> tuple[int, int]:
-    """(unexcused, excused) counts of tokens kept by one side only."""
+                    band=KEPT_BAND) -> tuple[int, int]:
+    """(unexcused, excused) counts of tokens kept by one side only; `band` is
+    one number or one per problem."""
     P, N = sc["Z"].shape
     C, k = N - n_obs, budget - n_obs
     ref = oracle.select(sc["Z"], n_obs, budget)
@@ -52,8 +73,9 @@ def kept_mismatches(idx_gpu: np.ndarray, sc: dict, budget: int, n_obs: int,
         z = sc["Z"][p, :C]
         zk = np.sort(z)[::-1][k - 1]
         diff = set(idx_gpu[p, :k].tolist()) ^ set(ref[p, :k].tolist())
+        b = band[p] if np.ndim(band) else band
         for i in diff:
-            if abs(z[i] - zk) <= band or sc["border"][p, i]:
+            if abs(z[i] - zk) <= b or sc["border"][p, i]:
                 ok += 1
             else:
                 bad += 1

@@ -104,11 +104,83 @@ def test_long_context_selection_paths(cuda_ok, n_cached, budget):
     """Long contexts on both sides of the fused select + gather's shared-memory
     limit (scores, sort keys and kept indices of one problem): the first size
     runs the fused kernel with ~150 KB of shared memory, the second the
-    separate select and gather kernels."""
+    separate select and gather kernels (and, with a scoring variant, the
+    separate variant kernel)."""
     w = wl.BY_NAME["llama8b_layer"].scaled(head_dim=64, n_cached=n_cached, budget=budget,
                                            layers=1, batch=1, kv_heads=1)
     K, V, Q = wl.make_inputs(w, device=DEV)
     _full_check(w, K, V, Q, [0])
+    _variant_check(w, K, V, Q, [0], True, 5)
+
+
+def _variant_check(w, K, V, Q, problems, softmax, window, in_place=False):
+    """Variant scores through rkv_score_ex and the kept set and rows through
+    rkv_compress_ex, against the oracle's base scores plus its variant."""
+    C = w.n_cached - w.n_obs
+    I, R, Z = rkv.rkv_score_ex(K, Q, w.n_cached, w.n_obs, w.lam, w.beta, w.tau,
+                               redundancy_softmax=softmax, pool_window=window)
+    base = _oracle_scores(K, Q, w, problems)
+    sc = oracle.variant(base, w.n_obs, w.lam, softmax, window)
+    sub = {"I": I[problems], "R": R[problems], "Z": Z[problems]}
+    err = parity.scaled_score_errors(sub, sc, C)
+    assert max(err.values()) <= parity.SCORE_ATOL, err
+    parity.check_observation_scores(sub, C)
+    src_K, src_V = (K.clone(), V.clone()) if in_place else (K, V)
+    oK, oV, idx = rkv.rkv_compress_ex(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta,
+                                      w.tau, redundancy_softmax=softmax, pool_window=window,
+                                      **({"out_K": K, "out_V": V} if in_place else {}))
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    parity.check_idx_valid(gi, w.n_cached, w.budget, w.n_obs)
+    # the step forms Z inside its selection kernel with the same arithmetic as
+    # rkv_score_ex: the same Z bit for bit, so the same kept set everywhere
+    np.testing.assert_array_equal(gi, rkv.rkv_select(Z, w.n_obs, w.budget).cpu().numpy())
+    bad, excused = parity.kept_mismatches(gi[problems], sc, w.budget, w.n_obs,
+                                          band=parity.scaled_band(sc, C))
+    assert bad == 0, f"{bad} kept-set mismatches outside the tie band ({excused} excused)"
+    parity.check_gathered(oK, src_K, idx, w.budget, problems)
+    parity.check_gathered(oV, src_V, idx, w.budget, problems)
+    return err, excused
+
+
+@pytest.mark.parametrize("softmax,window", [(True, 1), (False, 7), (True, 7), (True, 255)])
+def test_scoring_variants_llama_layer(cuda_ok, softmax, window):
+    """Redundancy softmax and importance pooling window on Llama-shaped
+    problems (tensor-core scoring path)."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(kv_heads=2)
+    K, V, Q = wl.make_inputs(w, device=DEV)
+    _variant_check(w, K, V, Q, list(range(w.problems)), softmax, window)
+
+
+def test_scoring_variants_other_paths(cuda_ok):
+    """The variants after the CUDA-core scoring (fp32; beta above the
+    tensor-core path's cap), after the two-pass importance (long rows), and
+    with in-place compaction."""
+    tiny = wl.BY_NAME["tiny"]
+    K, V, Q = wl.make_inputs(tiny, device=DEV)
+    _variant_check(tiny, K, V, Q, list(range(tiny.problems)), True, 5)
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=640, budget=512, kv_heads=1, beta=64)
+    K, V, Q = wl.make_inputs(w, device=DEV)
+    _variant_check(w, K, V, Q, list(range(w.problems)), True, 3, in_place=True)
+    q = wl.BY_NAME["qwen14b"].scaled(layers=1, batch=1, kv_heads=2)
+    K, V, Q = wl.make_inputs(q, device=DEV)
+    _variant_check(q, K, V, Q, [0, 1], True, 9)
+
+
+def test_parameter_sweep(cuda_ok):
+    """lambda, beta and tau swept one at a time around the page's setting
+    (beta 64 takes the CUDA-core Gram, tau <= 0 the all-pairs branch), with
+    and without the variants."""
+    base = wl.BY_NAME["llama8b_layer"].scaled(n_cached=640, budget=512, kv_heads=2)
+    K, V, Q = wl.make_inputs(base, device=DEV)
+    for lam in (0.0, 0.05, 0.3, 0.7, 1.0):
+        _full_check(base.scaled(lam=lam), K, V, Q, [0, 1])
+    for beta in (0, 1, 3, 8, 63, 64):
+        _full_check(base.scaled(beta=beta), K, V, Q, [0, 1])
+    for tau in (-0.2, 0.0, 0.3, 0.6, 0.95):
+        _full_check(base.scaled(tau=tau), K, V, Q, [0, 1])
+    for lam, beta, tau in ((0.0, 2, 0.9), (0.5, 8, 0.6), (1.0, 1, 0.3)):
+        _variant_check(base.scaled(lam=lam, beta=beta, tau=tau), K, V, Q, [0, 1], True, 7)
 
 
 def test_parameter_variants(cuda_ok):

@@ -52,9 +52,9 @@ def _desc(P=4, G=4, d=128, n_cap=1152, dtype=0):
 def test_workspace_size(lib):
     d = _desc()
     n = lib.rkv_workspace_size(ctypes.byref(d), 1152, 8)
-    # status block + four fp32 [P, N] arrays + the [P, 16, 128] bf16 s rows,
-    # each rounded to 256 bytes
-    assert n == 256 + 4 * ((4 * 1152 * 4 + 255) // 256 * 256) + (2 * 4 * 16 * 128 + 255) // 256 * 256
+    # status block + five fp32 [P, N] arrays (inverse norms, similarity sums,
+    # I, R, Z) + the [P, 16, 128] bf16 s rows, each rounded to 256 bytes
+    assert n == 256 + 5 * ((4 * 1152 * 4 + 255) // 256 * 256) + (2 * 4 * 16 * 128 + 255) // 256 * 256
     assert lib.rkv_workspace_size(None, 1152, 8) == 0
     bad = _desc(d=96)
     assert lib.rkv_workspace_size(ctypes.byref(bad), 1152, 8) == 0
@@ -84,6 +84,30 @@ def test_argument_errors_need_no_device(lib):
     assert lib.rkv_select(1, 100, fake, 8, 100, fake, None) == 1   # budget >= n
     assert lib.rkv_select(1, 100, fake, 9, 8, fake, None) == 1     # n_obs > budget
     assert lib.rkv_gather(ctypes.byref(d), fake, fake, 0, fake, None) == 1
+
+
+def test_variant_argument_errors(lib):
+    """rkv_compress_ex / rkv_score_ex reject an invalid variant before
+    anything else (nothing is dereferenced or enqueued)."""
+    from decode_kv_cache_02_gb300 import rkv
+    d = _desc()
+    fake = 1 << 20
+    for soft, win in ((2, 1), (-1, 1), (0, 0), (0, 2), (1, 8), (0, rkv.RKV_MAX_POOL_WINDOW + 2),
+                      (0, -3)):
+        v = rkv._Variant(soft, win)
+        rc = lib.rkv_compress_ex(ctypes.byref(d), fake, fake + 2 ** 30, fake + 2 ** 31, 1152,
+                                 1024, 8, 0.1, 2, 0.9, ctypes.byref(v), fake + 2 ** 32,
+                                 fake + 2 ** 33, fake + 2 ** 34, fake + 2 ** 35, 1 << 40, None)
+        assert rc == 1, (soft, win)
+        rc = lib.rkv_score_ex(ctypes.byref(d), fake, fake + 2 ** 31, 1152, 8, 0.1, 2, 0.9,
+                              ctypes.byref(v), fake + 2 ** 32, fake + 2 ** 33, fake + 2 ** 34,
+                              fake + 2 ** 35, 1 << 40, None)
+        assert rc == 1, (soft, win)
+    # a valid variant still meets the ordinary checks (workspace too small)
+    v = rkv._Variant(1, rkv.RKV_MAX_POOL_WINDOW)
+    assert lib.rkv_compress_ex(ctypes.byref(d), fake, fake + 2 ** 30, fake + 2 ** 31, 1152, 1024,
+                               8, 0.1, 2, 0.9, ctypes.byref(v), fake + 2 ** 32, fake + 2 ** 33,
+                               fake + 2 ** 34, fake + 2 ** 35, 10, None) == 3
 
 
 def test_binding_rejects_cpu_tensors(lib):

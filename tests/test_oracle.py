@@ -213,7 +213,7 @@ def _key_order_ok(Z, kept, C):
 
 @pytest.mark.parametrize("seed", range(6))
 def test_selection_brute_force(seed):
-    """Top-k row ('keep the top tokens to fit the budget'): for tiny problems,
+    """Top-k row (the best tokens that fit the budget are kept): for tiny problems,
     enumerate every k-subset of candidates; the oracle's kept set has the
     largest total score, and ties are broken toward larger indices."""
     rng = np.random.default_rng(100 + seed)
@@ -285,6 +285,106 @@ def test_duplicate_earlier_copy_goes_first(copies, beta):
     idx = oracle.select(sc["Z"], n_obs, N - 1)[0]
     evicted = sorted(set(range(N)) - set(idx.tolist()))
     assert evicted == [pos[0]]
+
+
+# --------------------------------------------------------------- variants --
+# Question 2, cause 3 of the review lists a softmax of the redundancy; the
+# summary table's comparison method SnapKV pools its importance over
+# positions.  Readings R10 / R11 of the oracle; off by default.
+
+def _sc(I, R):
+    return {"I": np.asarray(I, dtype=np.float64), "R": np.asarray(R, dtype=np.float64)}
+
+
+@pytest.mark.parametrize("w", [3, 7, 31])
+def test_variant_pooling_equals_maximum_filter(w):
+    """I' = max of I over the window, cut at the candidates' ends:
+    scipy.ndimage.maximum_filter1d with edge replication is the same window
+    maximum (catches an off-by-one half width or a window reaching into the
+    observation tokens)."""
+    from scipy.ndimage import maximum_filter1d
+    wk = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(wk)
+    sc = oracle.score(K, Q, wk.n_obs, wk.lam, wk.beta, wk.tau)
+    C = wk.n_cached - wk.n_obs
+    out = oracle.variant(sc, wk.n_obs, wk.lam, pool_window=w)
+    ref = maximum_filter1d(sc["I"][:, :C], size=w, axis=1, mode="nearest")
+    np.testing.assert_array_equal(out["I"][:, :C], ref)
+    np.testing.assert_array_equal(out["I"][:, C:], sc["I"][:, C:])
+    np.testing.assert_array_equal(out["R"], sc["R"])
+    np.testing.assert_allclose(out["Z"][:, :C], wk.lam * ref - (1 - wk.lam) * sc["R"][:, :C],
+                               rtol=0, atol=1e-15)
+
+
+def test_variant_pooling_spike_closed_form():
+    """A single spike spreads to exactly the (w-1)/2 neighbours on each side
+    inside the candidates; a spike on an observation token spreads nowhere."""
+    N, n_obs, w = 20, 4, 5
+    C = N - n_obs
+    for s_ in (0, 7, C - 1, C + 1):
+        I = np.zeros((1, N))
+        I[0, s_] = 1.0
+        out = oracle.variant(_sc(I, np.zeros((1, N))), n_obs, 1.0, pool_window=w)
+        exp = np.zeros(N)
+        if s_ < C:
+            exp[max(0, s_ - 2):min(C, s_ + 3)] = 1.0
+        else:
+            exp[s_] = 1.0
+        np.testing.assert_array_equal(out["I"][0], exp)
+
+
+def test_variant_softmax_equals_scipy():
+    """R' = softmax of R over the C candidates only (scipy.special.softmax
+    of the candidates' row); observation tokens R = 0, Z = +inf."""
+    from scipy.special import softmax
+    wk = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(wk)
+    sc = oracle.score(K, Q, wk.n_obs, wk.lam, wk.beta, wk.tau)
+    C = wk.n_cached - wk.n_obs
+    out = oracle.variant(sc, wk.n_obs, wk.lam, redundancy_softmax=True)
+    ref = softmax(sc["R"][:, :C], axis=1)
+    np.testing.assert_allclose(out["R"][:, :C], ref, rtol=1e-13, atol=0)
+    np.testing.assert_allclose(out["R"][:, :C].sum(axis=1), 1.0, rtol=0, atol=1e-13)
+    assert np.all(out["R"][:, C:] == 0) and np.all(np.isposinf(out["Z"][:, C:]))
+    np.testing.assert_array_equal(out["I"], sc["I"])
+
+
+def test_variant_softmax_closed_form():
+    """R_j = ln c_j gives R'_j = c_j / sum c exactly (up to rounding)."""
+    c = np.array([1.0, 2.0, 3.0, 4.0, 10.0])
+    N, n_obs = 7, 2
+    R = np.zeros((1, N))
+    R[0, :5] = np.log(c)
+    out = oracle.variant(_sc(np.zeros((1, N)), R), n_obs, 0.0, redundancy_softmax=True)
+    np.testing.assert_allclose(out["R"][0, :5], c / c.sum(), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(out["Z"][0, :5], -c / c.sum(), rtol=1e-14, atol=0)
+
+
+def test_variant_identical_keys_uniform_redundancy():
+    """All keys identical: R = 1 everywhere, so the softmax is 1/C."""
+    P, N, d, n_obs = 2, 30, 8, 4
+    K = np.tile(np.random.default_rng(3).standard_normal(d), (P, N, 1))
+    Q = np.random.default_rng(4).standard_normal((P, 2, n_obs, d))
+    sc = oracle.score(K, Q, n_obs, 0.1, 2, 0.9)
+    out = oracle.variant(sc, n_obs, 0.1, redundancy_softmax=True)
+    np.testing.assert_allclose(out["R"][:, :N - n_obs], 1.0 / (N - n_obs), rtol=1e-14, atol=0)
+
+
+def test_variant_off_is_identity_and_softmax_keeps_redundancy_order():
+    """Window 1 without softmax changes nothing; the softmax is monotone, so
+    with lambda = 0 (redundancy only) the kept set does not change."""
+    wk = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(wk)
+    sc = oracle.score(K, Q, wk.n_obs, 0.0, wk.beta, wk.tau)
+    same = oracle.variant(sc, wk.n_obs, 0.0)
+    for k_ in ("I", "R", "Z"):
+        np.testing.assert_array_equal(same[k_], sc[k_])
+    soft = oracle.variant(sc, wk.n_obs, 0.0, redundancy_softmax=True)
+    np.testing.assert_array_equal(oracle.select(soft["Z"], wk.n_obs, wk.budget),
+                                  oracle.select(sc["Z"], wk.n_obs, wk.budget))
+    res = oracle.compress(K, Q, wk.n_cached, wk.budget, wk.n_obs, 0.0, wk.beta, wk.tau,
+                          redundancy_softmax=True)
+    np.testing.assert_array_equal(res["idx"], oracle.select(sc["Z"], wk.n_obs, wk.budget))
 
 
 # ------------------------------------------------------------- invariants --
