@@ -373,6 +373,118 @@ def run_sweep(args, w):
             print(json.dumps(line), flush=True)
 
 
+def run_paged(args, w):
+    """The step on a paged cache (rkv_paged_compress, in place): the
+    workload's K, V scattered into [num_blocks, H, bs, d] pools through a
+    shuffled block table.  Each round compacts the pools and clears the
+    table's freed entries, so the pristine pools and table are restored
+    between timed rounds (outside the events; the 9.7 GB copy also flushes
+    L2) and the K rounds' event times are summed."""
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rkv.load()
+    bs = args.block_size
+    S, H, N, d = w.layers * w.batch, w.kv_heads, w.n_cached, w.head_dim
+    nb = -(-N // bs)
+    num_blocks = S * nb
+    g = torch.Generator().manual_seed(w.seed)
+    table0 = torch.randperm(num_blocks, generator=g).reshape(S, nb).to(torch.int32).to(dev)
+    K, V, Q = wl.make_inputs(w, device=dev, seed=w.seed + rank)
+    pools = []
+    for X in (K, V):
+        pool = torch.zeros((num_blocks, H, bs, d), dtype=X.dtype, device=dev)
+        Xl = X[:, :N].reshape(S, H, N, d)
+        if nb * bs > N:
+            Xl = torch.cat([Xl, torch.zeros((S, H, nb * bs - N, d), dtype=X.dtype, device=dev)], 2)
+        pool[table0.long()] = Xl.reshape(S, H, nb, bs, d).permute(0, 2, 1, 3, 4)
+        pools.append(pool)
+    del K, V
+    K0, V0 = pools
+    K_pool, V_pool, table = K0.clone(), V0.clone(), table0.clone()
+    n_free = rkv.rkv_paged_freed_per_seq(K_pool, table, N, w.budget)
+    idx = torch.empty((S * H, w.budget), dtype=torch.int32, device=dev)
+    freed = torch.empty((S, n_free), dtype=torch.int32, device=dev)
+    ws = torch.zeros(rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, N, w.n_obs),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def restore():
+        K_pool.copy_(K0)
+        V_pool.copy_(V0)
+        table.copy_(table0)
+
+    def step():
+        rkv.rkv_paged_compress(K_pool, V_pool, Q, table, N, w.budget, w.n_obs, w.lam, w.beta,
+                               w.tau, redundancy_softmax=args.redundancy_softmax,
+                               pool_window=args.pool_window, out_idx=idx, out_freed=freed,
+                               workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        restore()
+        step()
+    torch.cuda.synchronize()
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    rkv.rkv_timing_read(reset=True)
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        for a, b in evs:
+            restore()
+            a.record(stream)
+            rkv.rkv_timing_enable(True)
+            step()
+            rkv.rkv_timing_enable(False)
+            b.record(stream)
+        torch.cuda.synchronize()
+    elapsed = sum(a.elapsed_time(b) for a, b in evs)
+    timing = rkv.rkv_timing_read(reset=True)
+    kernels = {k: {"ms": v[0], "launches": v[1]} for k, v in timing.items() if v[1] > 0}
+    if rkv.rkv_get_device_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device error in the timed region")
+    # rows the in-place compaction moves: from each problem's first evicted
+    # position on (the identity prefix stays where it is)
+    ar = torch.arange(w.budget, device=dev, dtype=torch.int32)
+    first = torch.where(idx != ar, ar, w.budget).min(dim=1).values
+    moved_rows = int((w.budget - first).sum())
+    es = 2 if w.dtype == "bf16" else 4
+    P = S * H
+    model = {
+        "key_stats_paged": {"bytes": 2 * P * N * d * es + 2 * P * N * 4},
+        "compact_paged": {"bytes": P * (N - w.n_obs) * 4 + P * w.budget * 4
+                          + 4 * moved_rows * d * es},
+    }
+    peaks = _peaks()
+    roof = {}
+    for k, v in kernels.items():
+        per = v["ms"] / v["launches"] * 1e-3
+        e = {"ms_per_launch": per * 1e3}
+        if k in model:
+            e["hbm_frac"] = model[k]["bytes"] / per / 1e9 / peaks["hbm_gbs"]
+        if k == "gram_tc":
+            e["tensor_frac"] = P * N * (N - 1) * d / per / 1e12 / peaks["bf16_tflops_sustained"]
+        roof[k] = e
+    line = {
+        "mode": "paged", "metric": METRIC, "value": args.steps * P * N / (elapsed * 1e-3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": elapsed / args.steps, "higher_is_better": True, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": _config(w, block_size=bs, num_seqs=S, num_blocks=num_blocks,
+                          blocks_freed_per_seq=n_free, moved_rows_per_problem=moved_rows / P,
+                          variant={"redundancy_softmax": args.redundancy_softmax,
+                                   "pool_window": args.pool_window},
+                          l2="pools restored between rounds (9.7 GB copy, flushes L2)"),
+        "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
+        "roofline_all": roof,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args, w):
     world, rank, local = _dist()
     if world > 1:
@@ -607,6 +719,9 @@ def main():
                     help="scoring variant: softmax of the redundancy over the candidates")
     ap.add_argument("--pool-window", type=int, default=1,
                     help="scoring variant: odd max-pooling window on the importance")
+    ap.add_argument("--paged", action="store_true",
+                    help="time the step on a paged cache (block pools + block table)")
+    ap.add_argument("--block-size", type=int, default=16, help="rows per block with --paged")
     ap.add_argument("--sweep", action="store_true",
                     help="time the step over a lambda/beta/tau/variant sweep, one line each")
     args = ap.parse_args()
@@ -617,6 +732,8 @@ def main():
         run_reference(args, w)
     elif args.sweep:
         run_sweep(args, w)
+    elif args.paged:
+        run_paged(args, w)
     elif w.gen_tokens:
         run_stream(args, w)
     else:

@@ -21,8 +21,13 @@
 //           before the first evicted token are skipped and the rest move in
 //           ascending chunks, each read completely before any of it is written
 //           (kept indices are ascending and idx[r] >= r).
+//   paged   the same chunked in-place order through the block table: kept V
+//           rows move inside the pool, kept K rows come from the contiguous
+//           copy the key statistics wrote (so K's reads never meet its
+//           writes); every block id is checked before it is used.
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
+#include "rkv_paged.cuh"
 #include "rkv_variant.cuh"
 #include "../../include/rkv.h"
 
@@ -106,10 +111,12 @@ RKV_DEV int bucket_of(float z, float zmin, float scale) {
     return min(255, max(0, (int)((z - zmin) * scale)));
 }
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads)
 compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
                int32_t* __restrict__ idx, const uint4* a_src, const uint4* b_src, uint4* a_dst,
-               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st, VariantIn var) {
+               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st, VariantIn var,
+               PagedIn pg) {
     extern __shared__ uint32_t s_dyn[];
     const int C = N - n_obs, k = budget - n_obs;
     uint32_t* keys = s_dyn;                                         // [C]
@@ -288,6 +295,49 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
     for (int r = tid; r < budget; r += kThreads) out[r] = sidx[r];
 
     // ------------------------------------------------------------ copy --
+    if constexpr (kPaged) {
+        // a_src: contiguous K copy [P, N, vpr]; a_dst: K pool; b_dst: V pool
+        int l = 0, h = budget;
+        while (l < h) {
+            const int mid = (l + h) >> 1;
+            if (sidx[mid] == mid) l = mid + 1;
+            else h = mid;
+        }
+        const int64_t kc_base = (int64_t)p * N * vpr;
+        const int rows_per_chunk = kThreads * kCopyVecs / vpr;
+        for (int c0 = l; c0 < budget; c0 += rows_per_chunk) {
+            uint4 va[kCopyVecs], vb[kCopyVecs];
+            int64_t dst[kCopyVecs];
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                const int e = t * kThreads + tid;
+                const int r = c0 + e / vpr, v = e % vpr;
+                dst[t] = -1;
+                if (r < budget) {
+                    const int s = sidx[r];
+                    const int64_t dr = paged_phys_row(pg, p, r);
+                    const int64_t sr = (s >= 0 && s < N) ? paged_phys_row(pg, p, s) : -1;
+                    if (dr >= 0 && sr >= 0) {
+                        dst[t] = dr * vpr + v;
+                        va[t] = a_src[kc_base + (int64_t)s * vpr + v];
+                        vb[t] = b_dst[sr * vpr + v];
+                    } else if (v == 0) {
+                        set_error(st, kDevErrIndex, (unsigned)r);
+                    }
+                }
+            }
+            __syncthreads();  // every source row of the chunk has been read
+#pragma unroll
+            for (int t = 0; t < kCopyVecs; ++t) {
+                if (dst[t] >= 0) {
+                    a_dst[dst[t]] = va[t];
+                    b_dst[dst[t]] = vb[t];
+                }
+            }
+            __syncthreads();
+        }
+        return;
+    }
     const int64_t base = (int64_t)p * n_cap * vpr;
     if (!in_place) {
         const int total = budget * vpr;
@@ -372,13 +422,29 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
                            cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
     const size_t smem = compact_smem_bytes(N, n_obs, budget);
-    cudaError_t e =
-        cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(compact_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    compact_kernel<<<(unsigned)P, kThreads, smem, s>>>(
+    compact_kernel<false><<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(src_a),
         static_cast<const uint4*>(src_b), static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), n_cap,
-        row_bytes / 16, in_place ? 1 : 0, st, var);
+        row_bytes / 16, in_place ? 1 : 0, st, var, PagedIn{});
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, int n_obs,
+                                 int budget, int32_t* idx, const void* kc, void* k_pool,
+                                 void* v_pool, const PagedIn& pg, int row_bytes, DeviceStatus* st,
+                                 cudaStream_t s, const VariantIn& var) {
+    if (P == 0 || budget == 0) return cudaSuccess;
+    const size_t smem = compact_smem_bytes(N, n_obs, budget);
+    cudaError_t e = cudaFuncSetAttribute(compact_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    compact_kernel<true><<<(unsigned)P, kThreads, smem, s>>>(
+        Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(kc), nullptr,
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), N, row_bytes / 16, 1, st, var,
+        pg);
     return cudaGetLastError();
 }
 

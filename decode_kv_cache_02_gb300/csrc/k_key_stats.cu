@@ -18,8 +18,14 @@
 // tensor-core importance kernel runs, only pass 1 is needed: it writes
 // |khat_i|^2 into sum_i and s as bf16 rows (hi, lo) that the importance MMA
 // multiplies with every key block anyway, which completes sum_i there.
+//
+// Paged input (kPaged): rows are found through the block table, and pass 1
+// also stores every row, bit for bit, into the contiguous copy Kc [P, N, d]
+// that the tensor-core stages then read (their TMA tiles rely on rows past N
+// reading as zero, which only the contiguous copy gives).
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
+#include "rkv_paged.cuh"
 #include "../../include/rkv.h"
 
 namespace rkv {
@@ -41,17 +47,35 @@ RKV_DEV float group_sum(float v) {
     return v;
 }
 
-template <typename T, int D>
+// 8 consecutive elements as raw 16-byte vectors (one for bf16, two for fp32)
+template <typename T>
+struct Raw8 {
+    static constexpr int kVecs = (int)sizeof(T) * 8 / 16;
+    uint4 u[kVecs];
+    RKV_DEV void load(const T* p) {
+#pragma unroll
+        for (int t = 0; t < kVecs; ++t) u[t] = reinterpret_cast<const uint4*>(p)[t];
+    }
+    RKV_DEV void store(T* p) const {
+#pragma unroll
+        for (int t = 0; t < kVecs; ++t) reinterpret_cast<uint4*>(p)[t] = u[t];
+    }
+    RKV_DEV void to_float(float* o) const { load8(reinterpret_cast<const T*>(u), o); }
+};
+
+template <typename T, int D, bool kPaged>
 __global__ void __launch_bounds__(kThreads)
 key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
                  float* __restrict__ sum_s, int64_t ld, bool two_pass,
-                 __nv_bfloat16* __restrict__ s_rows) {
+                 __nv_bfloat16* __restrict__ s_rows, PagedIn pg, T* __restrict__ Kc,
+                 DeviceStatus* st) {
     constexpr int L = D / 8;                 // lanes per row
     constexpr int RPI = kThreads / L;        // rows per iteration of the CTA
     __shared__ float s_part[RPI][D];
     __shared__ float s_vec[D];
     const int64_t p = blockIdx.x;
     const T* Kp = K + (size_t)p * n_cap * D;
+    T* Kcp = kPaged ? Kc + (size_t)p * N * D : nullptr;
     const int sub = threadIdx.x % L;         // which 8 columns
     const int r0 = threadIdx.x / L;          // first row of this thread
     const int col = sub * 8;
@@ -62,14 +86,47 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
     // ---- pass 1: norms and the partial sums of khat
     for (int base = r0; base < N; base += RPI * kUnroll) {
         float v[kUnroll][8];
+        if constexpr (kPaged) {
+            Raw8<T> raw[kUnroll];
+            bool ok[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int i = base + u * RPI;
-            if (i < N) {
-                load8(Kp + (size_t)i * D + col, v[u]);
-            } else {
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = base + u * RPI;
+                ok[u] = false;
+                if (i < N) {
+                    const int64_t pr = paged_phys_row(pg, p, i);
+                    if (pr >= 0) {
+                        raw[u].load(K + pr * D + col);
+                        ok[u] = true;
+                    } else if (sub == 0) {
+                        set_error(st, kDevErrIndex, (unsigned)i);
+                    }
+                }
+            }
 #pragma unroll
-                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            for (int u = 0; u < kUnroll; ++u) {
+                if (ok[u]) {
+                    raw[u].store(Kcp + (size_t)(base + u * RPI) * D + col);
+                    raw[u].to_float(v[u]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+                    if (base + u * RPI < N) {
+                        Raw8<T> z{};
+                        z.store(Kcp + (size_t)(base + u * RPI) * D + col);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = base + u * RPI;
+                if (i < N) {
+                    load8(Kp + (size_t)i * D + col, v[u]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+                }
             }
         }
 #pragma unroll
@@ -114,6 +171,9 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
     float sv[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) sv[t] = s_vec[col + t];
+    // the paged rows are re-read from the contiguous copy (written above by
+    // this CTA; the barrier makes them visible)
+    const T* Kp2 = kPaged ? Kcp : Kp;
     // ---- pass 2: sum_i = khat_i . s - |khat_i|^2
     for (int base = r0; base < N; base += RPI * kUnroll) {
         float v[kUnroll][8];
@@ -121,7 +181,7 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
         for (int u = 0; u < kUnroll; ++u) {
             const int i = base + u * RPI;
             if (i < N) {
-                load8(Kp + (size_t)i * D + col, v[u]);
+                load8(Kp2 + (size_t)i * D + col, v[u]);
             } else {
 #pragma unroll
                 for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
@@ -146,9 +206,14 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
 
 template <typename T, int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
-    key_stats_kernel<T, D><<<(unsigned)a.P, kThreads, 0, s>>>(
-        static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
-        static_cast<__nv_bfloat16*>(a.s_rows));
+    if (a.pg.table != nullptr)
+        key_stats_kernel<T, D, true><<<(unsigned)a.P, kThreads, 0, s>>>(
+            static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
+            static_cast<__nv_bfloat16*>(a.s_rows), a.pg, static_cast<T*>(a.Kc), a.status);
+    else
+        key_stats_kernel<T, D, false><<<(unsigned)a.P, kThreads, 0, s>>>(
+            static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
+            static_cast<__nv_bfloat16*>(a.s_rows), a.pg, nullptr, a.status);
     return cudaGetLastError();
 }
 

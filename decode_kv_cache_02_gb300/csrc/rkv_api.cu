@@ -36,11 +36,14 @@ enum KernelId {
     kIdentity,
     kCompact,
     kVariant,
+    kKeyStatsPaged,
+    kCompactPaged,
+    kPagedRelease,
     kNumKernels
 };
 const char* const kKernelNames[kNumKernels] = {
     "key_stats", "importance", "importance_tc", "gram_tc", "gram_simt", "select", "gather",
-    "identity_idx", "compact", "variant"};
+    "identity_idx", "compact", "variant", "key_stats_paged", "compact_paged", "paged_release"};
 
 // ---------------------------------------------------------------- timing --
 struct TimedLaunch {
@@ -91,14 +94,16 @@ struct Workspace {
     float* R;
     float* Z;
     void* s_rows;
+    void* Kc;  // paged calls: contiguous copy of the keys [P, N, d]
     int64_t ld;
     size_t bytes;
 };
 
 int64_t row_pitch(int n) { return ((int64_t)n + 3) / 4 * 4; }
 
-// Carves the workspace; with base == nullptr only computes the size.
-Workspace carve(void* base, int64_t P, int n) {
+// Carves the workspace; with base == nullptr only computes the size.  kc_bytes
+// (paged calls) appends the contiguous key copy.
+Workspace carve(void* base, int64_t P, int n, size_t kc_bytes = 0) {
     Workspace w{};
     w.ld = row_pitch(n);
     const size_t arr = align_up(sizeof(float) * (size_t)P * (size_t)w.ld);
@@ -118,6 +123,8 @@ Workspace carve(void* base, int64_t P, int n) {
     off += arr;
     w.s_rows = b + off;
     off += align_up(2 * (size_t)P * 16 * 128);
+    w.Kc = kc_bytes ? b + off : nullptr;
+    off += align_up(kc_bytes);
     w.bytes = off;
     return w;
 }
@@ -170,10 +177,12 @@ int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, 
     return RKV_OK;
 }
 
-// Runs the four scoring stages; I/R/Z land in the given rows.
+// Runs the four scoring stages; I/R/Z land in the given rows.  With a paged
+// K (pg), the key statistics read through the block table and write the
+// contiguous copy w.Kc, which the later stages read.
 int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
-               const Workspace& w, cudaStream_t s) {
+               const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr) {
     // I, R, Z as defined on the page (R may be null: not stored)
     ScoreArgs a{};
     a.K = K;
@@ -197,21 +206,29 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.Z = Z;
     a.ld_out = ld_out;
     a.status = w.status;
-    const bool gram_tc = rkv::gram_tc_supported(a);
-    const bool imp_tc = rkv::importance_tc_supported(a);
-    a.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
-    cudaError_t e = timed(kKeyStats, s, [&] { return rkv::launch_key_stats(a, s); });
+    ScoreArgs b = a;  // what the stages after the key statistics read
+    if (pg) {
+        a.pg = *pg;
+        a.Kc = w.Kc;
+        b.K = w.Kc;
+        b.n_cap = n_cached;
+    }
+    const bool gram_tc = rkv::gram_tc_supported(b);
+    const bool imp_tc = rkv::importance_tc_supported(b);
+    a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
+    cudaError_t e = timed(pg ? kKeyStatsPaged : kKeyStats, s,
+                          [&] { return rkv::launch_key_stats(a, s); });
     if (e == cudaSuccess) {
         if (imp_tc)
-            e = timed(kImportanceTc, s, [&] { return rkv::launch_importance_tc(a, s); });
+            e = timed(kImportanceTc, s, [&] { return rkv::launch_importance_tc(b, s); });
         else
-            e = timed(kImportance, s, [&] { return rkv::launch_importance(a, s); });
+            e = timed(kImportance, s, [&] { return rkv::launch_importance(b, s); });
     }
     if (e == cudaSuccess) {
         if (gram_tc)
-            e = timed(kGramTc, s, [&] { return rkv::launch_gram_tc(a, s); });
+            e = timed(kGramTc, s, [&] { return rkv::launch_gram_tc(b, s); });
         else
-            e = timed(kGramSimt, s, [&] { return rkv::launch_gram_simt(a, s); });
+            e = timed(kGramSimt, s, [&] { return rkv::launch_gram_simt(b, s); });
     }
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
@@ -364,6 +381,145 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
                                           row_bytes, in_place, w.status, s);
             });
     }
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- paged --
+
+}  // extern "C"
+
+namespace {
+
+int log2_exact(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return (1 << l) == x ? l : -1;
+}
+
+int blocks_for(int rows, int bs) { return (rows + bs - 1) / bs; }
+
+// The contiguous descriptor of the same problems (capacity = the pool's rows
+// per sequence, only used for sizes) after the paged descriptor's checks.
+int check_paged_desc(const rkv_paged_desc* d, rkv_desc* flat) {
+    if (!d) return RKV_ERR_INVALID_ARG;
+    if (d->num_seqs < 0 || d->num_kv_heads < 1 || d->num_blocks < 1 ||
+        d->max_blocks_per_seq < 1)
+        return RKV_ERR_INVALID_ARG;
+    if (d->block_size < 1 || d->block_size > 1024 || log2_exact(d->block_size) < 0)
+        return RKV_ERR_INVALID_ARG;
+    if (d->num_seqs * (int64_t)d->num_kv_heads > ((int64_t)1 << 31)) return RKV_ERR_INVALID_ARG;
+    if ((int64_t)d->num_blocks * d->num_kv_heads * d->block_size > ((int64_t)1 << 40))
+        return RKV_ERR_INVALID_ARG;
+    flat->num_problems = d->num_seqs * d->num_kv_heads;
+    flat->gqa_group = d->gqa_group;
+    flat->head_dim = d->head_dim;
+    const int64_t cap = (int64_t)d->max_blocks_per_seq * d->block_size;
+    flat->n_capacity = (int32_t)(cap < RKV_MAX_TOKENS ? cap : RKV_MAX_TOKENS);
+    flat->dtype = d->dtype;
+    return check_desc(flat);
+}
+
+size_t kc_bytes_for(const rkv_desc& flat, int n_cached) {
+    return (size_t)flat.num_problems * n_cached * flat.head_dim * elem_size(flat.dtype);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs) {
+    rkv_desc flat{};
+    if (check_paged_desc(desc, &flat) != RKV_OK || n_cached < 1 || n_cached > flat.n_capacity ||
+        n_obs < 0)
+        return 0;
+    return carve(nullptr, flat.num_problems, n_cached, kc_bytes_for(flat, n_cached)).bytes;
+}
+
+int rkv_paged_freed_per_seq(const rkv_paged_desc* desc, int n_cached, int budget) {
+    rkv_desc flat{};
+    if (check_paged_desc(desc, &flat) != RKV_OK || n_cached < 1 || budget < 1 ||
+        n_cached > flat.n_capacity || budget > flat.n_capacity)
+        return -1;
+    if (n_cached <= budget) return 0;
+    return blocks_for(n_cached, desc->block_size) - blocks_for(budget, desc->block_size);
+}
+
+int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
+                       const void* Q_obs, int32_t* block_table, int n_cached, int budget,
+                       int n_obs, float lambda, int beta, float tau,
+                       const rkv_variant* variant, int32_t* out_idx, int32_t* out_freed,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    bool var_on = false;
+    int rc = check_variant(variant, &var_on);
+    if (rc) return rc;
+    rkv_desc flat{};
+    rc = check_paged_desc(desc, &flat);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t P = flat.num_problems;
+    if (n_cached < 1 || n_cached > flat.n_capacity || budget < 1 || budget > flat.n_capacity ||
+        n_obs < 1 || n_obs > budget || beta < 0)
+        return RKV_ERR_INVALID_ARG;
+    const size_t es = elem_size(flat.dtype);
+    const size_t pool_bytes =
+        (size_t)desc->num_blocks * desc->num_kv_heads * desc->block_size * desc->head_dim * es;
+    const int n_free = n_cached <= budget ? 0
+                                          : blocks_for(n_cached, desc->block_size) -
+                                                blocks_for(budget, desc->block_size);
+    if (P > 0) {
+        if (!K_pool || !V_pool || !Q_obs || !block_table || !out_idx) return RKV_ERR_INVALID_ARG;
+        if (n_free > 0 && !out_freed) return RKV_ERR_INVALID_ARG;
+        if (!aligned16(K_pool) || !aligned16(V_pool) || !aligned16(Q_obs))
+            return RKV_ERR_INVALID_ARG;
+        if (K_pool == V_pool || partial_overlap(K_pool, pool_bytes, V_pool, pool_bytes))
+            return RKV_ERR_ALIAS;
+    }
+    if (n_cached <= budget) {
+        // nothing to evict: the rows stay where they are
+        if (P == 0) return RKV_OK;
+        cudaError_t e = timed(kIdentity, s, [&] {
+            return rkv::launch_identity_idx(P, n_cached, budget, out_idx, s);
+        });
+        return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+    }
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return RKV_ERR_WORKSPACE;
+    if (n_cached < 2 || n_obs >= n_cached) return RKV_ERR_INVALID_ARG;
+    if (flat.gqa_group * n_obs > 128) return RKV_ERR_UNSUPPORTED;
+    if (rkv::compact_smem_bytes(n_cached, n_obs, budget) > kCompactSmemMax)
+        return RKV_ERR_UNSUPPORTED;
+    const size_t kc = kc_bytes_for(flat, n_cached);
+    if (workspace_bytes < carve(nullptr, P, n_cached, kc).bytes) return RKV_ERR_WORKSPACE;
+    if (P == 0) return RKV_OK;
+    const Workspace w = carve(workspace, P, n_cached, kc);
+    rkv::PagedIn pg;
+    pg.table = block_table;
+    pg.max_blocks = desc->max_blocks_per_seq;
+    pg.log2bs = log2_exact(desc->block_size);
+    pg.H = desc->num_kv_heads;
+    pg.num_blocks = desc->num_blocks;
+    rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
+                    var_on ? w.R : nullptr, w.Z, w.ld, w, s, &pg);
+    if (rc) return rc;
+    rkv::VariantIn vin;
+    if (var_on) {
+        vin.I = w.I;
+        vin.R = w.R;
+        vin.ld = w.ld;
+        vin.lambda = lambda;
+        vin.softmax = variant->redundancy_softmax;
+        vin.half = (variant->pool_window - 1) / 2;
+    }
+    const int row_bytes = desc->head_dim * (int)es;
+    cudaError_t e = timed(kCompactPaged, s, [&] {
+        return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.Kc,
+                                         K_pool, V_pool, pg, row_bytes, w.status, s, vin);
+    });
+    if (e == cudaSuccess && n_free > 0)
+        e = timed(kPagedRelease, s, [&] {
+            return rkv::launch_paged_release(desc->num_seqs, block_table, desc->max_blocks_per_seq,
+                                             blocks_for(budget, desc->block_size),
+                                             blocks_for(n_cached, desc->block_size), out_freed, s);
+        });
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 

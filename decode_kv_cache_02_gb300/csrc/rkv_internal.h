@@ -8,6 +8,17 @@ namespace rkv {
 
 struct DeviceStatus;
 
+// A paged pool [num_blocks, H, 1 << log2bs, d]: logical row r of problem
+// p = s * H + h lives in block table[s * max_blocks + (r >> log2bs)], head h,
+// row r & (bs - 1).  table == nullptr: the contiguous layout.
+struct PagedIn {
+    const int32_t* table = nullptr;
+    int max_blocks = 0;
+    int log2bs = 0;
+    int H = 1;
+    int num_blocks = 0;
+};
+
 // Everything the scoring kernels of one call need.
 struct ScoreArgs {
     const void* K;       // [P, n_cap, d]
@@ -28,6 +39,10 @@ struct ScoreArgs {
     float* Z;
     int64_t ld_out;
     DeviceStatus* status;
+    // paged input: key stats read K through pg and write the contiguous
+    // copy Kc [P, N, d], which the later stages read instead
+    PagedIn pg;
+    void* Kc = nullptr;
 };
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
@@ -66,6 +81,17 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
                            void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
                            cudaStream_t s, const VariantIn& var = VariantIn{});
+// The same on a paged pool, in place: kept K rows come from the contiguous
+// copy kc [P, N, d], kept V rows move inside v_pool; both land in the pool
+// rows of logical positions 0..budget-1.
+cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, int n_obs,
+                                 int budget, int32_t* idx, const void* kc, void* k_pool,
+                                 void* v_pool, const PagedIn& pg, int row_bytes, DeviceStatus* st,
+                                 cudaStream_t s, const VariantIn& var = VariantIn{});
+// Hands back each sequence's blocks past the kept ones: out_freed[s, j] =
+// table[s, nb_keep + j], then that entry = -1, for j < nb_old - nb_keep.
+cudaError_t launch_paged_release(int64_t S, int32_t* table, int max_blocks, int nb_keep,
+                                 int nb_old, int32_t* out_freed, cudaStream_t s);
 
 // Variant scores (redundancy softmax, importance pooling window) from the
 // base I and R rows (stride ld_in): Z, and I', R' when I_out / R_out are given

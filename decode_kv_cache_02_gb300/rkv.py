@@ -26,9 +26,10 @@ EXPORTED = [
     "rkv_workspace_size", "rkv_compress", "rkv_score", "rkv_select", "rkv_gather",
     "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
     "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
-    "rkv_score_ex",
+    "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
 ]
 RKV_MAX_POOL_WINDOW = 255
+RKV_ERR_DEVICE = 6
 RKV_ERR_TOO_LARGE = 7
 
 
@@ -46,6 +47,13 @@ class _Desc(ctypes.Structure):
 
 class _Variant(ctypes.Structure):
     _fields_ = [("redundancy_softmax", ctypes.c_int32), ("pool_window", ctypes.c_int32)]
+
+
+class _PagedDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("gqa_group", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -81,6 +89,14 @@ def load(path: str | None = None):
         lib.rkv_score_ex.argtypes = [dp, vp, vp, i32, i32, f32, i32, f32, vr, vp, vp, vp, vp, sz,
                                      vp]
         lib.rkv_score_ex.restype = i32
+        pdp = ctypes.POINTER(_PagedDesc)
+        lib.rkv_paged_workspace_size.argtypes = [pdp, i32, i32]
+        lib.rkv_paged_workspace_size.restype = sz
+        lib.rkv_paged_freed_per_seq.argtypes = [pdp, i32, i32]
+        lib.rkv_paged_freed_per_seq.restype = i32
+        lib.rkv_paged_compress.argtypes = [pdp, vp, vp, vp, vp, i32, i32, i32, f32, i32, f32, vr,
+                                           vp, vp, vp, sz, vp]
+        lib.rkv_paged_compress.restype = i32
         lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
         lib.rkv_select.restype = i32
         lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
@@ -334,3 +350,75 @@ def rkv_timing_read(reset: bool = True) -> dict:
     if k < 0:
         raise RkvError(-k, "rkv_timing_read")
     return {lib.rkv_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(min(k, n))}
+
+
+# ------------------------------------------------------------------ paged --
+
+def make_paged_desc(K_pool: torch.Tensor, block_table: torch.Tensor, gqa_group: int) -> _PagedDesc:
+    """Descriptor of a pool [num_blocks, H, block_size, d] and a block table
+    [num_seqs, max_blocks_per_seq] (int32)."""
+    if K_pool.dim() != 4:
+        raise ValueError("K_pool must be [num_blocks, H, block_size, head_dim]")
+    if block_table.dim() != 2 or block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32 [num_seqs, max_blocks_per_seq]")
+    nb, H, bs, d = K_pool.shape
+    S, mb = block_table.shape
+    return _PagedDesc(S, H, int(gqa_group), d, bs, nb, mb, _dtype_code(K_pool))
+
+
+def rkv_paged_workspace_size(K_pool, block_table, gqa_group: int, n_cached: int,
+                             n_obs: int) -> int:
+    desc = make_paged_desc(K_pool, block_table, gqa_group)
+    return int(load().rkv_paged_workspace_size(ctypes.byref(desc), int(n_cached), int(n_obs)))
+
+
+def rkv_paged_freed_per_seq(K_pool, block_table, n_cached: int, budget: int) -> int:
+    desc = make_paged_desc(K_pool, block_table, 1)
+    n = int(load().rkv_paged_freed_per_seq(ctypes.byref(desc), int(n_cached), int(budget)))
+    if n < 0:
+        raise ValueError("invalid paged request")
+    return n
+
+
+def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget: int,
+                       n_obs: int = 8, lam: float = 0.1, beta: int = 2, tau: float = 0.9,
+                       redundancy_softmax: bool = False, pool_window: int = 1, out_idx=None,
+                       out_freed=None, workspace=None, stream=None):
+    """One compression round of a paged cache, in place: K_pool, V_pool
+    [num_blocks, H, block_size, d], Q_obs [S*H, G, n_obs, d], block_table
+    [S, max_blocks] int32 (entries of freed blocks become -1).  Returns
+    (out_idx [S*H, budget], out_freed [S, n_free])."""
+    for t, n in ((K_pool, "K_pool"), (V_pool, "V_pool"), (Q_obs, "Q_obs"),
+                 (block_table, "block_table")):
+        _cuda(t, n)
+    if V_pool.shape != K_pool.shape or V_pool.dtype != K_pool.dtype or Q_obs.dtype != K_pool.dtype:
+        raise ValueError("K_pool, V_pool, Q_obs must share shape/dtype")
+    G = Q_obs.shape[1]
+    desc = make_paged_desc(K_pool, block_table, G)
+    P = desc.num_seqs * desc.num_kv_heads
+    if Q_obs.dim() != 4 or Q_obs.shape[0] != P or Q_obs.shape[2] != n_obs \
+            or Q_obs.shape[3] != K_pool.shape[3]:
+        raise ValueError("Q_obs must be [num_seqs * H, G, n_obs, d]")
+    n_free = rkv_paged_freed_per_seq(K_pool, block_table, n_cached, budget)
+    if out_idx is None:
+        out_idx = torch.empty((P, budget), dtype=torch.int32, device=K_pool.device)
+    if out_freed is None:
+        out_freed = torch.empty((desc.num_seqs, n_free), dtype=torch.int32, device=K_pool.device)
+    if workspace is None:
+        n = rkv_paged_workspace_size(K_pool, block_table, G, max(n_cached, 1), n_obs)
+        if n == 0:
+            raise ValueError("invalid workspace request")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=K_pool.device)
+    _cuda(out_idx, "out_idx")
+    _cuda(out_freed, "out_freed")
+    if out_idx.shape != (P, budget) or out_idx.dtype != torch.int32 \
+            or out_freed.shape != (desc.num_seqs, n_free) or out_freed.dtype != torch.int32:
+        raise ValueError("output shapes")
+    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
+    rc = load().rkv_paged_compress(
+        ctypes.byref(desc), K_pool.data_ptr(), V_pool.data_ptr(), Q_obs.data_ptr(),
+        block_table.data_ptr(), int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
+        float(tau), ctypes.byref(var), out_idx.data_ptr(), out_freed.data_ptr(),
+        workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _check(rc, "rkv_paged_compress")
+    return out_idx, out_freed

@@ -147,6 +147,62 @@ int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_c
                  float* out_I, float* out_R, float* out_Z,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- paged --
+ * The step on a paged KV cache.  The review (question 2, cause 4) names the
+ * clash between pruning and a block-structured (PagedAttention) cache as a
+ * main limitation: pruning re-lays the KV tensor out, and freeing the old
+ * cache to allocate a compressed one costs memory management.  Here a
+ * sequence's rows live in fixed-size blocks of a shared pool, compaction runs
+ * in place inside the sequence's own blocks, and the blocks it empties are
+ * handed back whole.
+ *
+ * Layout: K_pool, V_pool [num_blocks, num_kv_heads, block_size, head_dim]:
+ * one (block, head) is a contiguous block_size x head_dim tile.  Sequence s
+ * (one row of block_table [num_seqs, max_blocks_per_seq], int32) holds its
+ * logical row r of head h at block block_table[s][r / block_size], row
+ * r % block_size.  Problem p = s * num_kv_heads + h; Q_obs is
+ * [P, G, n_obs, head_dim] and out_idx [P, budget] as for rkv_compress.
+ * The entries 0 .. ceil(n_cached / block_size) - 1 of every table row must be
+ * distinct valid block ids, not shared between sequences; entries outside
+ * 0..num_blocks-1 are recorded as a device error and their rows skipped.
+ *
+ * Effect: for every problem the kept rows (out_idx) move to logical rows
+ * 0..budget-1 of the same sequence and head, in place; rows past budget in
+ * the last kept block are left as they were.  The blocks past the kept ones,
+ * entries ceil(budget/bs) .. ceil(n_cached/bs) - 1 of each row, are no longer
+ * used: their ids are written to out_freed [num_seqs, n_free] (n_free =
+ * rkv_paged_freed_per_seq()) and the table entries are set to -1.  Blocks not
+ * named by the first ceil(n_cached/bs) entries of any row are not touched. */
+typedef struct {
+    int64_t num_seqs;           /* S, rows of the block table (>= 0)         */
+    int32_t num_kv_heads;       /* H, heads per block; P = S * H problems     */
+    int32_t gqa_group;          /* G, query heads per KV head, 1..16          */
+    int32_t head_dim;           /* d, 64 or 128                               */
+    int32_t block_size;         /* rows per block, a power of two, 1..1024    */
+    int32_t num_blocks;         /* blocks in each pool (>= 1)                 */
+    int32_t max_blocks_per_seq; /* row stride of block_table (>= 1)           */
+    int32_t dtype;              /* RKV_DTYPE_BF16 or RKV_DTYPE_FP32           */
+} rkv_paged_desc;
+
+/* Workspace bytes rkv_paged_compress needs (0 if the arguments are invalid):
+ * the scratch of rkv_compress plus one contiguous copy of the P problems'
+ * keys [P, n_cached, head_dim]. */
+size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs);
+
+/* Blocks freed per sequence: ceil(n_cached/bs) - ceil(budget/bs), or 0 when
+ * n_cached <= budget; -1 if the arguments are invalid. */
+int rkv_paged_freed_per_seq(const rkv_paged_desc* desc, int n_cached, int budget);
+
+/* One compression round on the paged cache (see above).  n_cached <= budget:
+ * out_idx is the identity and nothing moves or is freed.  Problems whose
+ * scores, keys and kept indices exceed the fused selection kernel's shared
+ * memory (8*(n_cached-n_obs) + 4*budget > 160 KB) return RKV_ERR_UNSUPPORTED. */
+int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
+                       const void* Q_obs, int32_t* block_table, int n_cached, int budget,
+                       int n_obs, float lambda, int beta, float tau,
+                       const rkv_variant* variant, int32_t* out_idx, int32_t* out_freed,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* The selection alone: for scores Z [P, n] (fp32), out_idx [P, budget] as
  * rkv_compress would produce it (top budget-n_obs of the candidates
  * 0..n-n_obs-1 by Z, ties to the larger index, then the n_obs observation

@@ -217,3 +217,68 @@ def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
             sc = variant(sc, n_obs, lam, redundancy_softmax, pool_window)
         idx = select(sc["Z"], n_obs, budget)
     return {"idx": idx, "scores": sc}
+
+
+# ------------------------------------------------------------------ paged --
+# Question 2, cause 4 of the review: a block-structured (PagedAttention) cache
+# and pruning clash.  The paged round is the plain round on the rows read
+# through the block table, with the kept rows written back through it and the
+# emptied blocks listed.
+
+
+def paged_rows(pool: np.ndarray, table: np.ndarray, n_rows: int) -> np.ndarray:
+    """Logical rows [S*H, n_rows, ...] of pool [num_blocks, H, bs, ...] read
+    through table [S, max_blocks]: problem s*H + h, row r is
+    pool[table[s, r // bs], h, r % bs]."""
+    pool = np.asarray(pool)
+    table = np.asarray(table)
+    H, bs = pool.shape[1], pool.shape[2]
+    S = table.shape[0]
+    r = np.arange(n_rows)
+    out = np.empty((S * H, n_rows) + pool.shape[3:], dtype=pool.dtype)
+    for s_ in range(S):
+        blk = table[s_, r // bs]
+        for h in range(H):
+            out[s_ * H + h] = pool[blk, h, r % bs]
+    return out
+
+
+def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: int,
+                   lam: float, beta: int, tau: float, idx_used=None, nthreads=None,
+                   redundancy_softmax: bool = False, pool_window: int = 1) -> dict:
+    """One paged compression round.  K_pool / V_pool: raw arrays [num_blocks,
+    H, bs, d] (any element type; rows move as they are); the keys are scored
+    from ``K_f64`` = the float values of K_pool's logical rows.  Returns
+    dict(idx, scores, K_pool, V_pool, table, freed): the oracle's kept set and
+    the expected state after the round, with the rows moved by ``idx_used``
+    (default: the oracle's own kept set; a GPU test passes the GPU's, so that
+    exact score ties cannot change which rows are compared)."""
+    K_pool = np.asarray(K_pool)
+    V_pool = np.asarray(V_pool)
+    table = np.asarray(table, dtype=np.int32)
+    H, bs = K_pool.shape[1], K_pool.shape[2]
+    S = table.shape[0]
+    K_f = paged_rows(K_pool, table, n_cached)
+    if K_f.dtype == np.int16:  # bf16 bit patterns: widen exactly to float
+        K_f = (K_f.astype(np.int32) << 16).view(np.float32)
+    res = compress(K_f, Q, n_cached, budget, n_obs, lam, beta, tau, nthreads,
+                   redundancy_softmax, pool_window)
+    idx = res["idx"] if idx_used is None else np.asarray(idx_used)
+    Kp, Vp, new_table = K_pool.copy(), V_pool.copy(), table.copy()
+    freed = np.zeros((S, 0), dtype=np.int32)
+    if n_cached > budget:
+        K_log = paged_rows(K_pool, table, n_cached)
+        V_log = paged_rows(V_pool, table, n_cached)
+        for s_ in range(S):
+            for h in range(H):
+                p = s_ * H + h
+                for r in range(budget):
+                    blk = table[s_, r // bs]
+                    Kp[blk, h, r % bs] = K_log[p, idx[p, r]]
+                    Vp[blk, h, r % bs] = V_log[p, idx[p, r]]
+        nb_keep = -(-budget // bs)
+        nb_old = -(-n_cached // bs)
+        freed = table[:, nb_keep:nb_old].copy()
+        new_table[:, nb_keep:nb_old] = -1
+    return {"idx": res["idx"], "scores": res["scores"], "K_pool": Kp, "V_pool": Vp,
+            "table": new_table, "freed": freed}

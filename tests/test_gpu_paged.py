@@ -1,0 +1,138 @@
+"""GPU parity of the paged round (rkv_paged_compress) against the oracle's
+paged round: kept sets, the pools after the in-place compaction (byte for
+byte, including every row that must stay untouched), the block table and the
+freed block ids."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_kv_cache_02_gb300 import rkv, workloads as wl
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _raw(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    return (t.view(torch.int16) if t.dtype == torch.bfloat16 else t).numpy()
+
+
+def _make_paged(w, bs, extra=5, seed=0, tail_garbage=True):
+    """The workload's logical K, V, Q scattered into pools through a shuffled
+    block table.  Rows past N in the last block hold large values, unused
+    blocks a sentinel, and the table's entries past the blocks in use ids
+    that do not exist (none of these may be read)."""
+    K, V, Q = wl.make_inputs(w, device=DEV)
+    S, H = w.layers * w.batch, w.kv_heads
+    N, d = w.n_cached, w.head_dim
+    nb = -(-N // bs)
+    num_blocks = S * nb + extra
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_blocks, generator=g)
+    mb = nb + 2
+    table = torch.full((S, mb), 1 << 30, dtype=torch.int32)
+    table[:, :nb] = perm[:S * nb].reshape(S, nb).to(torch.int32)
+    K_pool = torch.full((num_blocks, H, bs, d), -7.5, dtype=K.dtype, device=DEV)
+    V_pool = torch.full_like(K_pool, 3.25)
+    Kl = K[:, :N].reshape(S, H, N, d)
+    Vl = V[:, :N].reshape(S, H, N, d)
+    pad = nb * bs - N
+    if pad:
+        fill = 1e4 if tail_garbage else 0.0
+        Kl = torch.cat([Kl, torch.full((S, H, pad, d), fill, dtype=K.dtype, device=DEV)], 2)
+        Vl = torch.cat([Vl, torch.full((S, H, pad, d), fill, dtype=K.dtype, device=DEV)], 2)
+    blocks = table[:, :nb].long().to(DEV)
+    K_pool[blocks] = Kl.reshape(S, H, nb, bs, d).permute(0, 2, 1, 3, 4)
+    V_pool[blocks] = Vl.reshape(S, H, nb, bs, d).permute(0, 2, 1, 3, 4)
+    return K_pool, V_pool, Q, table.to(DEV)
+
+
+def _paged_check(w, bs, problems=None, softmax=False, window=1, **kw):
+    K_pool, V_pool, Q, table = _make_paged(w, bs, **kw)
+    K0, V0, T0 = _raw(K_pool), _raw(V_pool), table.cpu().numpy()
+    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+    idx, freed = rkv.rkv_paged_compress(K_pool, V_pool, Q, table, w.n_cached, w.budget, w.n_obs,
+                                        w.lam, w.beta, w.tau, redundancy_softmax=softmax,
+                                        pool_window=window, workspace=ws)
+    assert rkv.rkv_get_device_status(ws) == 0
+    gi = idx.cpu().numpy()
+    P = gi.shape[0]
+    problems = list(range(P)) if problems is None else problems
+    if w.n_cached <= w.budget:
+        assert np.all(gi[:, :w.n_cached] == np.arange(w.n_cached))
+        np.testing.assert_array_equal(_raw(K_pool), K0)
+        np.testing.assert_array_equal(table.cpu().numpy(), T0)
+        return
+    parity.check_idx_valid(gi, w.n_cached, w.budget, w.n_obs)
+    exp = oracle.paged_compress(K0, V0, Q.cpu(), T0, w.n_cached, w.budget, w.n_obs, w.lam,
+                                w.beta, w.tau, idx_used=gi, redundancy_softmax=softmax,
+                                pool_window=window)
+    sc = exp["scores"]
+    sub = {k: sc[k][problems] for k in ("Z", "border")}
+    band = parity.scaled_band(sub, w.n_cached - w.n_obs) if softmax else parity.KEPT_BAND
+    bad, excused = parity.kept_mismatches(gi[problems], sub, w.budget, w.n_obs, band=band)
+    assert bad == 0, f"{bad} kept-set mismatches outside the tie band ({excused} excused)"
+    np.testing.assert_array_equal(_raw(K_pool), exp["K_pool"])
+    np.testing.assert_array_equal(_raw(V_pool), exp["V_pool"])
+    np.testing.assert_array_equal(table.cpu().numpy(), exp["table"])
+    np.testing.assert_array_equal(freed.cpu().numpy(), exp["freed"])
+    return excused
+
+
+def test_paged_llama_shapes_block16():
+    """Llama-shaped problems (d = 128, G = 4, bf16), ragged N, 16-row blocks."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=301, budget=200, layers=1, batch=3,
+                                           kv_heads=2)
+    _paged_check(w, 16)
+
+
+def test_paged_full_row_block16():
+    """A whole Llama row (N = 1152 -> 1024) for 2 sequences x 8 heads: eight
+    16-row blocks freed per sequence."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(layers=1, batch=2, kv_heads=8)
+    _paged_check(w, 16, problems=[0, 5, 9, 15])
+
+
+@pytest.mark.parametrize("bs", [1, 64, 128, 1024])
+def test_paged_block_sizes(bs):
+    """One row per block up to one block per sequence (nothing freed)."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=301, budget=200, layers=1, batch=2,
+                                           kv_heads=2, head_dim=64)
+    _paged_check(w, bs)
+
+
+def test_paged_fp32_cuda_core_path():
+    """fp32 keys take the CUDA-core importance and Gram on the contiguous copy."""
+    w = wl.BY_NAME["tiny"].scaled(batch=2)
+    _paged_check(w, 32)
+
+
+def test_paged_with_variant():
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=640, budget=512, layers=1, batch=2,
+                                           kv_heads=2)
+    _paged_check(w, 64, softmax=True, window=5)
+
+
+def test_paged_identity_when_not_over_budget():
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=1000, budget=1024, layers=1, batch=2,
+                                           kv_heads=2)
+    _paged_check(w, 16)
+
+
+def test_paged_bad_block_id_is_reported():
+    """A table entry naming no block is caught by the kernels' own checks:
+    its rows are skipped and the device status reports it."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=301, budget=200, layers=1, batch=2,
+                                           kv_heads=2, head_dim=64)
+    K_pool, V_pool, Q, table = _make_paged(w, 16)
+    table[1, 3] = K_pool.shape[0] + 11
+    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+    rkv.rkv_paged_compress(K_pool, V_pool, Q, table, w.n_cached, w.budget, w.n_obs,
+                           workspace=ws)
+    assert rkv.rkv_get_device_status(ws) == rkv.RKV_ERR_DEVICE
+    assert rkv.rkv_get_device_status(ws) == 0  # read and cleared

@@ -110,6 +110,39 @@ def test_variant_argument_errors(lib):
                                fake + 2 ** 34, fake + 2 ** 35, 10, None) == 3
 
 
+def test_paged_sizes_and_argument_errors(lib):
+    """Paged descriptor checks, freed-block counts and workspace sizes are
+    answered on the host; invalid calls enqueue nothing."""
+    from decode_kv_cache_02_gb300 import rkv
+    D = lambda **kw: rkv._PagedDesc(kw.get("S", 4), kw.get("H", 8), kw.get("G", 4),
+                                    kw.get("d", 128), kw.get("bs", 16), kw.get("nb", 400),
+                                    kw.get("mb", 80), kw.get("dtype", 0))
+    d = D()
+    assert lib.rkv_paged_freed_per_seq(ctypes.byref(d), 1152, 1024) == 72 - 64
+    assert lib.rkv_paged_freed_per_seq(ctypes.byref(d), 1000, 1024) == 0
+    assert lib.rkv_paged_freed_per_seq(ctypes.byref(d), 1153, 1024) == 73 - 64
+    assert lib.rkv_paged_freed_per_seq(ctypes.byref(D(bs=12)), 1152, 1024) == -1  # not 2^k
+    assert lib.rkv_paged_freed_per_seq(ctypes.byref(D(mb=10)), 1152, 1024) == -1  # > capacity
+    flat = lib.rkv_workspace_size(ctypes.byref(_desc(P=32, n_cap=1152)), 1152, 8)
+    assert lib.rkv_paged_workspace_size(ctypes.byref(d), 1152, 8) == \
+        flat + (32 * 1152 * 128 * 2 + 255) // 256 * 256
+    assert lib.rkv_paged_workspace_size(ctypes.byref(D(bs=0)), 1152, 8) == 0
+    fake = 1 << 20
+    v = rkv._Variant(0, 1)
+    call = lambda desc, n=1152, budget=1024, K=fake, V=fake + 2 ** 36, ws_bytes=1 << 40: \
+        lib.rkv_paged_compress(ctypes.byref(desc), K, V, fake + 2 ** 37, fake + 2 ** 38, n,
+                               budget, 8, 0.1, 2, 0.9, ctypes.byref(v), fake + 2 ** 39,
+                               fake + 2 ** 40, fake + 2 ** 41, ws_bytes, None)
+    assert call(D(bs=3)) == 1                      # block size not a power of two
+    assert call(D(bs=2048)) == 1                   # block size too large
+    assert call(D(mb=70)) == 1                     # n_cached beyond the table's rows
+    assert call(D(d=80)) == 2                      # unsupported head_dim
+    assert call(D(), K=fake + 8) == 1              # misaligned pool
+    assert call(D(), V=fake) == 4                  # K and V pools are the same memory
+    assert call(D(), ws_bytes=10) == 3             # workspace too small
+    assert call(D(mb=2000), n=30000, budget=2048) == 2  # beyond the fused kernel's shared memory
+
+
 def test_binding_rejects_cpu_tensors(lib):
     from decode_kv_cache_02_gb300 import rkv
     K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)

@@ -387,6 +387,88 @@ def test_variant_off_is_identity_and_softmax_keeps_redundancy_order():
     np.testing.assert_array_equal(res["idx"], oracle.select(sc["Z"], wk.n_obs, wk.budget))
 
 
+# ------------------------------------------------------------------ paged --
+# Question 2, cause 4 of the review: the paged round is the plain round read
+# and written through a block table, with the emptied blocks handed back.
+
+def _paged_case(S=3, H=2, bs=8, N=45, budget=30, d=16, extra=5, seed=0):
+    rng = np.random.default_rng(seed)
+    nb = -(-N // bs)
+    num_blocks = S * nb + extra
+    perm = rng.permutation(num_blocks)
+    table = perm[:S * nb].reshape(S, nb).astype(np.int32)
+    K_pool = rng.standard_normal((num_blocks, H, bs, d)).astype(np.float32)
+    V_pool = rng.standard_normal((num_blocks, H, bs, d)).astype(np.float32)
+    Q = rng.standard_normal((S * H, 2, 4, d))
+    return K_pool, V_pool, Q, table, perm
+
+
+def test_paged_rows_follow_the_table():
+    """With the table naming consecutive blocks, the logical rows are the
+    pool with the head and block axes swapped (a torch permute, not the
+    oracle's loop)."""
+    S, H, bs, nb, d = 2, 3, 4, 5, 6
+    pool = np.random.default_rng(1).standard_normal((S * nb, H, bs, d))
+    table = np.arange(S * nb, dtype=np.int32).reshape(S, nb)
+    ref = torch.from_numpy(pool).reshape(S, nb, H, bs, d).permute(0, 2, 1, 3, 4)
+    ref = ref.reshape(S * H, nb * bs, d).numpy()
+    np.testing.assert_array_equal(oracle.paged_rows(pool, table, nb * bs), ref)
+    np.testing.assert_array_equal(oracle.paged_rows(pool, table, 7), ref[:, :7])
+
+
+def test_paged_round_equals_contiguous_round():
+    """Kept sets equal the contiguous round on the same logical rows; every
+    kept row lands at its logical position; blocks no table names, rows past
+    the budget in the last kept block and the freed blocks' data are left as
+    they were; the freed ids are the table's tail, ceil(N/bs) - ceil(B/bs)
+    per sequence, and their entries become -1."""
+    K_pool, V_pool, Q, table, perm = _paged_case()
+    S, H, bs, N, B, n_obs = 3, 2, 8, 45, 30, 4
+    out = oracle.paged_compress(K_pool, V_pool, Q, table, N, B, n_obs, 0.1, 2, 0.6)
+    K_log = oracle.paged_rows(K_pool, table, N)
+    V_log = oracle.paged_rows(V_pool, table, N)
+    ref = oracle.compress(K_log, Q, N, B, n_obs, 0.1, 2, 0.6)
+    np.testing.assert_array_equal(out["idx"], ref["idx"])
+    new_K = oracle.paged_rows(out["K_pool"], table, B)
+    new_V = oracle.paged_rows(out["V_pool"], table, B)
+    np.testing.assert_array_equal(new_K, oracle.gather(K_log, ref["idx"])[:, :B])
+    np.testing.assert_array_equal(new_V, oracle.gather(V_log, ref["idx"])[:, :B])
+    nb_keep, nb_old = -(-B // bs), -(-N // bs)
+    assert out["freed"].shape == (S, nb_old - nb_keep) == (S, 2)
+    np.testing.assert_array_equal(out["freed"], table[:, nb_keep:nb_old])
+    assert np.all(out["table"][:, nb_keep:nb_old] == -1)
+    np.testing.assert_array_equal(out["table"][:, :nb_keep], table[:, :nb_keep])
+    untouched = sorted(set(range(K_pool.shape[0])) - set(table[:, :nb_keep].ravel().tolist()))
+    np.testing.assert_array_equal(out["K_pool"][untouched], K_pool[untouched])
+    np.testing.assert_array_equal(out["V_pool"][untouched], V_pool[untouched])
+    last = table[:, nb_keep - 1]
+    np.testing.assert_array_equal(out["K_pool"][last, :, B % bs:], K_pool[last, :, B % bs:])
+
+
+def test_paged_round_ignores_physical_placement():
+    """Renumbering the physical blocks (pool and table together) changes
+    nothing but the placement."""
+    K_pool, V_pool, Q, table, _ = _paged_case(seed=2)
+    N, B, n_obs = 45, 30, 4
+    a = oracle.paged_compress(K_pool, V_pool, Q, table, N, B, n_obs, 0.1, 2, 0.6)
+    ren = np.random.default_rng(3).permutation(K_pool.shape[0])
+    K2, V2 = np.empty_like(K_pool), np.empty_like(V_pool)
+    K2[ren], V2[ren] = K_pool, V_pool
+    b = oracle.paged_compress(K2, V2, Q, ren[table].astype(np.int32), N, B, n_obs, 0.1, 2, 0.6)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_array_equal(b["K_pool"][ren], a["K_pool"])
+    np.testing.assert_array_equal(b["V_pool"][ren], a["V_pool"])
+    np.testing.assert_array_equal(b["freed"], ren[a["freed"]])
+
+
+def test_paged_round_identity_when_not_over_budget():
+    K_pool, V_pool, Q, table, _ = _paged_case(N=45, budget=48)
+    out = oracle.paged_compress(K_pool, V_pool, Q, table, 45, 48, 4, 0.1, 2, 0.6)
+    np.testing.assert_array_equal(out["K_pool"], K_pool)
+    np.testing.assert_array_equal(out["table"], table)
+    assert out["freed"].shape[1] == 0
+
+
 # ------------------------------------------------------------- invariants --
 
 def test_compress_invariants_tiny_and_identity():
