@@ -292,13 +292,26 @@ def _config(w, **extra):
     return c
 
 
-def _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, softmax=False, window=1):
+def _sentences(args, w, dev):
+    """Synthetic sentence inputs at the workload's size (model width of the
+    Llama-8B configuration), or None without --sentences."""
+    if not args.sentences:
+        return None
+    si = wl.make_sentences(w.batch, w.kv_heads, w.layers, w.n_cached, wl.HIDDEN_LLAMA8B,
+                           device=dev)
+    reps = rkv.rkv_sentence_reps(si.hidden, si.token_seg, si.max_sentences)
+    return rkv.Sentences(reps, si.count, si.seg_id, si.heads, wl.SENT_TAU)
+
+
+def _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, softmax=False, window=1,
+             sentences=None):
     """One compression step of workload `w` (with a scoring variant if asked)."""
-    if softmax or window != 1:
+    if softmax or window != 1 or sentences is not None:
         def step():
             rkv.rkv_compress_ex(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
-                                redundancy_softmax=softmax, pool_window=window, out_K=out_K,
-                                out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
+                                redundancy_softmax=softmax, pool_window=window,
+                                sentences=sentences, out_K=out_K, out_V=out_V, out_idx=idx,
+                                workspace=ws, stream=stream)
     else:
         def step():
             rkv.rkv_compress(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
@@ -408,17 +421,21 @@ def run_paged(args, w):
     ws = torch.zeros(rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, N, w.n_obs),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    sent = _sentences(args, w, dev)
+    seg0 = sent.seg_id.clone() if sent is not None else None
 
     def restore():
         K_pool.copy_(K0)
         V_pool.copy_(V0)
         table.copy_(table0)
+        if sent is not None:
+            sent.seg_id.copy_(seg0)
 
     def step():
         rkv.rkv_paged_compress(K_pool, V_pool, Q, table, N, w.budget, w.n_obs, w.lam, w.beta,
                                w.tau, redundancy_softmax=args.redundancy_softmax,
-                               pool_window=args.pool_window, out_idx=idx, out_freed=freed,
-                               workspace=ws, stream=stream)
+                               pool_window=args.pool_window, sentences=sent, out_idx=idx,
+                               out_freed=freed, workspace=ws, stream=stream)
 
     for _ in range(max(3, args.warmup)):
         restore()
@@ -475,7 +492,8 @@ def run_paged(args, w):
         "config": _config(w, block_size=bs, num_seqs=S, num_blocks=num_blocks,
                           blocks_freed_per_seq=n_free, moved_rows_per_problem=moved_rows / P,
                           variant={"redundancy_softmax": args.redundancy_softmax,
-                                   "pool_window": args.pool_window},
+                                   "pool_window": args.pool_window,
+                                   "sentences": sent is not None},
                           l2="pools restored between rounds (9.7 GB copy, flushes L2)"),
         "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
         "roofline_all": roof,
@@ -499,8 +517,9 @@ def run_ours(args, w):
     idx = torch.empty((w.problems, w.budget), dtype=torch.int32, device=dev)
     ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
     stream = torch.cuda.current_stream()
+    sent = _sentences(args, w, dev)
     step = _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, args.redundancy_softmax,
-                    args.pool_window)
+                    args.pool_window, sent)
     elapsed, kernels, clock_summary = _time_steps(step, args.steps, args.warmup, ws, stream,
                                                   local, world)
     launches = sum(v["launches"] for v in kernels.values())
@@ -523,9 +542,13 @@ def run_ours(args, w):
         "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
         "clocks": clock_summary,
     }
-    if args.redundancy_softmax or args.pool_window != 1:
+    if args.redundancy_softmax or args.pool_window != 1 or sent is not None:
         line["config"]["variant"] = {"redundancy_softmax": args.redundancy_softmax,
                                      "pool_window": args.pool_window}
+        if sent is not None:
+            line["config"]["variant"]["sentences"] = {
+                "sequences": sent.reps.shape[0], "max_sentences": sent.reps.shape[1],
+                "hidden": sent.reps.shape[2], "tau": sent.tau}
     line["roofline"] = roofline(kernels, model, peaks, args.steps, w)
     # all kernels' fractions, for the record
     line["roofline_all"] = {}
@@ -542,7 +565,7 @@ def run_ours(args, w):
         line["roofline_all"][k] = entry
 
     if not args.no_e2e:
-        line["e2e"] = e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world)
+        line["e2e"] = e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w, K, Q, seconds=args.cpu_seconds)
     if rank == 0:
@@ -552,7 +575,7 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
-def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world):
+def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent=None):
     """Same step through the public API with host buffers: every step copies
     K, V, Q_obs in from pinned host memory and the compacted K, V (the kept
     rows) and idx out.  Steps are pipelined over two device buffer sets: the
@@ -593,8 +616,8 @@ def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world):
             stream.wait_event(done_d2h[sl])  # slot's outputs copied out
         rkv.rkv_compress_ex(dK, dV, dQ, w.n_cached, B, w.n_obs, w.lam, w.beta, w.tau,
                             redundancy_softmax=args.redundancy_softmax,
-                            pool_window=args.pool_window, out_K=dOK, out_V=dOV, out_idx=dI,
-                            workspace=ws, stream=stream)
+                            pool_window=args.pool_window, sentences=sent, out_K=dOK, out_V=dOV,
+                            out_idx=dI, workspace=ws, stream=stream)
         e_c = ev()
         e_c.record(stream)
         done_compute[sl] = e_c
@@ -722,6 +745,8 @@ def main():
     ap.add_argument("--paged", action="store_true",
                     help="time the step on a paged cache (block pools + block table)")
     ap.add_argument("--block-size", type=int, default=16, help="rows per block with --paged")
+    ap.add_argument("--sentences", action="store_true",
+                    help="scoring variant: sentence-level penalty on synthetic sentences")
     ap.add_argument("--sweep", action="store_true",
                     help="time the step over a lambda/beta/tau/variant sweep, one line each")
     args = ap.parse_args()

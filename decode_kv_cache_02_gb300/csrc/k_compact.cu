@@ -144,17 +144,25 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
         // replaced by its own Z key)
         float* sI = reinterpret_cast<float*>(list);
         float* sR = reinterpret_cast<float*>(keys);
+        float* sP = reinterpret_cast<float*>(sidx + budget);  // [C] with sentences
+#pragma unroll 4
         for (int i = tid; i < C; i += kThreads) {
             sI[i] = var.I[p * var.ld + i];
             sR[i] = var.R[p * var.ld + i];
+        }
+        if (var.pen != nullptr) {
+            // each candidate's sentence penalty, loads of several rows in flight
+#pragma unroll 4
+            for (int i = tid; i < C; i += kThreads) sP[i] = row_penalty(var, p, i);
         }
         __syncthreads();
         SoftmaxStats sm{0.f, 1.f};
         if (var.softmax) sm = softmax_stats<kThreads>(sR, C, s_red[0]);
         for (int i = tid; i < C; i += kThreads) {
             const float r = sR[i];
-            const float z = variant_z(var.lambda, pooled_importance(sI, i, C, var.half),
-                                      var.softmax ? softmax_term(r, sm) : r);
+            const float z = __fsub_rn(variant_z(var.lambda, pooled_importance(sI, i, C, var.half),
+                                                var.softmax ? softmax_term(r, sm) : r),
+                                      var.pen != nullptr ? sP[i] : 0.f);
             keys[i] = orderable(z);
             zmin = fminf(zmin, z);
             zmax = fmaxf(zmax, z);
@@ -293,6 +301,19 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
     __syncthreads();
     int32_t* out = idx + p * (int64_t)budget;
     for (int r = tid; r < budget; r += kThreads) out[r] = sidx[r];
+    if (var.seg != nullptr) {
+        // the kept rows' sentence ids follow them (the cache-range mapping),
+        // in place in ascending chunks: sidx[r] >= r, so a chunk's sources
+        // lie at or after the chunk and are read before it is written
+        int32_t* sg = var.seg + p * var.ld_seg;
+        for (int c0 = 0; c0 < budget; c0 += kThreads) {
+            const int r = c0 + tid;
+            const int32_t v = r < budget ? sg[sidx[r]] : 0;
+            __syncthreads();
+            if (r < budget) sg[r] = v;
+            __syncthreads();
+        }
+    }
 
     // ------------------------------------------------------------ copy --
     if constexpr (kPaged) {
@@ -411,9 +432,11 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
 
 }  // namespace
 
-size_t compact_smem_bytes(int N, int n_obs, int budget) {
+size_t compact_smem_bytes(int N, int n_obs, int budget, bool sentences) {
     const int C = N - n_obs;
-    return sizeof(uint32_t) * (size_t)(2 * (C > 0 ? C : 1)) + sizeof(int32_t) * (size_t)budget;
+    const size_t c = (size_t)(C > 0 ? C : 1);
+    return sizeof(uint32_t) * 2 * c + sizeof(int32_t) * (size_t)budget +
+           (sentences ? sizeof(float) * c : 0);
 }
 
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
@@ -421,7 +444,7 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
                            void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
                            cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
-    const size_t smem = compact_smem_bytes(N, n_obs, budget);
+    const size_t smem = compact_smem_bytes(N, n_obs, budget, var.pen != nullptr);
     cudaError_t e = cudaFuncSetAttribute(compact_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -437,7 +460,7 @@ cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, 
                                  void* v_pool, const PagedIn& pg, int row_bytes, DeviceStatus* st,
                                  cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
-    const size_t smem = compact_smem_bytes(N, n_obs, budget);
+    const size_t smem = compact_smem_bytes(N, n_obs, budget, var.pen != nullptr);
     cudaError_t e = cudaFuncSetAttribute(compact_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -11,7 +11,8 @@
 //   R'_i = exp(R_i - m) / sum_{j<C} exp(R_j - m),  m = max_{j<C} R_j
 //          (the softmax; subtracting m changes nothing but the range)
 //   I'_i = max { I_j : j < C, |j - i| <= h }
-//   Z_i  = lambda*I'_i - (1-lambda)*R'_i          for i < C
+//   Z_i  = lambda*I'_i - (1-lambda)*R'_i - pen_i   for i < C
+//          (pen_i: the sentence penalty of row i's sentence, see k_sentence.cu)
 // Observation tokens (i >= C) keep their I, get R = 0 and Z = +inf.
 //
 // One CTA per problem: a block maximum and a block sum over the candidates'
@@ -31,23 +32,22 @@ constexpr int kThreads = 256;
 // I_out and R_out may be null.  R_out may equal R (each thread rewrites only
 // the rows it read after both reductions); I_out must not overlap I.
 __global__ void __launch_bounds__(kThreads)
-variant_kernel(const float* __restrict__ I, const float* R, int64_t ld_in, float* __restrict__ Z,
-               float* __restrict__ I_out, float* R_out, int64_t ld_out, int N, int n_obs,
-               float lambda, int softmax, int half) {
+variant_kernel(VariantIn v, float* __restrict__ Z, float* __restrict__ I_out, float* R_out,
+               int64_t ld_out, int N, int n_obs) {
     __shared__ float s_red[kThreads / 32];
     const int64_t p = blockIdx.x;
     const int C = N - n_obs;
-    const float* Ip = I + p * ld_in;
-    const float* Rp = R + p * ld_in;
+    const float* Ip = v.I + p * v.ld;
+    const float* Rp = v.R + p * v.ld;
     SoftmaxStats st{0.f, 1.f};
-    if (softmax) st = softmax_stats<kThreads>(Rp, C, s_red);
+    if (v.softmax) st = softmax_stats<kThreads>(Rp, C, s_red);
     for (int i = threadIdx.x; i < N; i += kThreads) {
         const int64_t o = p * ld_out + i;
         if (i < C) {
-            const float ip = pooled_importance(Ip, i, C, half);
+            const float ip = pooled_importance(Ip, i, C, v.half);
             const float r = Rp[i];
-            const float rs = softmax ? softmax_term(r, st) : r;
-            Z[o] = variant_z(lambda, ip, rs);
+            const float rs = v.softmax ? softmax_term(r, st) : r;
+            Z[o] = variant_score(v, p, i, ip, rs);
             if (I_out) I_out[o] = ip;
             if (R_out) R_out[o] = rs;
         } else {
@@ -60,12 +60,10 @@ variant_kernel(const float* __restrict__ I, const float* R, int64_t ld_in, float
 
 }  // namespace
 
-cudaError_t launch_variant(int64_t P, int N, int n_obs, float lambda, int softmax, int window,
-                           const float* I, const float* R, int64_t ld_in, float* Z, float* I_out,
-                           float* R_out, int64_t ld_out, cudaStream_t s) {
+cudaError_t launch_variant(int64_t P, int N, int n_obs, const VariantIn& v, float* Z,
+                           float* I_out, float* R_out, int64_t ld_out, cudaStream_t s) {
     if (P == 0) return cudaSuccess;
-    variant_kernel<<<(unsigned)P, kThreads, 0, s>>>(I, R, ld_in, Z, I_out, R_out, ld_out, N, n_obs,
-                                                     lambda, softmax, (window - 1) / 2);
+    variant_kernel<<<(unsigned)P, kThreads, 0, s>>>(v, Z, I_out, R_out, ld_out, N, n_obs);
     return cudaGetLastError();
 }
 

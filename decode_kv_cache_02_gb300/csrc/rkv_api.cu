@@ -39,11 +39,14 @@ enum KernelId {
     kKeyStatsPaged,
     kCompactPaged,
     kPagedRelease,
+    kSentencePenalty,
+    kSentenceReps,
     kNumKernels
 };
 const char* const kKernelNames[kNumKernels] = {
     "key_stats", "importance", "importance_tc", "gram_tc", "gram_simt", "select", "gather",
-    "identity_idx", "compact", "variant", "key_stats_paged", "compact_paged", "paged_release"};
+    "identity_idx", "compact", "variant", "key_stats_paged", "compact_paged", "paged_release",
+    "sentence_penalty", "sentence_reps"};
 
 // ---------------------------------------------------------------- timing --
 struct TimedLaunch {
@@ -158,8 +161,22 @@ int check_variant(const rkv_variant* v, bool* active) {
     if (v->redundancy_softmax != 0 && v->redundancy_softmax != 1) return RKV_ERR_INVALID_ARG;
     if (v->pool_window < 1 || v->pool_window > RKV_MAX_POOL_WINDOW || (v->pool_window & 1) == 0)
         return RKV_ERR_INVALID_ARG;
-    *active = v->redundancy_softmax != 0 || v->pool_window > 1;
+    if (const rkv_sentences* t = v->sentences) {
+        if (!t->reps || !t->count || !t->seg_id || !t->penalty || !aligned16(t->reps))
+            return RKV_ERR_INVALID_ARG;
+        if (t->num_seqs < 1 || t->heads < 1 || t->max_sentences < 1 ||
+            t->max_sentences > RKV_MAX_SENTENCES || t->hidden_dim < 4 ||
+            t->hidden_dim > RKV_MAX_HIDDEN || (t->hidden_dim & 3) != 0 || t->ld_seg < 1)
+            return RKV_ERR_INVALID_ARG;
+        if (t->num_seqs * (int64_t)t->max_sentences >= ((int64_t)1 << 31)) return RKV_ERR_INVALID_ARG;
+    }
+    *active = v->redundancy_softmax != 0 || v->pool_window > 1 || v->sentences != nullptr;
     return RKV_OK;
+}
+
+// The variant's sentence rows must cover the cached rows.
+int check_variant_rows(const rkv_variant* v, int n_cached) {
+    return (v && v->sentences && v->sentences->ld_seg < n_cached) ? RKV_ERR_INVALID_ARG : RKV_OK;
 }
 
 int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
@@ -233,17 +250,50 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
+// The device-side form of a variant, reading the base I and R rows of w.
+rkv::VariantIn variant_in(const rkv_variant& v, float lambda, const Workspace& w) {
+    rkv::VariantIn vin;
+    vin.I = w.I;
+    vin.R = w.R;
+    vin.ld = w.ld;
+    vin.lambda = lambda;
+    vin.softmax = v.redundancy_softmax;
+    vin.half = (v.pool_window - 1) / 2;
+    if (const rkv_sentences* t = v.sentences) {
+        vin.pen = t->penalty;
+        vin.count = t->count;
+        vin.seg = t->seg_id;
+        vin.ld_seg = t->ld_seg;
+        vin.num_seqs = t->num_seqs;
+        vin.heads = t->heads;
+        vin.max_sent = t->max_sentences;
+    }
+    return vin;
+}
+
+// The sentence penalties a variant needs, before anything reads them.
+cudaError_t launch_penalty(const rkv_variant* v, cudaStream_t s) {
+    if (!v || !v->sentences) return cudaSuccess;
+    const rkv_sentences* t = v->sentences;
+    return timed(kSentencePenalty, s, [&] {
+        return rkv::launch_sentence_penalty(t->num_seqs, t->max_sentences, t->hidden_dim, t->reps,
+                                            t->count, t->tau, t->penalty, s);
+    });
+}
+
 // The scores with a variant: the base scores into the workspace, then I', R'
 // and Z into the given rows (I_out, R_out may be null).
 int run_scores_variant(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                        float lambda, int beta, float tau, const rkv_variant& v, float* I_out,
                        float* R_out, float* Z, int64_t ld_out, const Workspace& w,
                        cudaStream_t s) {
+    if (launch_penalty(&v, s) != cudaSuccess) return RKV_ERR_CUDA;
     int rc = run_scores(d, K, Q, n_cached, n_obs, lambda, beta, tau, w.I, w.R, w.Z, w.ld, w, s);
     if (rc) return rc;
+    const rkv::VariantIn vin = variant_in(v, lambda, w);
     cudaError_t e = timed(kVariant, s, [&] {
-        return rkv::launch_variant(d->num_problems, n_cached, n_obs, lambda, v.redundancy_softmax,
-                                   v.pool_window, w.I, w.R, w.ld, Z, I_out, R_out, ld_out, s);
+        return rkv::launch_variant(d->num_problems, n_cached, n_obs, vin, Z, I_out, R_out, ld_out,
+                                   s);
     });
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
@@ -270,6 +320,7 @@ int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_c
     if (beta < 0) return RKV_ERR_INVALID_ARG;
     if (desc->num_problems == 0) return RKV_OK;
     if (!out_I || !out_R || !out_Z) return RKV_ERR_INVALID_ARG;
+    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
     const Workspace w = carve(workspace, desc->num_problems, n_cached);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (var_on)
@@ -344,28 +395,25 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
     rc = check_scores(desc, K, Q_obs, n_cached, n_obs, workspace, workspace_bytes);
     if (rc) return rc;
     if (P == 0) return RKV_OK;
+    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
     const Workspace w = carve(workspace, P, n_cached);
-    const bool fused = rkv::compact_smem_bytes(n_cached, n_obs, budget) <= kCompactSmemMax;
-    if (var_on && !fused)
+    const bool fused = rkv::compact_smem_bytes(n_cached, n_obs, budget,
+                                               var_on && variant->sentences) <= kCompactSmemMax;
+    if (var_on && !fused) {
         rc = run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
                                 nullptr, nullptr, w.Z, w.ld, w, s);
-    else
+    } else {
+        if (var_on && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
         rc = run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
                         var_on ? w.R : nullptr, w.Z, w.ld, w, s);
+    }
     if (rc) return rc;
     cudaError_t e;
     if (fused) {
         // selection and compaction in one pass per problem (a variant's Z is
         // formed there from I and R)
         rkv::VariantIn vin;
-        if (var_on) {
-            vin.I = w.I;
-            vin.R = w.R;
-            vin.ld = w.ld;
-            vin.lambda = lambda;
-            vin.softmax = variant->redundancy_softmax;
-            vin.half = (variant->pool_window - 1) / 2;
-        }
+        if (var_on) vin = variant_in(*variant, lambda, w);
         e = timed(kCompact, s, [&] {
             return rkv::launch_compact(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, K, V, out_K,
                                        out_V, desc->n_capacity, row_bytes, in_place, w.status, s,
@@ -485,10 +533,12 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return RKV_ERR_WORKSPACE;
     if (n_cached < 2 || n_obs >= n_cached) return RKV_ERR_INVALID_ARG;
     if (flat.gqa_group * n_obs > 128) return RKV_ERR_UNSUPPORTED;
-    if (rkv::compact_smem_bytes(n_cached, n_obs, budget) > kCompactSmemMax)
+    if (rkv::compact_smem_bytes(n_cached, n_obs, budget, var_on && variant->sentences) >
+        kCompactSmemMax)
         return RKV_ERR_UNSUPPORTED;
     const size_t kc = kc_bytes_for(flat, n_cached);
     if (workspace_bytes < carve(nullptr, P, n_cached, kc).bytes) return RKV_ERR_WORKSPACE;
+    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
     if (P == 0) return RKV_OK;
     const Workspace w = carve(workspace, P, n_cached, kc);
     rkv::PagedIn pg;
@@ -497,18 +547,12 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     pg.log2bs = log2_exact(desc->block_size);
     pg.H = desc->num_kv_heads;
     pg.num_blocks = desc->num_blocks;
+    if (var_on && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
     rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
                     var_on ? w.R : nullptr, w.Z, w.ld, w, s, &pg);
     if (rc) return rc;
     rkv::VariantIn vin;
-    if (var_on) {
-        vin.I = w.I;
-        vin.R = w.R;
-        vin.ld = w.ld;
-        vin.lambda = lambda;
-        vin.softmax = variant->redundancy_softmax;
-        vin.half = (variant->pool_window - 1) / 2;
-    }
+    if (var_on) vin = variant_in(*variant, lambda, w);
     const int row_bytes = desc->head_dim * (int)es;
     cudaError_t e = timed(kCompactPaged, s, [&] {
         return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.Kc,
@@ -520,6 +564,36 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
                                              blocks_for(budget, desc->block_size),
                                              blocks_for(n_cached, desc->block_size), out_freed, s);
         });
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
+int rkv_sentence_penalty(const rkv_sentences* sent, void* stream) {
+    if (!sent) return RKV_ERR_INVALID_ARG;
+    rkv_variant v{0, 1, sent};
+    bool on = false;
+    int rc = check_variant(&v, &on);
+    if (rc) return rc;
+    return launch_penalty(&v, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RKV_OK
+                                                                               : RKV_ERR_CUDA;
+}
+
+int rkv_sentence_reps(const void* hidden, const int32_t* token_seg, int64_t num_seqs, int T,
+                      int hidden_dim, int dtype, int max_sentences, float* out_reps,
+                      void* stream) {
+    if (num_seqs < 0 || T < 0 || hidden_dim < 4 || hidden_dim > RKV_MAX_HIDDEN ||
+        (hidden_dim & 3) != 0 || max_sentences < 1 || max_sentences > RKV_MAX_SENTENCES)
+        return RKV_ERR_INVALID_ARG;
+    if (dtype != RKV_DTYPE_BF16 && dtype != RKV_DTYPE_FP32) return RKV_ERR_UNSUPPORTED;
+    const int64_t chunks = (hidden_dim / 4 + 255) / 256;
+    if (num_seqs * chunks >= ((int64_t)1 << 31)) return RKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return RKV_OK;
+    if (!out_reps || !aligned16(out_reps) || (T > 0 && (!hidden || !token_seg || !aligned16(hidden))))
+        return RKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = timed(kSentenceReps, s, [&] {
+        return rkv::launch_sentence_reps(hidden, dtype, token_seg, num_seqs, T, hidden_dim,
+                                         max_sentences, out_reps, s);
+    });
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 

@@ -73,10 +73,28 @@ struct VariantIn {
     float lambda = 0.f;
     int softmax = 0;
     int half = 0;  // (pool window - 1) / 2
+    // sentence-level penalty: Z_i -= pen[s, seg[p, i]] for 0 <= seg < count[s],
+    // s = (p / heads) % num_seqs; seg rows are compacted with the kept rows
+    const float* pen = nullptr;  // [num_seqs, max_sent]
+    const int32_t* count = nullptr;
+    int32_t* seg = nullptr;  // [P, ld_seg]
+    int64_t ld_seg = 0;
+    int64_t num_seqs = 1;
+    int heads = 1;
+    int max_sent = 0;
 };
 
+// Sentence penalties pen[s, a] = max_{b > a, cos(a, b) > tau} cos(a, b) from
+// reps [S, max_sent, hidden] (fp32) and count [S].
+cudaError_t launch_sentence_penalty(int64_t S, int max_sent, int hidden, const float* reps,
+                                    const int32_t* count, float tau, float* pen, cudaStream_t s);
+// Sentence representations: the mean hidden state of each sentence's tokens.
+cudaError_t launch_sentence_reps(const void* hidden, int dtype, const int32_t* token_seg,
+                                 int64_t S, int T, int hidden_dim, int max_sent, float* reps,
+                                 cudaStream_t s);
+
 // select + gather fused (one CTA per problem); dynamic shared memory it needs
-size_t compact_smem_bytes(int N, int n_obs, int budget);
+size_t compact_smem_bytes(int N, int n_obs, int budget, bool sentences = false);
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
                            void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
@@ -93,11 +111,10 @@ cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, 
 cudaError_t launch_paged_release(int64_t S, int32_t* table, int max_blocks, int nb_keep,
                                  int nb_old, int32_t* out_freed, cudaStream_t s);
 
-// Variant scores (redundancy softmax, importance pooling window) from the
-// base I and R rows (stride ld_in): Z, and I', R' when I_out / R_out are given
-// (stride ld_out).
-cudaError_t launch_variant(int64_t P, int N, int n_obs, float lambda, int softmax, int window,
-                           const float* I, const float* R, int64_t ld_in, float* Z, float* I_out,
-                           float* R_out, int64_t ld_out, cudaStream_t s);
+// Variant scores (redundancy softmax, importance pooling window, sentence
+// penalty) from the base I and R rows of v: Z, and I', R' when I_out / R_out
+// are given (stride ld_out).
+cudaError_t launch_variant(int64_t P, int N, int n_obs, const VariantIn& v, float* Z,
+                           float* I_out, float* R_out, int64_t ld_out, cudaStream_t s);
 
 }  // namespace rkv

@@ -14,6 +14,7 @@
 #pragma once
 
 #include "rkv_common.cuh"
+#include "rkv_internal.h"
 
 namespace rkv {
 
@@ -73,6 +74,22 @@ RKV_DEV float softmax_term(float r, const SoftmaxStats& st) {
 // (no contraction into a fused multiply-add).
 RKV_DEV float variant_z(float lambda, float ip, float rs) {
     return __fsub_rn(__fmul_rn(lambda, ip), __fmul_rn(__fsub_rn(1.0f, lambda), rs));
+}
+
+// The sentence penalty of row i of problem p (SkipKV review, row "Final
+// eviction score"): pen[s, a] for the row's sentence a, 0 for rows outside a
+// sentence or without sentence information.
+RKV_DEV float row_penalty(const VariantIn& v, int64_t p, int i) {
+    if (v.pen == nullptr) return 0.f;
+    const int64_t s = (p / v.heads) % v.num_seqs;
+    const int a = v.seg[p * v.ld_seg + i];
+    const int n = min(v.count[s], v.max_sent);
+    return (a >= 0 && a < n) ? v.pen[s * v.max_sent + a] : 0.f;
+}
+
+// Z of candidate i with every variant term.
+RKV_DEV float variant_score(const VariantIn& v, int64_t p, int i, float ip, float rs) {
+    return __fsub_rn(variant_z(v.lambda, ip, rs), row_penalty(v, p, i));
 }
 
 }  // namespace rkv

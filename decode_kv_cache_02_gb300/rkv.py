@@ -27,6 +27,7 @@ EXPORTED = [
     "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
     "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
     "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
+    "rkv_sentence_reps", "rkv_sentence_penalty",
 ]
 RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_DEVICE = 6
@@ -45,8 +46,52 @@ class _Desc(ctypes.Structure):
                 ("dtype", ctypes.c_int32)]
 
 
+class _Sentences(ctypes.Structure):
+    _fields_ = [("reps", ctypes.c_void_p), ("count", ctypes.c_void_p),
+                ("seg_id", ctypes.c_void_p), ("penalty", ctypes.c_void_p),
+                ("num_seqs", ctypes.c_int64), ("heads", ctypes.c_int32),
+                ("max_sentences", ctypes.c_int32), ("hidden_dim", ctypes.c_int32),
+                ("ld_seg", ctypes.c_int32), ("tau", ctypes.c_float)]
+
+
 class _Variant(ctypes.Structure):
-    _fields_ = [("redundancy_softmax", ctypes.c_int32), ("pool_window", ctypes.c_int32)]
+    _fields_ = [("redundancy_softmax", ctypes.c_int32), ("pool_window", ctypes.c_int32),
+                ("sentences", ctypes.POINTER(_Sentences))]
+
+
+class Sentences:
+    """Sentence-level penalty inputs (rkv_sentences in include/rkv.h):
+    reps [S, max_sentences, hidden] fp32, count [S] int32, seg_id [P, ld_seg]
+    int32 (the sentence of each cached row; compacted in place by the
+    compression), heads (problem p belongs to sequence (p // heads) % S),
+    tau.  penalty [S, max_sentences] fp32 receives the sentence penalties."""
+
+    def __init__(self, reps, count, seg_id, heads: int, tau: float, penalty=None):
+        for t, n in ((reps, "reps"), (count, "count"), (seg_id, "seg_id")):
+            _cuda(t, n)
+        if reps.dtype != torch.float32 or reps.dim() != 3:
+            raise ValueError("reps must be fp32 [S, max_sentences, hidden]")
+        if count.dtype != torch.int32 or seg_id.dtype != torch.int32 or seg_id.dim() != 2:
+            raise ValueError("count, seg_id must be int32 ([S], [P, ld_seg])")
+        self.reps, self.count, self.seg_id = reps, count, seg_id
+        self.heads, self.tau = int(heads), float(tau)
+        self.penalty = penalty if penalty is not None else torch.empty(
+            reps.shape[:2], dtype=torch.float32, device=reps.device)
+
+    def _c(self) -> _Sentences:
+        S, M, Dh = self.reps.shape
+        return _Sentences(self.reps.data_ptr(), self.count.data_ptr(), self.seg_id.data_ptr(),
+                          self.penalty.data_ptr(), S, self.heads, M, Dh, self.seg_id.shape[1],
+                          self.tau)
+
+
+def _variant(redundancy_softmax: bool, pool_window: int, sentences):
+    """The C variant struct (and the sentence struct it points to, which the
+    caller keeps alive for the call)."""
+    sc = sentences._c() if sentences is not None else None
+    v = _Variant(1 if redundancy_softmax else 0, int(pool_window),
+                 ctypes.pointer(sc) if sc is not None else None)
+    return v, sc
 
 
 class _PagedDesc(ctypes.Structure):
@@ -97,6 +142,10 @@ def load(path: str | None = None):
         lib.rkv_paged_compress.argtypes = [pdp, vp, vp, vp, vp, i32, i32, i32, f32, i32, f32, vr,
                                            vp, vp, vp, sz, vp]
         lib.rkv_paged_compress.restype = i32
+        lib.rkv_sentence_reps.argtypes = [vp, vp, i64, i32, i32, i32, i32, vp, vp]
+        lib.rkv_sentence_reps.restype = i32
+        lib.rkv_sentence_penalty.argtypes = [ctypes.POINTER(_Sentences), vp]
+        lib.rkv_sentence_penalty.restype = i32
         lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
         lib.rkv_select.restype = i32
         lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
@@ -215,14 +264,15 @@ def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: f
 
 def rkv_compress_ex(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
                     beta: int = 2, tau: float = 0.9, redundancy_softmax: bool = False,
-                    pool_window: int = 1, out_K=None, out_V=None, out_idx=None, workspace=None,
-                    stream=None):
+                    pool_window: int = 1, sentences: Sentences | None = None, out_K=None,
+                    out_V=None, out_idx=None, workspace=None, stream=None):
     """rkv_compress with a scoring variant: redundancy_softmax turns R into a
     softmax over the candidates, pool_window (odd) max-pools I over that many
-    neighbouring positions."""
+    neighbouring positions, sentences adds the sentence-level penalty (and
+    compacts sentences.seg_id with the rows)."""
     desc, out_K, out_V, out_idx, workspace = _compress_args(
         K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, workspace)
-    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
+    var, _keep = _variant(redundancy_softmax, pool_window, sentences)
     rc = load().rkv_compress_ex(ctypes.byref(desc), K.data_ptr(), V.data_ptr(), Q_obs.data_ptr(),
                                 int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
                                 float(tau), ctypes.byref(var), out_K.data_ptr(), out_V.data_ptr(),
@@ -258,7 +308,7 @@ def rkv_compress_noalloc(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8
     return out_K, out_V, out_idx
 
 
-def _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, variant, workspace, stream):
+def _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, variant, workspace, stream, _keep=None):
     _cuda(K, "K")
     _cuda(Q_obs, "Q_obs")
     G = Q_obs.shape[1]
@@ -290,11 +340,11 @@ def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: i
 
 def rkv_score_ex(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
                  tau: float = 0.9, redundancy_softmax: bool = False, pool_window: int = 1,
-                 workspace=None, stream=None):
+                 sentences: Sentences | None = None, workspace=None, stream=None):
     """(I', R', Z), each fp32 [P, n_cached], for a scoring variant (see
     rkv_compress_ex); I' and R' are the terms that enter Z."""
-    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
-    return _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, var, workspace, stream)
+    var, keep = _variant(redundancy_softmax, pool_window, sentences)
+    return _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, var, workspace, stream, keep)
 
 
 def rkv_select(Z, n_obs: int, budget: int, out_idx=None, stream=None):
@@ -382,8 +432,9 @@ def rkv_paged_freed_per_seq(K_pool, block_table, n_cached: int, budget: int) -> 
 
 def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget: int,
                        n_obs: int = 8, lam: float = 0.1, beta: int = 2, tau: float = 0.9,
-                       redundancy_softmax: bool = False, pool_window: int = 1, out_idx=None,
-                       out_freed=None, workspace=None, stream=None):
+                       redundancy_softmax: bool = False, pool_window: int = 1,
+                       sentences: Sentences | None = None, out_idx=None, out_freed=None,
+                       workspace=None, stream=None):
     """One compression round of a paged cache, in place: K_pool, V_pool
     [num_blocks, H, block_size, d], Q_obs [S*H, G, n_obs, d], block_table
     [S, max_blocks] int32 (entries of freed blocks become -1).  Returns
@@ -414,7 +465,7 @@ def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget
     if out_idx.shape != (P, budget) or out_idx.dtype != torch.int32 \
             or out_freed.shape != (desc.num_seqs, n_free) or out_freed.dtype != torch.int32:
         raise ValueError("output shapes")
-    var = _Variant(1 if redundancy_softmax else 0, int(pool_window))
+    var, _keep = _variant(redundancy_softmax, pool_window, sentences)
     rc = load().rkv_paged_compress(
         ctypes.byref(desc), K_pool.data_ptr(), V_pool.data_ptr(), Q_obs.data_ptr(),
         block_table.data_ptr(), int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
@@ -422,3 +473,31 @@ def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget
         workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _check(rc, "rkv_paged_compress")
     return out_idx, out_freed
+
+
+# -------------------------------------------------------------- sentences --
+
+def rkv_sentence_reps(hidden, token_seg, max_sentences: int, out_reps=None, stream=None):
+    """Mean hidden state of each sentence: hidden [S, T, Dh] (bf16/fp32),
+    token_seg [S, T] int32 (-1: none; a sentence's tokens consecutive) ->
+    reps [S, max_sentences, Dh] fp32."""
+    _cuda(hidden, "hidden")
+    _cuda(token_seg, "token_seg")
+    S, T, Dh = hidden.shape
+    if token_seg.shape != (S, T) or token_seg.dtype != torch.int32:
+        raise ValueError("token_seg must be int32 [S, T]")
+    if out_reps is None:
+        out_reps = torch.empty((S, max_sentences, Dh), dtype=torch.float32, device=hidden.device)
+    rc = load().rkv_sentence_reps(hidden.data_ptr(), token_seg.data_ptr(), S, T, Dh,
+                                  _dtype_code(hidden), int(max_sentences), out_reps.data_ptr(),
+                                  _stream_ptr(stream))
+    _check(rc, "rkv_sentence_reps")
+    return out_reps
+
+
+def rkv_sentence_penalty(sentences: Sentences, stream=None):
+    """Writes and returns sentences.penalty [S, max_sentences]."""
+    sc = sentences._c()
+    _check(load().rkv_sentence_penalty(ctypes.byref(sc), _stream_ptr(stream)),
+           "rkv_sentence_penalty")
+    return sentences.penalty

@@ -235,3 +235,65 @@ def random_indices(P: int, n_cached: int, budget: int, device="cpu",
     keys = torch.rand(P, n_cached, generator=g, device=device)
     top = torch.topk(keys, budget, dim=1).indices
     return torch.sort(top, dim=1).values.to(torch.int32).contiguous()
+
+
+# -------------------------------------------------------------- sentences --
+# Stand-in for the sentence structure of a reasoning trace (SkipKV review,
+# yoonschallenge.tistory.com/1230, row "Method 1": sentences split at
+# newlines and punctuation, represented by mean last-layer hidden states;
+# redundant reflections repeat earlier sentences).  Sentence lengths are drawn
+# uniformly in [SENT_MIN, SENT_MAX] tokens; each sentence's hidden states are
+# a random direction (shared by its tokens) plus per-token noise, and with
+# probability SENT_REPEAT a sentence restates an earlier one (the earlier
+# direction plus a small perturbation), so its mean representation is close
+# to that sentence's.  HIDDEN_LLAMA8B is the model width of the Llama-8B
+# configuration.
+SENT_MIN, SENT_MAX = 8, 48
+SENT_REPEAT = 0.3
+SENT_TAU = 0.9
+HIDDEN_LLAMA8B = 4096
+
+
+@dataclasses.dataclass
+class SentenceInputs:
+    token_seg: torch.Tensor   # [S, T] int32, the sentence of each generated token
+    hidden: torch.Tensor      # [S, T, hidden] per-token last-layer hidden states
+    count: torch.Tensor       # [S] int32, sentences per sequence
+    seg_id: torch.Tensor      # [P, N] int32, the sentence of each cached row
+    max_sentences: int
+    heads: int                # problem p belongs to sequence (p // heads) % S
+
+
+def make_sentences(S: int, heads_per_seq: int, layers: int, N: int, hidden_dim: int,
+                   device="cpu", seed: int = 11, dtype=torch.bfloat16) -> SentenceInputs:
+    """Sentences for S sequences of N cached tokens, for P = layers * S *
+    heads_per_seq problems ordered (layer, sequence, head)."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = []
+    for s in range(S):
+        ls, total = [], 0
+        while total < N:
+            n = int(torch.randint(SENT_MIN, SENT_MAX + 1, (1,), generator=g))
+            ls.append(min(n, N - total))
+            total += ls[-1]
+        lengths.append(ls)
+    M = max(len(ls) for ls in lengths)
+    token_seg = torch.full((S, N), -1, dtype=torch.int32)
+    count = torch.tensor([len(ls) for ls in lengths], dtype=torch.int32)
+    hidden = torch.empty((S, N, hidden_dim))
+    for s, ls in enumerate(lengths):
+        dirs = []
+        t = 0
+        for a, n in enumerate(ls):
+            if a > 0 and float(torch.rand((1,), generator=g)) < SENT_REPEAT:
+                src = int(torch.randint(0, a, (1,), generator=g))
+                d = dirs[src] + 0.1 * torch.randn(hidden_dim, generator=g)
+            else:
+                d = torch.randn(hidden_dim, generator=g)
+            dirs.append(d)
+            token_seg[s, t:t + n] = a
+            hidden[s, t:t + n] = d + 0.5 * torch.randn((n, hidden_dim), generator=g)
+            t += n
+    seg_id = token_seg.repeat_interleave(heads_per_seq, dim=0).repeat(layers, 1)
+    return SentenceInputs(token_seg.to(device), hidden.to(dtype).to(device), count.to(device),
+                          seg_id.contiguous().to(device), M, heads_per_seq)

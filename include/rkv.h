@@ -114,7 +114,7 @@ int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cach
               float* out_I, float* out_R, float* out_Z,
               void* workspace, size_t workspace_bytes, void* stream);
 
-/* Variants of the scoring (both off: the step above).
+/* Variants of the scoring (all off: the step above).
  *   redundancy_softmax  the R-KV review, question 2, cause 3, lists a softmax
  *                       of the redundancy among the operations of a
  *                       compression round.  1: the candidates' redundancy
@@ -127,13 +127,64 @@ int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cach
  *                       against): I'_i = max of I_j over the candidates j
  *                       with |j - i| <= (w-1)/2 (the window is cut at the
  *                       candidates' ends).  1: no pooling.
- * Z_i = lambda*I'_i - (1-lambda)*R'_i; observation tokens keep their I, get
- * R = 0 and Z = +inf as before.  A NULL variant is both off. */
+ *   sentences           a sentence-level penalty (below), or NULL.
+ * Z_i = lambda*I'_i - (1-lambda)*R'_i - pen_i; observation tokens keep their
+ * I, get R = 0 and Z = +inf as before.  A NULL variant is all off. */
+/* Sentence-level redundancy (the SkipKV review, yoonschallenge.tistory.com/
+ * 1230, summary-table rows "Method 1: Sentence-level KV Storage Skipping",
+ * "Final eviction score" and "Cache Range Monitoring").  A sentence is
+ * represented by the mean of its tokens' last-layer hidden states
+ * (rkv_sentence_reps computes it); when the cosine similarity of sentence a
+ * and a later sentence b of the same sequence exceeds tau, a is the
+ * redundant one.  Its penalty is pen_a = max of cos(a, b) over the later b
+ * with cos(a, b) > tau (0 if none), and every cached row of sentence a has
+ * pen_a subtracted from its Z, so redundant earlier sentences go first while
+ * the budget still decides how many rows stay.  The sentence of each cached
+ * row is tracked in seg_id, which the compression compacts along with the
+ * rows (the cache-range mapping the review describes).
+ *   reps      [num_seqs, max_sentences, hidden_dim] fp32 (rows >= count[s]
+ *             ignored)
+ *   count     [num_seqs] sentences in use per sequence (device memory)
+ *   seg_id    [P, ld_seg] int32: sentence of cached row i of problem p, or
+ *             -1 (ids outside 0..count-1 count as none).  Problem p belongs
+ *             to sequence (p / heads) % num_seqs (problems ordered layer,
+ *             sequence, head).  After rkv_compress_ex / rkv_paged_compress
+ *             entries 0..budget-1 hold the kept rows' sentences.
+ *   penalty   [num_seqs, max_sentences] fp32, written: pen_a per sentence.
+ * All pointers are device memory owned by the caller. */
 typedef struct {
-    int32_t redundancy_softmax; /* 0 or 1 */
-    int32_t pool_window;        /* odd, 1 .. RKV_MAX_POOL_WINDOW */
+    const float* reps;
+    const int32_t* count;
+    int32_t* seg_id;
+    float* penalty;
+    int64_t num_seqs;      /* >= 1 */
+    int32_t heads;         /* >= 1 */
+    int32_t max_sentences; /* 1 .. RKV_MAX_SENTENCES */
+    int32_t hidden_dim;    /* 4 .. RKV_MAX_HIDDEN, a multiple of 4 */
+    int32_t ld_seg;        /* row stride of seg_id, >= n_cached */
+    float tau;             /* sentence-similarity threshold */
+} rkv_sentences;
+#define RKV_MAX_SENTENCES 65536
+#define RKV_MAX_HIDDEN 16384
+
+typedef struct {
+    int32_t redundancy_softmax;       /* 0 or 1 */
+    int32_t pool_window;              /* odd, 1 .. RKV_MAX_POOL_WINDOW */
+    const rkv_sentences* sentences;   /* NULL: no sentence-level penalty */
 } rkv_variant;
 #define RKV_MAX_POOL_WINDOW 255
+
+/* Sentence representations: out_reps[s, a, :] = mean of hidden[s, t, :] over
+ * the tokens t with token_seg[s, t] == a (zeros for a sentence without
+ * tokens).  hidden [num_seqs, T, hidden_dim] (dtype bf16 or fp32), token_seg
+ * [num_seqs, T] int32 (-1: no sentence; ids >= max_sentences ignored),
+ * out_reps [num_seqs, max_sentences, hidden_dim] fp32. */
+int rkv_sentence_reps(const void* hidden, const int32_t* token_seg, int64_t num_seqs, int T,
+                      int hidden_dim, int dtype, int max_sentences, float* out_reps,
+                      void* stream);
+
+/* The penalties alone: writes sent->penalty from reps, count and tau. */
+int rkv_sentence_penalty(const rkv_sentences* sent, void* stream);
 
 /* rkv_compress / rkv_score with a variant (invalid variant fields:
  * RKV_ERR_INVALID_ARG).  rkv_score_ex's out_I and out_R are the I' and R'

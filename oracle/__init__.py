@@ -6,7 +6,9 @@ package.  The product library (``decode_kv_cache_02_gb300``) never imports,
 loads or calls it, and the two share no code.
 
 The arithmetic lives in ``rkv_oracle.c`` (plain fp64 loops, a pthread pool over
-independent problems); this module only marshals numpy arrays through ctypes.
+independent problems); this module marshals numpy arrays through ctypes, and
+holds the paged round and the sentence-level penalty of the SkipKV review
+(yoonschallenge.tistory.com/1230) as plain fp64 numpy loops.
 Every function follows the R-KV review page (yoonschallenge.tistory.com/1236):
 the opening notes and the summary-table rows "Decoding-time compression
 scheme", "importance", "redundancy" and "final selection criterion", and
@@ -165,11 +167,12 @@ def select(Z, n_obs: int, budget: int) -> np.ndarray:
 
 
 def variant(sc: dict, n_obs: int, lam: float, redundancy_softmax: bool = False,
-            pool_window: int = 1) -> dict:
+            pool_window: int = 1, row_penalty=None) -> dict:
     """The scores of a variant (readings R10, R11) from the base scores
     ``sc`` of ``score()``: a copy of ``sc`` whose I, R, Z are I pooled over
     ``pool_window`` positions, R softmaxed over the candidates, and their
-    combination."""
+    combination, minus ``row_penalty`` [P, N] (the sentence penalty of each
+    row, ``row_penalties()``) when given."""
     I, R = _f64(sc["I"]), _f64(sc["R"])
     P, N = I.shape
     out = dict(sc)
@@ -180,6 +183,9 @@ def variant(sc: dict, n_obs: int, lam: float, redundancy_softmax: bool = False,
         _ptr(out["R"], ctypes.c_double), _ptr(out["Z"], ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle variant: invalid sizes")
+    if row_penalty is not None:
+        C = N - n_obs
+        out["Z"][:, :C] = out["Z"][:, :C] - np.asarray(row_penalty, dtype=np.float64)[:, :C]
     return out
 
 
@@ -199,7 +205,8 @@ def gather(src: np.ndarray, idx: np.ndarray) -> np.ndarray:
 
 def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
              beta: int, tau: float, nthreads: int | None = None,
-             redundancy_softmax: bool = False, pool_window: int = 1) -> dict:
+             redundancy_softmax: bool = False, pool_window: int = 1,
+             row_penalty=None) -> dict:
     """Scores and selection of one compression round of P problems.
     K [P, n_cap, d] (rows >= n_cached ignored), Q [P, G, n_obs, d].  Returns
     dict(idx, scores); the kept rows themselves are ``gather(src, idx)``.
@@ -213,8 +220,8 @@ def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
         sc = None
     else:
         sc = score(_f64(K)[:, :n_cached], Q, n_obs, lam, beta, tau, nthreads)
-        if redundancy_softmax or pool_window != 1:
-            sc = variant(sc, n_obs, lam, redundancy_softmax, pool_window)
+        if redundancy_softmax or pool_window != 1 or row_penalty is not None:
+            sc = variant(sc, n_obs, lam, redundancy_softmax, pool_window, row_penalty)
         idx = select(sc["Z"], n_obs, budget)
     return {"idx": idx, "scores": sc}
 
@@ -245,7 +252,8 @@ def paged_rows(pool: np.ndarray, table: np.ndarray, n_rows: int) -> np.ndarray:
 
 def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: int,
                    lam: float, beta: int, tau: float, idx_used=None, nthreads=None,
-                   redundancy_softmax: bool = False, pool_window: int = 1) -> dict:
+                   redundancy_softmax: bool = False, pool_window: int = 1,
+                   row_penalty=None) -> dict:
     """One paged compression round.  K_pool / V_pool: raw arrays [num_blocks,
     H, bs, d] (any element type; rows move as they are); the keys are scored
     from ``K_f64`` = the float values of K_pool's logical rows.  Returns
@@ -262,7 +270,7 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
     if K_f.dtype == np.int16:  # bf16 bit patterns: widen exactly to float
         K_f = (K_f.astype(np.int32) << 16).view(np.float32)
     res = compress(K_f, Q, n_cached, budget, n_obs, lam, beta, tau, nthreads,
-                   redundancy_softmax, pool_window)
+                   redundancy_softmax, pool_window, row_penalty)
     idx = res["idx"] if idx_used is None else np.asarray(idx_used)
     Kp, Vp, new_table = K_pool.copy(), V_pool.copy(), table.copy()
     freed = np.zeros((S, 0), dtype=np.int32)
@@ -282,3 +290,76 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
         new_table[:, nb_keep:nb_old] = -1
     return {"idx": res["idx"], "scores": res["scores"], "K_pool": Kp, "V_pool": Vp,
             "table": new_table, "freed": freed}
+
+
+# -------------------------------------------------------------- sentences --
+# SkipKV review (yoonschallenge.tistory.com/1230), summary-table rows "Method
+# 1: Sentence-level KV Storage Skipping" (a sentence is the mean of its
+# tokens' last-layer hidden states; when two sentences' cosine similarity
+# exceeds tau the earlier one is redundant and goes first), "Final eviction
+# score" (the tokens of a redundant sentence get the similarity as an extra
+# penalty) and "Cache Range Monitoring" (each cached row keeps its sentence).
+# Readings: R12 the penalty of sentence a is the largest cos(a, b) over the
+# later sentences b with cos(a, b) > tau (strict), 0 if none; R13 it is
+# subtracted from Z of every candidate row of sentence a; R14 rows whose
+# sentence id is outside 0..count-1 carry no penalty.
+
+
+def sentence_reps(hidden, token_seg, max_sentences: int) -> np.ndarray:
+    """reps [S, max_sentences, Dh]: mean of hidden[s, t] over the tokens t
+    with token_seg[s, t] == a; zeros for a sentence with no token."""
+    H = _f64(hidden)
+    seg = np.asarray(token_seg)
+    S, T, Dh = H.shape
+    reps = np.zeros((S, max_sentences, Dh))
+    for s_ in range(S):
+        for a in range(max_sentences):
+            rows = [t for t in range(T) if seg[s_, t] == a]
+            if rows:
+                reps[s_, a] = H[s_, rows].sum(axis=0) / len(rows)
+    return reps
+
+
+def sentence_penalty(reps, count, tau: float, border_eps: float = BORDER_EPS):
+    """(pen [S, M], border [S, M]): pen[s, a] = max cos(a, b) over a < b <
+    count[s] with cos(a, b) > tau, else 0; border marks sentences with some
+    later cos within border_eps of tau (the threshold decision can flip under
+    rounding)."""
+    R = _f64(reps)
+    cnt = np.asarray(count)
+    S, M, _ = R.shape
+    pen = np.zeros((S, M))
+    border = np.zeros((S, M), dtype=bool)
+    for s_ in range(S):
+        n = int(min(max(cnt[s_], 0), M))
+        for a in range(n):
+            na = max(np.sqrt(np.dot(R[s_, a], R[s_, a])), 1e-12)
+            best = None
+            for b in range(a + 1, n):
+                nb = max(np.sqrt(np.dot(R[s_, b], R[s_, b])), 1e-12)
+                c = np.dot(R[s_, a], R[s_, b]) / (na * nb)
+                if abs(c - tau) < border_eps:
+                    border[s_, a] = True
+                if c > tau and (best is None or c > best):
+                    best = c
+            pen[s_, a] = 0.0 if best is None else best
+    return pen, border
+
+
+def row_penalties(pen, count, seg_id, heads: int, n_rows: int) -> np.ndarray:
+    """[P, n_rows]: the penalty of each cached row's sentence; problem p
+    belongs to sequence (p // heads) % S (reading R14 for ids out of range)."""
+    pen = np.asarray(pen, dtype=np.float64)
+    cnt = np.asarray(count)
+    seg = np.asarray(seg_id)
+    S = pen.shape[0]
+    P = seg.shape[0]
+    out = np.zeros((P, n_rows))
+    for p in range(P):
+        s_ = (p // heads) % S
+        n = int(min(max(cnt[s_], 0), pen.shape[1]))
+        for i in range(n_rows):
+            a = int(seg[p, i])
+            if 0 <= a < n:
+                out[p, i] = pen[s_, a]
+    return out

@@ -143,6 +143,27 @@ def test_paged_sizes_and_argument_errors(lib):
     assert call(D(mb=2000), n=30000, budget=2048) == 2  # beyond the fused kernel's shared memory
 
 
+def test_sentence_argument_errors(lib):
+    """Invalid sentence descriptors are refused on the host."""
+    from decode_kv_cache_02_gb300 import rkv
+    fake = 1 << 20
+    S_ = lambda **kw: rkv._Sentences(kw.get("reps", fake), fake + 2 ** 30, fake + 2 ** 31,
+                                     fake + 2 ** 32, kw.get("S", 2), kw.get("heads", 8),
+                                     kw.get("M", 40), kw.get("Dh", 4096), kw.get("ld", 1152),
+                                     0.9)
+    for kw in ({"S": 0}, {"heads": 0}, {"M": 0}, {"M": 70000}, {"Dh": 4098}, {"Dh": 0},
+               {"Dh": 20000}, {"reps": fake + 4}, {"reps": 0}):
+        assert lib.rkv_sentence_penalty(ctypes.byref(S_(**kw)), None) == 1, kw
+    d = _desc(P=16)
+    v = rkv._Variant(0, 1, ctypes.pointer(S_(ld=1000)))  # seg rows shorter than n_cached
+    rc = lib.rkv_compress_ex(ctypes.byref(d), fake, fake + 2 ** 30, fake + 2 ** 31, 1152, 1024,
+                             8, 0.1, 2, 0.9, ctypes.byref(v), fake + 2 ** 32, fake + 2 ** 33,
+                             fake + 2 ** 34, fake + 2 ** 35, 1 << 40, None)
+    assert rc == 1
+    assert lib.rkv_sentence_reps(fake, fake, 2, 10, 4098, 0, 8, fake, None) == 1
+    assert lib.rkv_sentence_reps(fake, fake, 2, 10, 4096, 5, 8, fake, None) == 2
+
+
 def test_binding_rejects_cpu_tensors(lib):
     from decode_kv_cache_02_gb300 import rkv
     K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)

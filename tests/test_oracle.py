@@ -469,6 +469,91 @@ def test_paged_round_identity_when_not_over_budget():
     assert out["freed"].shape[1] == 0
 
 
+# -------------------------------------------------------------- sentences --
+# SkipKV review (yoonschallenge.tistory.com/1230), rows "Method 1" and "Final
+# eviction score": readings R12-R14 of the oracle.
+
+def test_sentence_reps_equal_index_add_mean():
+    """The mean hidden state per sentence equals torch's index_add divided
+    by the token counts (catches a wrong divisor or a shifted run)."""
+    si = wl.make_sentences(2, 1, 1, 97, 12, dtype=torch.float32)
+    reps = oracle.sentence_reps(si.hidden, si.token_seg, si.max_sentences)
+    for s_ in range(2):
+        seg = si.token_seg[s_].long()
+        tot = torch.zeros(si.max_sentences, 12, dtype=torch.float64).index_add_(
+            0, seg, si.hidden[s_].double())
+        cnt = torch.bincount(seg, minlength=si.max_sentences).double().clamp(min=1)[:, None]
+        np.testing.assert_allclose(reps[s_], (tot / cnt).numpy(), rtol=0, atol=1e-12)
+
+
+def test_sentence_penalty_equals_normalised_matmul():
+    """pen[a] = the largest cosine above tau with a later sentence: a masked
+    upper-triangular max of numpy's normalised matmul."""
+    rng = np.random.default_rng(5)
+    reps = rng.standard_normal((2, 9, 16))
+    reps[0, 2] = reps[0, 6] * 1.5 + 0.05 * rng.standard_normal(16)
+    reps[1, 0] = reps[1, 8] * 0.5 + 0.05 * rng.standard_normal(16)
+    count = np.array([9, 9])
+    pen, _ = oracle.sentence_penalty(reps, count, 0.3)
+    for s_ in range(2):
+        X = reps[s_] / np.linalg.norm(reps[s_], axis=1, keepdims=True)
+        C = X @ X.T
+        up = np.triu(np.ones((9, 9), dtype=bool), 1) & (C > 0.3)
+        ref = np.where(up.any(axis=1), np.where(up, C, -np.inf).max(axis=1), 0.0)
+        np.testing.assert_allclose(pen[s_], ref, rtol=0, atol=1e-13)
+    assert pen[0, 2] > 0.99 and pen[1, 0] > 0.99
+
+
+def test_sentence_penalty_closed_forms():
+    """Only the earlier of two equal sentences is penalised (by exactly 1);
+    of three copies the first two; the threshold is strict (cos = 3/5 at
+    tau = 0.6 gives nothing); the penalty is the similarity itself, also
+    below zero when tau is; sentences past count and zero vectors give 0."""
+    e = np.eye(4)
+    reps = np.stack([e[0], e[1], 2 * e[0], 3 * e[0] + 4 * e[2], e[3], 3 * e[1]])[None]
+    pen, _ = oracle.sentence_penalty(reps, np.array([6]), 0.9)
+    np.testing.assert_allclose(pen[0], [1, 1, 0, 0, 0, 0], rtol=0, atol=1e-15)
+    pen, _ = oracle.sentence_penalty(reps[:, [0, 3]], np.array([2]), 0.6)
+    assert pen[0, 0] == 0.0
+    pen, _ = oracle.sentence_penalty(reps[:, [0, 3]], np.array([2]), 0.5999)
+    assert pen[0, 0] == 0.6
+    neg = np.stack([e[0], -e[0] + np.sqrt(15) * e[1]])[None]  # cos = -1/4
+    pen, _ = oracle.sentence_penalty(neg, np.array([2]), -0.5)
+    assert abs(pen[0, 0] + 0.25) < 1e-15
+    pen, _ = oracle.sentence_penalty(reps, np.array([2]), 0.9)   # sentence 2 not counted
+    assert np.all(pen == 0)
+    zero = np.zeros((1, 2, 4))
+    assert np.all(oracle.sentence_penalty(zero, np.array([2]), -1.0)[0] == 0)
+
+
+def test_row_penalties_follow_the_sentence_ids():
+    pen = np.array([[0.5, 0.0, 0.9], [0.7, 0.2, 0.0]])
+    count = np.array([3, 2])
+    seg = np.array([[0, 0, 2, -1, 5], [0, 1, 2, 1, 0]] * 2)  # P = 4, heads = 1, 2 layers
+    out = oracle.row_penalties(pen, count, seg, 1, 5)
+    np.testing.assert_array_equal(out[0], [0.5, 0.5, 0.9, 0, 0])
+    np.testing.assert_array_equal(out[1], [0.7, 0.2, 0, 0.2, 0.7])  # id 2 >= count 2
+    np.testing.assert_array_equal(out[2], out[0])
+
+
+def test_redundant_earlier_sentence_goes_first():
+    """SkipKV's point: with equal importance and a sentence repeated later,
+    evicting that many tokens removes the earlier copy's rows."""
+    rng = np.random.default_rng(8)
+    N, d, n_obs = 40, 32, 4
+    K = rng.standard_normal((1, N, d))
+    Q = np.zeros((1, 2, n_obs, d))
+    seg = np.repeat(np.arange(5), 8)[None]  # five sentences of 8 rows
+    reps = rng.standard_normal((1, 5, 24))
+    reps[0, 3] = reps[0, 1] + 0.01 * rng.standard_normal(24)
+    pen, _ = oracle.sentence_penalty(reps, np.array([5]), 0.9)
+    assert pen[0, 1] > 0.99 and np.count_nonzero(pen) == 1
+    rp = oracle.row_penalties(pen, np.array([5]), seg, 1, N)
+    res = oracle.compress(K, Q, N, N - 8, n_obs, 0.1, 2, 0.9, row_penalty=rp)
+    evicted = sorted(set(range(N)) - set(res["idx"][0].tolist()))
+    assert evicted == list(range(8, 16))
+
+
 # ------------------------------------------------------------- invariants --
 
 def test_compress_invariants_tiny_and_identity():
