@@ -303,15 +303,29 @@ def _sentences(args, w, dev):
     return rkv.Sentences(reps, si.count, si.seg_id, si.heads, wl.SENT_TAU)
 
 
+def _schedule(args, w, dev):
+    """The ForesightKV-style schedule of --recent-window / --pool-extra /
+    --temperature, with seeded uniforms for a sampled pool, or None."""
+    if not args.recent_window:
+        return None
+    L = args.recent_window
+    C, k = w.n_cached - L, w.budget - L
+    u = None
+    if args.pool_extra > 0:
+        g = torch.Generator(device=dev).manual_seed(w.seed + 17)
+        u = torch.rand((w.problems, C), generator=g, device=dev)
+    return rkv.Schedule(L, min(C, k + args.pool_extra), args.temperature, u)
+
+
 def _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, softmax=False, window=1,
-             sentences=None):
+             sentences=None, schedule=None):
     """One compression step of workload `w` (with a scoring variant if asked)."""
-    if softmax or window != 1 or sentences is not None:
+    if softmax or window != 1 or sentences is not None or schedule is not None:
         def step():
             rkv.rkv_compress_ex(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
                                 redundancy_softmax=softmax, pool_window=window,
-                                sentences=sentences, out_K=out_K, out_V=out_V, out_idx=idx,
-                                workspace=ws, stream=stream)
+                                sentences=sentences, schedule=schedule, out_K=out_K,
+                                out_V=out_V, out_idx=idx, workspace=ws, stream=stream)
     else:
         def step():
             rkv.rkv_compress(K, V, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
@@ -518,8 +532,9 @@ def run_ours(args, w):
     ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
     stream = torch.cuda.current_stream()
     sent = _sentences(args, w, dev)
+    sch = _schedule(args, w, dev)
     step = _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, args.redundancy_softmax,
-                    args.pool_window, sent)
+                    args.pool_window, sent, sch)
     elapsed, kernels, clock_summary = _time_steps(step, args.steps, args.warmup, ws, stream,
                                                   local, world)
     launches = sum(v["launches"] for v in kernels.values())
@@ -542,9 +557,13 @@ def run_ours(args, w):
         "kernels_ms_per_step": {k: v["ms"] / args.steps for k, v in kernels.items()},
         "clocks": clock_summary,
     }
-    if args.redundancy_softmax or args.pool_window != 1 or sent is not None:
+    if args.redundancy_softmax or args.pool_window != 1 or sent is not None or sch is not None:
         line["config"]["variant"] = {"redundancy_softmax": args.redundancy_softmax,
                                      "pool_window": args.pool_window}
+        if sch is not None:
+            line["config"]["variant"]["schedule"] = {
+                "recent_window": sch.recent_window, "pool_size": sch.pool_size,
+                "temperature": sch.temperature, "sampled": sch.uniforms is not None}
         if sent is not None:
             line["config"]["variant"]["sentences"] = {
                 "sequences": sent.reps.shape[0], "max_sentences": sent.reps.shape[1],
@@ -747,6 +766,12 @@ def main():
     ap.add_argument("--block-size", type=int, default=16, help="rows per block with --paged")
     ap.add_argument("--sentences", action="store_true",
                     help="scoring variant: sentence-level penalty on synthetic sentences")
+    ap.add_argument("--recent-window", type=int, default=0,
+                    help="schedule: keep the newest L rows (ForesightKV-style), 0 = off")
+    ap.add_argument("--pool-extra", type=int, default=0,
+                    help="schedule: pool = kept + this many, sampled by Gumbel keys")
+    ap.add_argument("--temperature", type=float, default=0.05,
+                    help="schedule: sampling temperature")
     ap.add_argument("--sweep", action="store_true",
                     help="time the step over a lambda/beta/tau/variant sweep, one line each")
     args = ap.parse_args()

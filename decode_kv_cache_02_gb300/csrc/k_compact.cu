@@ -111,6 +111,172 @@ RKV_DEV int bucket_of(float z, float zmin, float scale) {
     return min(255, max(0, (int)((z - zmin) * scale)));
 }
 
+struct SelShared {
+    uint32_t hist[256];
+    float red[2][kWarps];
+    int warp[kWarps];
+    uint32_t m, uk, eq, need;
+};
+
+// The kk-th largest (kk >= 1) of the C keys: uk, and eq_cut such that the
+// keys equal to uk of rank >= eq_cut among them (in index order) are in the
+// top kk (ties go to the larger index).  zmin / zmax are this thread's bounds
+// of the keys' finite float values; `list` (C entries) is scratch.  Every
+// thread calls it; it ends with a barrier.
+__device__ __forceinline__ void kth_largest(const uint32_t* keys, uint32_t* list, int C, int kk,
+                                            float zmin, float zmax, SelShared& sh, uint32_t& uk_out,
+                                            uint32_t& eq_cut_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < 256; b += kThreads) sh.hist[b] = 0u;
+    if (tid == 0) sh.m = 0u;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        zmin = fminf(zmin, __shfl_xor_sync(0xffffffffu, zmin, o));
+        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    }
+    if (lane == 0) {
+        sh.red[0][warp] = zmin;
+        sh.red[1][warp] = zmax;
+    }
+    __syncthreads();
+    zmin = sh.red[0][0];
+    zmax = sh.red[1][0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) {
+        zmin = fminf(zmin, sh.red[0][w]);
+        zmax = fmaxf(zmax, sh.red[1][w]);
+    }
+    const float range = zmax - zmin;
+    const float scale = range > 0.f ? 255.5f / range : 0.f;
+    for (int i = tid; i < C; i += kThreads)
+        atomicAdd(&sh.hist[bucket_of(from_orderable(keys[i]), zmin, scale)], 1u);
+    __syncthreads();
+    uint32_t krem = (uint32_t)kk, bucket = 0, m = 0;
+    if (warp == 0) find_bin(sh.hist, krem, bucket, m);
+    if (tid == 0) sh.uk = bucket;
+    __syncthreads();
+    bucket = sh.uk;
+    for (int i = tid; i < C; i += kThreads) {
+        const uint32_t u = keys[i];
+        if ((uint32_t)bucket_of(from_orderable(u), zmin, scale) == bucket) list[atomicAdd(&sh.m, 1u)] = u;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // the krem-th largest of the m keys in the bucket: uk, how many keys
+        // equal it and how many of those are kept
+        m = sh.m;
+        uint32_t uk, eq_count, need_eq;
+        if (m <= 32) {
+            const uint32_t mine = lane < (int)m ? list[lane] : 0u;
+            uint32_t gt = 0, eq = 0;
+            for (uint32_t x = 0; x < m; ++x) {
+                const uint32_t o = __shfl_sync(0xffffffffu, mine, x);
+                gt += o > mine;
+                eq += o == mine;
+            }
+            const bool it = lane < (int)m && gt < krem && krem <= gt + eq;
+            const int src = __ffs(__ballot_sync(0xffffffffu, it)) - 1;
+            uk = __shfl_sync(0xffffffffu, mine, src);
+            eq_count = __shfl_sync(0xffffffffu, eq, src);
+            need_eq = krem - __shfl_sync(0xffffffffu, gt, src);
+        } else {
+            // radix passes over the bucket's keys, from the highest bit where
+            // they differ
+            uint32_t lmin = 0xffffffffu, lmax = 0u;
+            for (uint32_t x = lane; x < m; x += 32) {
+                lmin = min(lmin, list[x]);
+                lmax = max(lmax, list[x]);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                lmin = min(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+                lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            }
+            int top = lmin == lmax ? 0 : 32 - __clz(lmin ^ lmax);
+            uint32_t prefix = top == 32 ? 0u : lmax & ~((1u << top) - 1u);
+            eq_count = m;
+            while (top > 0) {
+                const int shf = top >= 8 ? top - 8 : 0;
+                const uint32_t dm = top >= 8 ? 255u : ((1u << top) - 1u);
+                const uint32_t pm = top == 32 ? 0u : ~((1u << top) - 1u);
+                __syncwarp();
+#pragma unroll
+                for (int b = 0; b < 8; ++b) sh.hist[lane * 8 + b] = 0u;
+                __syncwarp();
+                for (uint32_t x = lane; x < m; x += 32) {
+                    const uint32_t u = list[x];
+                    if ((u & pm) == prefix) atomicAdd(&sh.hist[(u >> shf) & dm], 1u);
+                }
+                __syncwarp();
+                uint32_t dg;
+                find_bin(sh.hist, krem, dg, eq_count);
+                prefix |= dg << shf;
+                top = shf;
+            }
+            uk = prefix;
+            need_eq = krem;
+        }
+        if (lane == 0) {
+            sh.uk = uk;
+            sh.eq = eq_count;
+            sh.need = need_eq;
+        }
+    }
+    __syncthreads();
+    uk_out = sh.uk;
+    eq_cut_out = sh.eq - sh.need;
+}
+
+// The top kk keys given their threshold (uk, eq_cut), in index order over
+// contiguous ranges per thread with block scans.  kMark: keys outside the top
+// kk become 0 (below every float's key); else: their indices, ascending,
+// into out[0..kk).
+template <bool kMark>
+__device__ __forceinline__ void take_top(uint32_t* keys, int C, uint32_t uk, uint32_t eq_cut,
+                                         int kk, int32_t* out, SelShared& sh) {
+    const int tid = threadIdx.x;
+    const int ipt = (C + kThreads - 1) / kThreads;
+    const int lo = min(C, tid * ipt), hi = min(C, lo + ipt);
+    int eq_before = 0;
+    if (eq_cut > 0) {
+        int n_eq = 0;
+        for (int i = lo; i < hi; ++i) n_eq += (keys[i] == uk);
+        int eq_total;
+        eq_before = block_scan(n_eq, sh.warp, &eq_total);
+    }
+    if constexpr (kMark) {
+        int e = eq_before;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t u = keys[i];
+            bool in = false;
+            if (u > uk) in = true;
+            else if (u == uk) { in = (e >= (int)eq_cut); ++e; }
+            if (!in) keys[i] = 0u;
+        }
+        __syncthreads();
+    } else {
+        int n_keep = 0;
+        {
+            int e = eq_before;
+            for (int i = lo; i < hi; ++i) {
+                const uint32_t u = keys[i];
+                if (u > uk) ++n_keep;
+                else if (u == uk) { n_keep += (e >= (int)eq_cut); ++e; }
+            }
+        }
+        int keep_total;
+        int pos = block_scan(n_keep, sh.warp, &keep_total);
+        int e = eq_before;
+        for (int i = lo; i < hi; ++i) {
+            const uint32_t u = keys[i];
+            bool keep = false;
+            if (u > uk) keep = true;
+            else if (u == uk) { keep = (e >= (int)eq_cut); ++e; }
+            if (keep && pos < kk) out[pos++] = i;
+        }
+    }
+}
+
 template <bool kPaged>
 __global__ void __launch_bounds__(kThreads)
 compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
@@ -122,11 +288,9 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
     uint32_t* keys = s_dyn;                                         // [C]
     uint32_t* list = keys + C;                                      // [C]
     int32_t* sidx = reinterpret_cast<int32_t*>(list + C);           // [budget]
-    __shared__ uint32_t s_hist[256];
-    __shared__ float s_red[2][kWarps];
-    __shared__ int s_warp[kWarps];
-    __shared__ uint32_t s_m, s_uk, s_eq, s_need;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ SelShared sh;
+    float (*s_red)[kWarps] = sh.red;
+    const int tid = threadIdx.x;
     const int64_t p = blockIdx.x;
 
     // ---------------------------------------------------------- select --
@@ -169,133 +333,34 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
         }
         __syncthreads();  // `list` is reused for the bucket's keys below
     }
-    for (int b = tid; b < 256; b += kThreads) s_hist[b] = 0u;
-    if (tid == 0) s_m = 0u;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        zmin = fminf(zmin, __shfl_xor_sync(0xffffffffu, zmin, o));
-        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-    }
-    if (lane == 0) {
-        s_red[0][warp] = zmin;
-        s_red[1][warp] = zmax;
-    }
-    __syncthreads();
-    zmin = s_red[0][0];
-    zmax = s_red[1][0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-        zmin = fminf(zmin, s_red[0][w]);
-        zmax = fmaxf(zmax, s_red[1][w]);
-    }
-    const float range = zmax - zmin;
-    const float scale = range > 0.f ? 255.5f / range : 0.f;
-    for (int i = tid; i < C; i += kThreads) atomicAdd(&s_hist[bucket_of(from_orderable(keys[i]), zmin, scale)], 1u);
-    __syncthreads();
-    uint32_t krem = (uint32_t)(k > 0 ? k : 1), bucket = 0, m = 0;
-    if (warp == 0) find_bin(s_hist, krem, bucket, m);
-    if (tid == 0) s_uk = bucket;
-    __syncthreads();
-    bucket = s_uk;
-    for (int i = tid; i < C; i += kThreads) {
-        const uint32_t u = keys[i];
-        if ((uint32_t)bucket_of(from_orderable(u), zmin, scale) == bucket) list[atomicAdd(&s_m, 1u)] = u;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // the krem-th largest of the m keys in the bucket: uk, how many keys
-        // equal it and how many of those are kept
-        m = s_m;
-        uint32_t uk, eq_count, need_eq;
-        if (m <= 32) {
-            const uint32_t mine = lane < (int)m ? list[lane] : 0u;
-            uint32_t gt = 0, eq = 0;
-            for (uint32_t x = 0; x < m; ++x) {
-                const uint32_t o = __shfl_sync(0xffffffffu, mine, x);
-                gt += o > mine;
-                eq += o == mine;
-            }
-            const bool it = lane < (int)m && gt < krem && krem <= gt + eq;
-            const int src = __ffs(__ballot_sync(0xffffffffu, it)) - 1;
-            uk = __shfl_sync(0xffffffffu, mine, src);
-            eq_count = __shfl_sync(0xffffffffu, eq, src);
-            need_eq = krem - __shfl_sync(0xffffffffu, gt, src);
-        } else {
-            // radix passes over the bucket's keys, from the highest bit where
-            // they differ
-            uint32_t lmin = 0xffffffffu, lmax = 0u;
-            for (uint32_t x = lane; x < m; x += 32) {
-                lmin = min(lmin, list[x]);
-                lmax = max(lmax, list[x]);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                lmin = min(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
-                lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-            }
-            int top = lmin == lmax ? 0 : 32 - __clz(lmin ^ lmax);
-            uint32_t prefix = top == 32 ? 0u : lmax & ~((1u << top) - 1u);
-            eq_count = m;
-            while (top > 0) {
-                const int sh = top >= 8 ? top - 8 : 0;
-                const uint32_t dm = top >= 8 ? 255u : ((1u << top) - 1u);
-                const uint32_t pm = top == 32 ? 0u : ~((1u << top) - 1u);
-                __syncwarp();
-#pragma unroll
-                for (int b = 0; b < 8; ++b) s_hist[lane * 8 + b] = 0u;
-                __syncwarp();
-                for (uint32_t x = lane; x < m; x += 32) {
-                    const uint32_t u = list[x];
-                    if ((u & pm) == prefix) atomicAdd(&s_hist[(u >> sh) & dm], 1u);
-                }
-                __syncwarp();
-                uint32_t dg;
-                find_bin(s_hist, krem, dg, eq_count);
-                prefix |= dg << sh;
-                top = sh;
-            }
-            uk = prefix;
-            need_eq = krem;
+    if (var.sample) {
+        // sampled selection: the pool of the top `pool` candidates by Z,
+        // then the top k of Z / temperature + Gumbel noise within the pool
+        uint32_t uk, eq_cut;
+        if (var.pool < C) {
+            kth_largest(keys, list, C, var.pool, zmin, zmax, sh, uk, eq_cut);
+            take_top<true>(keys, C, uk, eq_cut, var.pool, nullptr, sh);
         }
-        if (lane == 0) {
-            s_uk = uk;
-            s_eq = eq_count;
-            s_need = need_eq;
+        zmin = INFINITY;
+        zmax = -INFINITY;
+        const float* up = var.unif + p * var.ld_u;
+        for (int i = tid; i < C; i += kThreads) {
+            const uint32_t u = keys[i];
+            if (u == 0u) continue;  // outside the pool
+            const float g = -logf(-logf(up[i]));
+            const float key = __fadd_rn(__fmul_rn(from_orderable(u), var.inv_temp), g);
+            keys[i] = orderable(key);
+            if (isfinite(key)) {
+                zmin = fminf(zmin, key);
+                zmax = fmaxf(zmax, key);
+            }
         }
+        __syncthreads();
     }
-    __syncthreads();
-    const uint32_t uk = s_uk;
-    const uint32_t eq_cut = s_eq - s_need;  // equal keys of rank >= eq_cut are kept
-    // kept candidates in index order: contiguous ranges per thread, block scans
-    const int ipt = (C + kThreads - 1) / kThreads;
-    const int lo = min(C, tid * ipt), hi = min(C, lo + ipt);
-    int eq_before = 0;
-    if (eq_cut > 0) {
-        int n_eq = 0;
-        for (int i = lo; i < hi; ++i) n_eq += (keys[i] == uk);
-        int eq_total;
-        eq_before = block_scan(n_eq, s_warp, &eq_total);
-    }
-    int n_keep = 0;
     {
-        int e = eq_before;
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t u = keys[i];
-            if (u > uk) ++n_keep;
-            else if (u == uk) { n_keep += (e >= (int)eq_cut); ++e; }
-        }
-    }
-    int keep_total;
-    int pos = block_scan(n_keep, s_warp, &keep_total);
-    if (k > 0) {
-        int e = eq_before;
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t u = keys[i];
-            bool keep = false;
-            if (u > uk) keep = true;
-            else if (u == uk) { keep = (e >= (int)eq_cut); ++e; }
-            if (keep && pos < k) sidx[pos++] = i;
-        }
+        uint32_t uk, eq_cut;
+        kth_largest(keys, list, C, k > 0 ? k : 1, zmin, zmax, sh, uk, eq_cut);
+        if (k > 0) take_top<false>(keys, C, uk, eq_cut, k, sidx, sh);
     }
     for (int r = tid; r < n_obs; r += kThreads) sidx[k + r] = C + r;
     __syncthreads();

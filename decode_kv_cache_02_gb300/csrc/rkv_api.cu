@@ -154,9 +154,17 @@ bool partial_overlap(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-// A variant's fields; *active = whether it changes anything.
-int check_variant(const rkv_variant* v, bool* active) {
-    *active = false;
+// What a variant asks for: zvar = Z formed from I and R (softmax, pooling,
+// sentences); sched = a recent window / sampled selection.
+struct VarFlags {
+    bool zvar = false;
+    bool sched = false;
+    bool any() const { return zvar || sched; }
+};
+
+// A variant's fields (sizes that depend on the call: check_variant_sizes).
+int check_variant(const rkv_variant* v, VarFlags* f) {
+    *f = VarFlags{};
     if (!v) return RKV_OK;
     if (v->redundancy_softmax != 0 && v->redundancy_softmax != 1) return RKV_ERR_INVALID_ARG;
     if (v->pool_window < 1 || v->pool_window > RKV_MAX_POOL_WINDOW || (v->pool_window & 1) == 0)
@@ -170,13 +178,44 @@ int check_variant(const rkv_variant* v, bool* active) {
             return RKV_ERR_INVALID_ARG;
         if (t->num_seqs * (int64_t)t->max_sentences >= ((int64_t)1 << 31)) return RKV_ERR_INVALID_ARG;
     }
-    *active = v->redundancy_softmax != 0 || v->pool_window > 1 || v->sentences != nullptr;
+    if (const rkv_schedule* c = v->schedule) {
+        if (c->recent_window < 1 || c->pool_size < 0 || c->ld_uniforms < 0 ||
+            !(c->temperature > 0.f) || !(c->temperature < INFINITY))
+            return RKV_ERR_INVALID_ARG;
+    }
+    f->zvar = v->redundancy_softmax != 0 || v->pool_window > 1 || v->sentences != nullptr;
+    f->sched = v->schedule != nullptr;
     return RKV_OK;
 }
 
-// The variant's sentence rows must cover the cached rows.
-int check_variant_rows(const rkv_variant* v, int n_cached) {
-    return (v && v->sentences && v->sentences->ld_seg < n_cached) ? RKV_ERR_INVALID_ARG : RKV_OK;
+// Rows that are always kept: the schedule's window, else the observation tokens.
+int tail_rows(const rkv_variant* v, int n_obs) {
+    return (v && v->schedule) ? v->schedule->recent_window : n_obs;
+}
+
+// Whether the call samples (a pool larger than the number kept).
+bool samples(const rkv_variant* v, int n_cached, int budget) {
+    if (!v || !v->schedule || n_cached <= budget) return false;
+    return v->schedule->pool_size > budget - v->schedule->recent_window;
+}
+
+// The variant's sizes against the call: sentence rows cover the cached rows;
+// the window holds the observation tokens and leaves candidates; with a budget
+// (budget > 0), k <= pool <= C and uniforms for a sampled pool.
+int check_variant_sizes(const rkv_variant* v, int n_cached, int n_obs, int budget) {
+    if (!v) return RKV_OK;
+    if (v->sentences && v->sentences->ld_seg < n_cached) return RKV_ERR_INVALID_ARG;
+    if (const rkv_schedule* c = v->schedule) {
+        const int L = c->recent_window;
+        if (L < n_obs || L >= n_cached) return RKV_ERR_INVALID_ARG;
+        if (budget > 0) {
+            if (L > budget) return RKV_ERR_INVALID_ARG;
+            const int k = budget - L, C = n_cached - L;
+            if (c->pool_size < k || c->pool_size > C) return RKV_ERR_INVALID_ARG;
+            if (c->pool_size > k && (!c->uniforms || c->ld_uniforms < C)) return RKV_ERR_INVALID_ARG;
+        }
+    }
+    return RKV_OK;
 }
 
 int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
@@ -250,9 +289,20 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
-// The device-side form of a variant, reading the base I and R rows of w.
-rkv::VariantIn variant_in(const rkv_variant& v, float lambda, const Workspace& w) {
+// The device-side form of a variant: with zvar Z is formed from the base I
+// and R rows of w; a sampled schedule adds the pool and the uniforms.
+rkv::VariantIn variant_in(const rkv_variant& v, const VarFlags& f, float lambda,
+                          const Workspace& w, bool sample) {
     rkv::VariantIn vin;
+    if (sample) {
+        const rkv_schedule* c = v.schedule;
+        vin.sample = true;
+        vin.pool = c->pool_size;
+        vin.inv_temp = 1.0f / c->temperature;
+        vin.unif = c->uniforms;
+        vin.ld_u = c->ld_uniforms;
+    }
+    if (!f.zvar) return vin;
     vin.I = w.I;
     vin.R = w.R;
     vin.ld = w.ld;
@@ -290,9 +340,12 @@ int run_scores_variant(const rkv_desc* d, const void* K, const void* Q, int n_ca
     if (launch_penalty(&v, s) != cudaSuccess) return RKV_ERR_CUDA;
     int rc = run_scores(d, K, Q, n_cached, n_obs, lambda, beta, tau, w.I, w.R, w.Z, w.ld, w, s);
     if (rc) return rc;
-    const rkv::VariantIn vin = variant_in(v, lambda, w);
+    VarFlags f;
+    f.zvar = true;  // the variant kernel always forms Z from I and R
+    const rkv::VariantIn vin = variant_in(v, f, lambda, w, false);
+    const int tail = tail_rows(&v, n_obs);
     cudaError_t e = timed(kVariant, s, [&] {
-        return rkv::launch_variant(d->num_problems, n_cached, n_obs, vin, Z, I_out, R_out, ld_out,
+        return rkv::launch_variant(d->num_problems, n_cached, tail, vin, Z, I_out, R_out, ld_out,
                                    s);
     });
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
@@ -312,18 +365,18 @@ int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_c
                  int n_obs, float lambda, int beta, float tau, const rkv_variant* variant,
                  float* out_I, float* out_R, float* out_Z, void* workspace,
                  size_t workspace_bytes, void* stream) {
-    bool var_on = false;
-    int rc = check_variant(variant, &var_on);
+    VarFlags vf;
+    int rc = check_variant(variant, &vf);
     if (rc) return rc;
     rc = check_scores(desc, K, Q_obs, n_cached, n_obs, workspace, workspace_bytes);
     if (rc) return rc;
     if (beta < 0) return RKV_ERR_INVALID_ARG;
     if (desc->num_problems == 0) return RKV_OK;
     if (!out_I || !out_R || !out_Z) return RKV_ERR_INVALID_ARG;
-    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
+    if (check_variant_sizes(variant, n_cached, n_obs, 0)) return RKV_ERR_INVALID_ARG;
     const Workspace w = carve(workspace, desc->num_problems, n_cached);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (var_on)
+    if (vf.zvar || tail_rows(variant, n_obs) > n_obs)
         return run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
                                   out_I, out_R, out_Z, n_cached, w, s);
     return run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, out_I, out_R, out_Z,
@@ -349,8 +402,8 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
                     int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                     const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    bool var_on = false;
-    int rc = check_variant(variant, &var_on);
+    VarFlags vf;
+    int rc = check_variant(variant, &vf);
     if (rc) return rc;
     rc = check_desc(desc);
     if (rc) return rc;
@@ -395,33 +448,36 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
     rc = check_scores(desc, K, Q_obs, n_cached, n_obs, workspace, workspace_bytes);
     if (rc) return rc;
     if (P == 0) return RKV_OK;
-    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
+    if (check_variant_sizes(variant, n_cached, n_obs, budget)) return RKV_ERR_INVALID_ARG;
     const Workspace w = carve(workspace, P, n_cached);
-    const bool fused = rkv::compact_smem_bytes(n_cached, n_obs, budget,
-                                               var_on && variant->sentences) <= kCompactSmemMax;
-    if (var_on && !fused) {
+    const int tail = tail_rows(variant, n_obs);
+    const bool sample = samples(variant, n_cached, budget);
+    const bool fused = rkv::compact_smem_bytes(n_cached, tail, budget,
+                                               vf.zvar && variant->sentences) <= kCompactSmemMax;
+    if (sample && !fused) return RKV_ERR_UNSUPPORTED;
+    if (!fused && (vf.zvar || tail > n_obs)) {
         rc = run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
                                 nullptr, nullptr, w.Z, w.ld, w, s);
     } else {
-        if (var_on && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
+        if (vf.zvar && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
         rc = run_scores(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
-                        var_on ? w.R : nullptr, w.Z, w.ld, w, s);
+                        vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s);
     }
     if (rc) return rc;
     cudaError_t e;
     if (fused) {
         // selection and compaction in one pass per problem (a variant's Z is
-        // formed there from I and R)
+        // formed there from I and R; a schedule's window is the kept tail)
         rkv::VariantIn vin;
-        if (var_on) vin = variant_in(*variant, lambda, w);
+        if (vf.any()) vin = variant_in(*variant, vf, lambda, w, sample);
         e = timed(kCompact, s, [&] {
-            return rkv::launch_compact(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, K, V, out_K,
+            return rkv::launch_compact(P, n_cached, w.Z, w.ld, tail, budget, out_idx, K, V, out_K,
                                        out_V, desc->n_capacity, row_bytes, in_place, w.status, s,
                                        vin);
         });
     } else {
         e = timed(kSelect, s, [&] {
-            return rkv::launch_select(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.status, s);
+            return rkv::launch_select(P, n_cached, w.Z, w.ld, tail, budget, out_idx, w.status, s);
         });
         if (e == cudaSuccess)
             e = timed(kGather, s, [&] {
@@ -497,8 +553,8 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
                        int n_obs, float lambda, int beta, float tau,
                        const rkv_variant* variant, int32_t* out_idx, int32_t* out_freed,
                        void* workspace, size_t workspace_bytes, void* stream) {
-    bool var_on = false;
-    int rc = check_variant(variant, &var_on);
+    VarFlags vf;
+    int rc = check_variant(variant, &vf);
     if (rc) return rc;
     rkv_desc flat{};
     rc = check_paged_desc(desc, &flat);
@@ -533,12 +589,13 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0) return RKV_ERR_WORKSPACE;
     if (n_cached < 2 || n_obs >= n_cached) return RKV_ERR_INVALID_ARG;
     if (flat.gqa_group * n_obs > 128) return RKV_ERR_UNSUPPORTED;
-    if (rkv::compact_smem_bytes(n_cached, n_obs, budget, var_on && variant->sentences) >
+    const int tail = tail_rows(variant, n_obs);
+    if (rkv::compact_smem_bytes(n_cached, tail, budget, vf.zvar && variant->sentences) >
         kCompactSmemMax)
         return RKV_ERR_UNSUPPORTED;
     const size_t kc = kc_bytes_for(flat, n_cached);
     if (workspace_bytes < carve(nullptr, P, n_cached, kc).bytes) return RKV_ERR_WORKSPACE;
-    if (check_variant_rows(variant, n_cached)) return RKV_ERR_INVALID_ARG;
+    if (check_variant_sizes(variant, n_cached, n_obs, budget)) return RKV_ERR_INVALID_ARG;
     if (P == 0) return RKV_OK;
     const Workspace w = carve(workspace, P, n_cached, kc);
     rkv::PagedIn pg;
@@ -547,15 +604,15 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     pg.log2bs = log2_exact(desc->block_size);
     pg.H = desc->num_kv_heads;
     pg.num_blocks = desc->num_blocks;
-    if (var_on && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
+    if (vf.zvar && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
     rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
-                    var_on ? w.R : nullptr, w.Z, w.ld, w, s, &pg);
+                    vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg);
     if (rc) return rc;
     rkv::VariantIn vin;
-    if (var_on) vin = variant_in(*variant, lambda, w);
+    if (vf.any()) vin = variant_in(*variant, vf, lambda, w, samples(variant, n_cached, budget));
     const int row_bytes = desc->head_dim * (int)es;
     cudaError_t e = timed(kCompactPaged, s, [&] {
-        return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, n_obs, budget, out_idx, w.Kc,
+        return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, tail, budget, out_idx, w.Kc,
                                          K_pool, V_pool, pg, row_bytes, w.status, s, vin);
     });
     if (e == cudaSuccess && n_free > 0)
@@ -569,9 +626,9 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
 
 int rkv_sentence_penalty(const rkv_sentences* sent, void* stream) {
     if (!sent) return RKV_ERR_INVALID_ARG;
-    rkv_variant v{0, 1, sent};
-    bool on = false;
-    int rc = check_variant(&v, &on);
+    rkv_variant v{0, 1, sent, nullptr};
+    VarFlags f;
+    int rc = check_variant(&v, &f);
     if (rc) return rc;
     return launch_penalty(&v, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RKV_OK
                                                                                : RKV_ERR_CUDA;

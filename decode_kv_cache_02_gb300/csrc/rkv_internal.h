@@ -82,6 +82,13 @@ struct VariantIn {
     int64_t num_seqs = 1;
     int heads = 1;
     int max_sent = 0;
+    // sampled selection: pool of the top `pool` candidates by Z, then the top
+    // k of Z * inv_temp - log(-log(u)) within it (u: unif rows, stride ld_u)
+    bool sample = false;
+    int pool = 0;
+    float inv_temp = 1.f;
+    const float* unif = nullptr;
+    int64_t ld_u = 0;
 };
 
 // Sentence penalties pen[s, a] = max_{b > a, cos(a, b) > tau} cos(a, b) from

@@ -54,9 +54,40 @@ class _Sentences(ctypes.Structure):
                 ("ld_seg", ctypes.c_int32), ("tau", ctypes.c_float)]
 
 
+class _Schedule(ctypes.Structure):
+    _fields_ = [("recent_window", ctypes.c_int32), ("pool_size", ctypes.c_int32),
+                ("temperature", ctypes.c_float), ("ld_uniforms", ctypes.c_int32),
+                ("uniforms", ctypes.c_void_p)]
+
+
 class _Variant(ctypes.Structure):
     _fields_ = [("redundancy_softmax", ctypes.c_int32), ("pool_window", ctypes.c_int32),
-                ("sentences", ctypes.POINTER(_Sentences))]
+                ("sentences", ctypes.POINTER(_Sentences)),
+                ("schedule", ctypes.POINTER(_Schedule))]
+
+
+class Schedule:
+    """ForesightKV-style schedule (rkv_schedule in include/rkv.h): keep the
+    newest recent_window rows, pool the top pool_size candidates by Z, draw
+    budget - recent_window of them without replacement with probabilities
+    proportional to exp(Z / temperature), using uniforms [P, >= C] fp32 in
+    [0, 1) (from a seeded generator).  pool_size = budget - recent_window:
+    deterministic top-k (uniforms may be None)."""
+
+    def __init__(self, recent_window: int, pool_size: int, temperature: float = 1.0,
+                 uniforms=None):
+        if uniforms is not None:
+            _cuda(uniforms, "uniforms")
+            if uniforms.dtype != torch.float32 or uniforms.dim() != 2:
+                raise ValueError("uniforms must be fp32 [P, >= C]")
+        self.recent_window, self.pool_size = int(recent_window), int(pool_size)
+        self.temperature, self.uniforms = float(temperature), uniforms
+
+    def _c(self) -> _Schedule:
+        u = self.uniforms
+        return _Schedule(self.recent_window, self.pool_size, self.temperature,
+                         u.shape[1] if u is not None else 0,
+                         u.data_ptr() if u is not None else None)
 
 
 class Sentences:
@@ -85,13 +116,15 @@ class Sentences:
                           self.tau)
 
 
-def _variant(redundancy_softmax: bool, pool_window: int, sentences):
-    """The C variant struct (and the sentence struct it points to, which the
-    caller keeps alive for the call)."""
+def _variant(redundancy_softmax: bool, pool_window: int, sentences, schedule=None):
+    """The C variant struct (and the structs it points to, which the caller
+    keeps alive for the call)."""
     sc = sentences._c() if sentences is not None else None
+    sh = schedule._c() if schedule is not None else None
     v = _Variant(1 if redundancy_softmax else 0, int(pool_window),
-                 ctypes.pointer(sc) if sc is not None else None)
-    return v, sc
+                 ctypes.pointer(sc) if sc is not None else None,
+                 ctypes.pointer(sh) if sh is not None else None)
+    return v, (sc, sh)
 
 
 class _PagedDesc(ctypes.Structure):
@@ -264,15 +297,17 @@ def rkv_compress(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: f
 
 def rkv_compress_ex(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8, lam: float = 0.1,
                     beta: int = 2, tau: float = 0.9, redundancy_softmax: bool = False,
-                    pool_window: int = 1, sentences: Sentences | None = None, out_K=None,
-                    out_V=None, out_idx=None, workspace=None, stream=None):
+                    pool_window: int = 1, sentences: Sentences | None = None,
+                    schedule: Schedule | None = None, out_K=None, out_V=None, out_idx=None,
+                    workspace=None, stream=None):
     """rkv_compress with a scoring variant: redundancy_softmax turns R into a
     softmax over the candidates, pool_window (odd) max-pools I over that many
     neighbouring positions, sentences adds the sentence-level penalty (and
-    compacts sentences.seg_id with the rows)."""
+    compacts sentences.seg_id with the rows), schedule keeps a recent window
+    and samples the kept candidates."""
     desc, out_K, out_V, out_idx, workspace = _compress_args(
         K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, workspace)
-    var, _keep = _variant(redundancy_softmax, pool_window, sentences)
+    var, _keep = _variant(redundancy_softmax, pool_window, sentences, schedule)
     rc = load().rkv_compress_ex(ctypes.byref(desc), K.data_ptr(), V.data_ptr(), Q_obs.data_ptr(),
                                 int(n_cached), int(budget), int(n_obs), float(lam), int(beta),
                                 float(tau), ctypes.byref(var), out_K.data_ptr(), out_V.data_ptr(),
@@ -340,10 +375,11 @@ def rkv_score(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: i
 
 def rkv_score_ex(K, Q_obs, n_cached: int, n_obs: int = 8, lam: float = 0.1, beta: int = 2,
                  tau: float = 0.9, redundancy_softmax: bool = False, pool_window: int = 1,
-                 sentences: Sentences | None = None, workspace=None, stream=None):
+                 sentences: Sentences | None = None, schedule: Schedule | None = None,
+                 workspace=None, stream=None):
     """(I', R', Z), each fp32 [P, n_cached], for a scoring variant (see
     rkv_compress_ex); I' and R' are the terms that enter Z."""
-    var, keep = _variant(redundancy_softmax, pool_window, sentences)
+    var, keep = _variant(redundancy_softmax, pool_window, sentences, schedule)
     return _score(K, Q_obs, n_cached, n_obs, lam, beta, tau, var, workspace, stream, keep)
 
 
@@ -433,8 +469,8 @@ def rkv_paged_freed_per_seq(K_pool, block_table, n_cached: int, budget: int) -> 
 def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget: int,
                        n_obs: int = 8, lam: float = 0.1, beta: int = 2, tau: float = 0.9,
                        redundancy_softmax: bool = False, pool_window: int = 1,
-                       sentences: Sentences | None = None, out_idx=None, out_freed=None,
-                       workspace=None, stream=None):
+                       sentences: Sentences | None = None, schedule: Schedule | None = None,
+                       out_idx=None, out_freed=None, workspace=None, stream=None):
     """One compression round of a paged cache, in place: K_pool, V_pool
     [num_blocks, H, block_size, d], Q_obs [S*H, G, n_obs, d], block_table
     [S, max_blocks] int32 (entries of freed blocks become -1).  Returns
@@ -465,7 +501,7 @@ def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget
     if out_idx.shape != (P, budget) or out_idx.dtype != torch.int32 \
             or out_freed.shape != (desc.num_seqs, n_free) or out_freed.dtype != torch.int32:
         raise ValueError("output shapes")
-    var, _keep = _variant(redundancy_softmax, pool_window, sentences)
+    var, _keep = _variant(redundancy_softmax, pool_window, sentences, schedule)
     rc = load().rkv_paged_compress(
         ctypes.byref(desc), K_pool.data_ptr(), V_pool.data_ptr(), Q_obs.data_ptr(),
         block_table.data_ptr(), int(n_cached), int(budget), int(n_obs), float(lam), int(beta),

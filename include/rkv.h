@@ -128,6 +128,10 @@ int rkv_score(const rkv_desc* desc, const void* K, const void* Q_obs, int n_cach
  *                       with |j - i| <= (w-1)/2 (the window is cut at the
  *                       candidates' ends).  1: no pooling.
  *   sentences           a sentence-level penalty (below), or NULL.
+ *   schedule            a recent window and sampled selection (below), or
+ *                       NULL.  With a schedule the L newest rows take the
+ *                       place of the observation tokens in everything that
+ *                       follows (they are not candidates; Z = +inf, R = 0).
  * Z_i = lambda*I'_i - (1-lambda)*R'_i - pen_i; observation tokens keep their
  * I, get R = 0 and Z = +inf as before.  A NULL variant is all off. */
 /* Sentence-level redundancy (the SkipKV review, yoonschallenge.tistory.com/
@@ -167,10 +171,36 @@ typedef struct {
 #define RKV_MAX_SENTENCES 65536
 #define RKV_MAX_HIDDEN 16384
 
+/* ForesightKV-style schedule and selection (the ForesightKV summary page,
+ * gist.science/ko/paper/2602.03203, section "Dynamic eviction process"):
+ * when the cache holds B + L rows the newest L are kept and the rest are
+ * compressed to B - L by the scores; the decision takes the top K and then
+ * samples (multinomial sampling) to add randomness.  The R-KV score Z stands
+ * in for the page's learned scorer.  Here:
+ *   - the newest L = recent_window rows (n_obs <= L <= budget) are kept like
+ *     the observation tokens (which still supply the importance queries);
+ *     the other C = n_cached - L rows are the candidates, k = budget - L of
+ *     them are kept;
+ *   - the pool is the top pool_size candidates by Z (ties to the newer);
+ *   - k of the pool are drawn without replacement with probabilities
+ *     proportional to exp(Z_i / temperature): exactly the k largest
+ *     Z_i / temperature + g_i over the pool, g_i = -log(-log(u_i)) (Gumbel
+ *     noise) from the caller's uniforms u [P, ld_uniforms] in [0, 1), so a
+ *     seeded generator on the caller's side makes the draw reproducible.
+ * pool_size == k is the deterministic top-k (uniforms may be NULL). */
+typedef struct {
+    int32_t recent_window;  /* L */
+    int32_t pool_size;      /* K, k <= K <= C */
+    float temperature;      /* > 0 */
+    int32_t ld_uniforms;    /* >= C when uniforms are given */
+    const float* uniforms;  /* [P, ld_uniforms]; needed when K > k */
+} rkv_schedule;
+
 typedef struct {
     int32_t redundancy_softmax;       /* 0 or 1 */
     int32_t pool_window;              /* odd, 1 .. RKV_MAX_POOL_WINDOW */
     const rkv_sentences* sentences;   /* NULL: no sentence-level penalty */
+    const rkv_schedule* schedule;     /* NULL: keep the n_obs newest, top-k */
 } rkv_variant;
 #define RKV_MAX_POOL_WINDOW 255
 

@@ -203,26 +203,76 @@ def gather(src: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return out
 
 
+def schedule_select(Z, n_tail: int, budget: int, pool_size: int, temperature: float = 1.0,
+                    uniforms=None) -> dict:
+    """The ForesightKV-style selection (readings R15-R16): the n_tail newest
+    rows are kept; of the C = N - n_tail candidates the pool is the top
+    pool_size by (Z, index); k = budget - n_tail of the pool are drawn without
+    replacement with probabilities proportional to exp(Z / temperature), as
+    the k largest (Z / temperature + g, index) with g = -log(-log u) from the
+    given uniforms.  pool_size == k is the plain top-k.  Returns dict(idx
+    [P, budget] ascending, pool [P, C] bool, keys [P, C] (sampling keys, -inf
+    outside the pool), z_pool [P] (the pool_size-th Z), key_k [P] (the k-th
+    key))."""
+    Z = _f64(Z)
+    P, N = Z.shape
+    C, k = N - n_tail, budget - n_tail
+    idx = np.empty((P, budget), dtype=np.int32)
+    pool = np.zeros((P, C), dtype=bool)
+    keys = np.full((P, C), -np.inf)
+    z_pool = np.zeros(P)
+    key_k = np.zeros(P)
+    for p in range(P):
+        order = sorted(range(C), key=lambda i: (Z[p, i], i), reverse=True)
+        members = order[:pool_size]
+        pool[p, members] = True
+        z_pool[p] = Z[p, members[-1]] if members else np.inf
+        if pool_size > k:
+            u = np.asarray(uniforms[p], dtype=np.float64)
+            with np.errstate(divide="ignore"):
+                for i in members:
+                    keys[p, i] = Z[p, i] / temperature - np.log(-np.log(u[i]))
+            chosen = sorted(members, key=lambda i: (keys[p, i], i), reverse=True)[:k]
+        else:
+            for i in members:
+                keys[p, i] = Z[p, i]
+            chosen = members[:k]
+        key_k[p] = keys[p, chosen[-1]] if chosen else np.inf
+        idx[p, :k] = sorted(chosen)
+        idx[p, k:] = np.arange(C, N)
+    return {"idx": idx, "pool": pool, "keys": keys, "z_pool": z_pool, "key_k": key_k}
+
+
 def compress(K, Q, n_cached: int, budget: int, n_obs: int, lam: float,
              beta: int, tau: float, nthreads: int | None = None,
              redundancy_softmax: bool = False, pool_window: int = 1,
-             row_penalty=None) -> dict:
+             row_penalty=None, recent_window: int | None = None,
+             pool_size: int | None = None, temperature: float = 1.0,
+             uniforms=None) -> dict:
     """Scores and selection of one compression round of P problems.
     K [P, n_cap, d] (rows >= n_cached ignored), Q [P, G, n_obs, d].  Returns
     dict(idx, scores); the kept rows themselves are ``gather(src, idx)``.
+    recent_window / pool_size / temperature / uniforms: the ForesightKV-style
+    schedule (``schedule_select``); the window's rows then take the place of
+    the observation tokens (Z = +inf, not candidates).
 
     n_cached <= budget is the identity (nothing evicted)."""
-    Kn = np.asarray(K.detach().cpu() if hasattr(K, "detach") else K)
-    P = Kn.shape[0]
+    P = K.shape[0]
     if n_cached <= budget:
         idx = np.tile(np.arange(budget, dtype=np.int32), (P, 1))
         idx[:, n_cached:] = -1
         sc = None
     else:
+        tail = n_obs if recent_window is None else recent_window
         sc = score(_f64(K)[:, :n_cached], Q, n_obs, lam, beta, tau, nthreads)
-        if redundancy_softmax or pool_window != 1 or row_penalty is not None:
-            sc = variant(sc, n_obs, lam, redundancy_softmax, pool_window, row_penalty)
-        idx = select(sc["Z"], n_obs, budget)
+        if redundancy_softmax or pool_window != 1 or row_penalty is not None or tail != n_obs:
+            sc = variant(sc, tail, lam, redundancy_softmax, pool_window, row_penalty)
+        if pool_size is not None and pool_size > budget - tail:
+            sel = schedule_select(sc["Z"], tail, budget, pool_size, temperature, uniforms)
+            sc = dict(sc, sampled=sel)
+            idx = sel["idx"]
+        else:
+            idx = select(sc["Z"], tail, budget)
     return {"idx": idx, "scores": sc}
 
 
@@ -253,7 +303,7 @@ def paged_rows(pool: np.ndarray, table: np.ndarray, n_rows: int) -> np.ndarray:
 def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: int,
                    lam: float, beta: int, tau: float, idx_used=None, nthreads=None,
                    redundancy_softmax: bool = False, pool_window: int = 1,
-                   row_penalty=None) -> dict:
+                   row_penalty=None, **schedule) -> dict:
     """One paged compression round.  K_pool / V_pool: raw arrays [num_blocks,
     H, bs, d] (any element type; rows move as they are); the keys are scored
     from ``K_f64`` = the float values of K_pool's logical rows.  Returns
@@ -270,7 +320,7 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
     if K_f.dtype == np.int16:  # bf16 bit patterns: widen exactly to float
         K_f = (K_f.astype(np.int32) << 16).view(np.float32)
     res = compress(K_f, Q, n_cached, budget, n_obs, lam, beta, tau, nthreads,
-                   redundancy_softmax, pool_window, row_penalty)
+                   redundancy_softmax, pool_window, row_penalty, **schedule)
     idx = res["idx"] if idx_used is None else np.asarray(idx_used)
     Kp, Vp, new_table = K_pool.copy(), V_pool.copy(), table.copy()
     freed = np.zeros((S, 0), dtype=np.int32)
@@ -303,6 +353,13 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
 # later sentences b with cos(a, b) > tau (strict), 0 if none; R13 it is
 # subtracted from Z of every candidate row of sentence a; R14 rows whose
 # sentence id is outside 0..count-1 carry no penalty.
+#
+# ForesightKV summary page (gist.science/ko/paper/2602.03203), section
+# "Dynamic eviction process" (schedule_select above): R15 the newest L rows
+# are kept like the observation tokens and the rest compete for B - L
+# places; R16 "top-K followed by multinomial sampling" is a pool of the top K
+# by score, from which the kept rows are drawn without replacement with
+# probabilities proportional to exp(score / temperature).
 
 
 def sentence_reps(hidden, token_seg, max_sentences: int) -> np.ndarray:

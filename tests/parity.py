@@ -93,3 +93,24 @@ def check_gathered(out: torch.Tensor, src: torch.Tensor, idx: torch.Tensor, budg
     o = out[ps].cpu()
     got = (o.view(torch.int16) if o.dtype == torch.bfloat16 else o.view(torch.int32)).numpy()
     np.testing.assert_array_equal(got[:, :budget], exp[:, :budget])
+
+
+def sampled_mismatches(idx_gpu: np.ndarray, sc: dict, sel: dict, budget: int, n_tail: int,
+                       temperature: float, band: float = KEPT_BAND) -> tuple[int, int]:
+    """(unexcused, excused) kept-set differences of a sampled selection
+    (oracle ``schedule_select`` result ``sel``, same uniforms).  Excused: a
+    token whose Z is within ``band`` of the pool's last Z (pool membership can
+    flip), whose sampling key is within band / temperature (+ 1e-5 for the
+    noise's fp32 rounding) of the k-th key, or a threshold-borderline token."""
+    k = budget - n_tail
+    bad = ok = 0
+    for p in range(idx_gpu.shape[0]):
+        diff = set(idx_gpu[p, :k].tolist()) ^ set(sel["idx"][p, :k].tolist())
+        for i in diff:
+            near_pool = abs(sc["Z"][p, i] - sel["z_pool"][p]) <= band
+            near_cut = abs(sel["keys"][p, i] - sel["key_k"][p]) <= band / temperature + 1e-5
+            if near_pool or near_cut or sc["border"][p, i]:
+                ok += 1
+            else:
+                bad += 1
+    return bad, ok

@@ -164,6 +164,28 @@ def test_sentence_argument_errors(lib):
     assert lib.rkv_sentence_reps(fake, fake, 2, 10, 4096, 5, 8, fake, None) == 2
 
 
+def test_schedule_argument_errors(lib):
+    """Schedule checks: window, pool bounds, uniforms for a sampled pool,
+    temperature."""
+    from decode_kv_cache_02_gb300 import rkv
+    d = _desc(P=16)
+    fake = 1 << 20
+
+    def call(L=128, K=896, T=1.0, u=fake + 2 ** 36, ld=1024, n_obs=8):
+        sch = rkv._Schedule(L, K, T, ld, u)
+        v = rkv._Variant(0, 1, None, ctypes.pointer(sch))
+        return lib.rkv_compress_ex(ctypes.byref(d), fake, fake + 2 ** 30, fake + 2 ** 31, 1152,
+                                   1024, n_obs, 0.1, 2, 0.9, ctypes.byref(v), fake + 2 ** 32,
+                                   fake + 2 ** 33, fake + 2 ** 34, fake + 2 ** 35, 1 << 40, None)
+    assert call(L=4) == 1            # window smaller than the observation tokens
+    assert call(L=1100) == 1         # window larger than the budget
+    assert call(K=800) == 1          # pool smaller than the number kept
+    assert call(K=1100) == 1         # pool larger than the candidates
+    assert call(K=900, u=None) == 1  # sampled pool without uniforms
+    assert call(K=900, ld=100) == 1  # uniform rows shorter than the candidates
+    assert call(T=0.0) == 1 and call(T=float("inf")) == 1
+
+
 def test_binding_rejects_cpu_tensors(lib):
     from decode_kv_cache_02_gb300 import rkv
     K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)

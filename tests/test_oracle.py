@@ -554,6 +554,71 @@ def test_redundant_earlier_sentence_goes_first():
     assert evicted == list(range(8, 16))
 
 
+# --------------------------------------------------------------- schedule --
+# ForesightKV summary page (gist.science/ko/paper/2602.03203), section
+# "Dynamic eviction process": readings R15-R16 of the oracle.
+
+def test_gumbel_top_k_is_multinomial_without_replacement():
+    """The sampled selection draws k of the pool with probabilities
+    proportional to exp(Z / T), one after another without replacement: the
+    frequencies of the kept pairs over 40,000 seeded draws match the exact
+    probabilities of sequential sampling (enumerated by hand, not via the
+    Gumbel route) within a chi-square bound."""
+    Z = np.array([[0.3, -0.2, 0.9, 0.1, 0.5, np.inf]])  # last row: the window
+    T, draws = 0.5, 40000
+    w = np.exp(Z[0, :5] / T)
+    pr = w / w.sum()
+    exact = {}
+    for a, b in itertools.permutations(range(5), 2):
+        key = tuple(sorted((a, b)))
+        exact[key] = exact.get(key, 0.0) + pr[a] * pr[b] / (1 - pr[a])
+    u = np.random.default_rng(21).random((draws, 5))
+    counts = {}
+    for t in range(draws):
+        sel = oracle.schedule_select(Z, 1, 3, 5, T, u[t:t + 1])
+        key = tuple(sel["idx"][0, :2].tolist())
+        counts[key] = counts.get(key, 0) + 1
+    chi2 = sum((counts.get(key, 0) - draws * p_) ** 2 / (draws * p_) for key, p_ in exact.items())
+    assert chi2 < 35.0, chi2  # 9 degrees of freedom: p ~ 1e-4
+    assert abs(sum(exact.values()) - 1.0) < 1e-12
+
+
+def test_schedule_pool_window_and_limits():
+    """Only pool members are ever kept; the window is always kept; a pool of
+    exactly k is the plain top-k; a tiny temperature gives the top-k of Z."""
+    rng = np.random.default_rng(4)
+    P, N, L, B = 6, 60, 10, 30
+    Z = rng.standard_normal((P, N))
+    u = rng.random((P, N))
+    k, C = B - L, N - L
+    s1 = oracle.schedule_select(Z, L, B, k + 12, 1.0, u)
+    for p in range(P):
+        kept = s1["idx"][p, :k]
+        assert s1["pool"][p, kept].all()
+        assert s1["pool"][p].sum() == k + 12
+        assert list(s1["idx"][p, k:]) == list(range(C, N))
+    np.testing.assert_array_equal(oracle.schedule_select(Z, L, B, k)["idx"],
+                                  oracle.select(Z, L, B))
+    np.testing.assert_array_equal(oracle.schedule_select(Z, L, B, C, 1e-9, u)["idx"],
+                                  oracle.select(Z, L, B))
+
+
+def test_compress_with_recent_window():
+    """With a window L > n_obs the L newest rows are kept and the importance
+    still comes from the n_obs observation queries (scores equal the plain
+    scores on the candidates)."""
+    w = wl.WORKLOADS[0]
+    K, V, Q = wl.make_inputs(w)
+    L = 16
+    res = oracle.compress(K, Q, w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau,
+                          recent_window=L)
+    base = oracle.score(K[:, :w.n_cached], Q, w.n_obs, w.lam, w.beta, w.tau)
+    C = w.n_cached - L
+    np.testing.assert_array_equal(res["scores"]["Z"][:, :C], base["Z"][:, :C])
+    assert np.all(np.isposinf(res["scores"]["Z"][:, C:]))
+    np.testing.assert_array_equal(res["idx"], oracle.select(base["Z"], L, w.budget))
+
+
 # ------------------------------------------------------------- invariants --
 
 def test_compress_invariants_tiny_and_identity():
