@@ -82,9 +82,11 @@ def test_llama_full_step_sampled(cuda_ok):
 
 
 def test_qwen_large_budget_sampled(cuda_ok):
+    """The 48-layer x 16-sequence x 8-head Qwen-14B step (N = 4224 -> 4096,
+    G = 5) in one call, oracle on 256 sampled problems."""
     w = wl.BY_NAME["qwen14b"]
     K, V, Q = wl.make_inputs(w, device=DEV)
-    problems = sorted(np.random.default_rng(1).choice(w.problems, 64, replace=False).tolist())
+    problems = sorted(np.random.default_rng(1).choice(w.problems, 256, replace=False).tolist())
     _full_check(w, K, V, Q, problems)
 
 
