@@ -43,10 +43,15 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "e756854d549ff789d165a66b10a6605ed7621c27bd23d87558afe54b8d43a031", 314486528 / 1024),
-        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329739008 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "0e195e5262769e197b8a0cad98677843c90d80e7d43bf5e88cfbc76f19f9e083", 324261888 / 1024),
-        "compact": ("k_compact.cu", "924b4134c31ad01bd24c4d198adc79e4302ddbef89325cbe6f37f3ce347f30f0", 1034703616 / 1024),
+        "key_stats": ("k_key_stats.cu", "ce17dc521018fad4a2d4bae5d959af39e5949c69e0c548e300f0fc0baa61c4bd", 314551296 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329625856 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "0e195e5262769e197b8a0cad98677843c90d80e7d43bf5e88cfbc76f19f9e083", 324306176 / 1024),
+        "compact": ("k_compact.cu", "77c9483fefe942a991c5cef30afe670c95ffbdc7cc07356e45ae6bfafc5f4b0a", 1035702016 / 1024),
+    },
+    # the paged round (bs 16, 8 heads per block), same problems
+    "llama8b_full_paged": {
+        "key_stats_paged": ("k_key_stats.cu", "ce17dc521018fad4a2d4bae5d959af39e5949c69e0c548e300f0fc0baa61c4bd", 572683776 / 1024),
+        "compact_paged": ("k_compact.cu", "77c9483fefe942a991c5cef30afe670c95ffbdc7cc07356e45ae6bfafc5f4b0a", 973886208 / 1024),
     },
 }
 
@@ -492,7 +497,8 @@ def run_paged(args, w):
     roof = {}
     for k, v in kernels.items():
         per = v["ms"] / v["launches"] * 1e-3
-        e = {"ms_per_launch": per * 1e3}
+        e = {"ms_per_launch": per * 1e3,
+             "traffic": measured_traffic(w.name + "_paged", k, P) if bs == 16 else None}
         if k in model:
             e["hbm_frac"] = model[k]["bytes"] / per / 1e9 / peaks["hbm_gbs"]
         if k == "gram_tc":
@@ -777,7 +783,10 @@ def main():
     args = ap.parse_args()
     w = wl.BY_NAME[args.workload]
     if args.problems:
-        w = w.scaled(layers=1, batch=1, kv_heads=args.problems)
+        # a scaled copy: sequences of the workload's heads where the count
+        # allows (blocks of a paged pool hold all heads of a sequence)
+        H = w.kv_heads if args.problems % w.kv_heads == 0 else 1
+        w = w.scaled(layers=1, batch=args.problems // H, kv_heads=H)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.sweep:
