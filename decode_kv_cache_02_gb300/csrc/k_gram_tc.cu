@@ -451,6 +451,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                                 uint32_t hits = 0;
                                 float rs = 0.f;  // the row's hits before inv_i
                                 if (!diag) {
+                                    // the hits first: the filter's bound is loose, and
+                                    // most chunks it passes hold no pair above tau
 #pragma unroll
                                     for (int e4 = 0; e4 < 8; ++e4) {
                                         const float4 w4 = iv4[e4];
@@ -459,18 +461,30 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                                         for (int u = 0; u < 4; ++u) {
                                             const int e = e4 * 4 + u;
                                             const float t = __uint_as_float(r[h][e]) * iv[u];
-                                            const bool hit = t > thr;
-                                            rs += hit ? t : 0.f;
-                                            hits |= hit ? (1u << e) : 0u;
-                                            // S_ij of the hits, in the registers of the raw values
-                                            r[h][e] = __float_as_uint(hit ? t * inv_i : 0.f);
+                                            hits |= (t > thr) ? (1u << e) : 0u;
                                         }
                                     }
-                                    // column side: lane L adds column jb+L over the warp's rows
-                                    const float cs = warp_column_sums_bits(r[h], lane);
-                                    if (cs != 0.f)
-                                        atomicAdd(&s_sim[jb + lane], __float2int_rn(cs * kSimScale));
-                                    newer += __popc(hits);  // every column is newer
+                                    if (__any_sync(0xffffffffu, hits != 0u)) {
+#pragma unroll
+                                        for (int e4 = 0; e4 < 8; ++e4) {
+                                            const float4 w4 = iv4[e4];
+                                            const float iv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                            for (int u = 0; u < 4; ++u) {
+                                                const int e = e4 * 4 + u;
+                                                const float t = __uint_as_float(r[h][e]) * iv[u];
+                                                const bool hit = (hits >> e) & 1u;
+                                                rs += hit ? t : 0.f;
+                                                // S_ij of the hits, in the registers of the raw values
+                                                r[h][e] = __float_as_uint(hit ? t * inv_i : 0.f);
+                                            }
+                                        }
+                                        // column side: lane L adds column jb+L over the warp's rows
+                                        const float cs = warp_column_sums_bits(r[h], lane);
+                                        if (cs != 0.f)
+                                            atomicAdd(&s_sim[jb + lane], __float2int_rn(cs * kSimScale));
+                                        newer += __popc(hits);  // every column is newer
+                                    }
                                 } else if (self_chunk) {
 #pragma unroll
                                     for (int e4 = 0; e4 < 8; ++e4) {
