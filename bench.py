@@ -45,7 +45,7 @@ NCU_TRAFFIC = {
     "llama8b_full": {
         "key_stats": ("k_key_stats.cu", "ce17dc521018fad4a2d4bae5d959af39e5949c69e0c548e300f0fc0baa61c4bd", 314551296 / 1024),
         "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329625856 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "896acbd52c4277b6080ed314e22cfef68c87f535936976e63f268c421f50c7a2", 324306176 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "0e195e5262769e197b8a0cad98677843c90d80e7d43bf5e88cfbc76f19f9e083", 324306176 / 1024),
         "compact": ("k_compact.cu", "77c9483fefe942a991c5cef30afe670c95ffbdc7cc07356e45ae6bfafc5f4b0a", 1035702016 / 1024),
     },
     # the paged round (bs 16, 8 heads per block), same problems
