@@ -382,7 +382,8 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
 
     // ------------------------------------------------------------ copy --
     if constexpr (kPaged) {
-        // a_src: contiguous K copy [P, N, vpr]; a_dst: K pool; b_dst: V pool
+        // a_src: contiguous K copy [P, N, vpr], or null when K moves inside
+        // its pool like V; a_dst: K pool; b_dst: V pool
         int l = 0, h = budget;
         while (l < h) {
             const int mid = (l + h) >> 1;
@@ -405,7 +406,7 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
                     const int64_t sr = (s >= 0 && s < N) ? paged_phys_row(pg, p, s) : -1;
                     if (dr >= 0 && sr >= 0) {
                         dst[t] = dr * vpr + v;
-                        va[t] = a_src[kc_base + (int64_t)s * vpr + v];
+                        va[t] = a_src ? a_src[kc_base + (int64_t)s * vpr + v] : a_dst[sr * vpr + v];
                         vb[t] = b_dst[sr * vpr + v];
                     } else if (v == 0) {
                         set_error(st, kDevErrIndex, (unsigned)r);

@@ -116,6 +116,7 @@ struct Params {
     float* Z;
     int64_t ld_out;
     DeviceStatus* status;
+    KeySource ks;  // contiguous keys, or the paged pool read through the table
 };
 
 constexpr uint32_t kIdesc = idesc_bf16(kRows, kRows);
@@ -257,9 +258,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                     if (!(ok = mbar_wait(&a_empty[sa], ((ka / C::kAStages) & 1) ^ 1, s_abort)))
                         break;
                     mbar_arrive_expect_tx(&a_full[sa], C::kBlockBytes);
-                    for (int c = 0; c < C::KC; ++c)
-                        tma_load_3d(sA + sa * C::kBlockBytes + c * kChunkBytes, &tmap, &a_full[sa],
-                                    c * kChunkElems, I * kRows, (int)p);
+                    load_key_rows(sA + sa * C::kBlockBytes, kChunkBytes, C::KC, &tmap, &a_full[sa], p,
+                                  I * kRows, kRows, prm.ks);
                     ++ka;
                     // the column blocks of the row's tiles: J > I one at a time (the
                     // diagonal tile reuses block I), or W at a time from J = I
@@ -268,9 +268,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                         if (!(ok = mbar_wait(&b_empty[sb], ((kb / C::kBStages) & 1) ^ 1, s_abort)))
                             break;
                         mbar_arrive_expect_tx(&b_full[sb], C::kBStageBytes);
-                        for (int c = 0; c < C::KC; ++c)
-                            tma_load_3d(sB + sb * C::kBStageBytes + c * C::kBChunkBytes, &bmap,
-                                        &b_full[sb], c * kChunkElems, J * kRows, (int)p);
+                        load_key_rows(sB + sb * C::kBStageBytes, C::kBChunkBytes, C::KC, &bmap,
+                                      &b_full[sb], p, J * kRows, W * kRows, prm.ks);
                         ++kb;
                     }
                     if (ok && I == 0 && p + gridDim.x < prm.P) {
@@ -620,12 +619,13 @@ template <int D, int MB, int W>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D, MB, W>;
     CUtensorMap map, bmap;
-    if (!make_map_3d_bf16(&map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
-        return cudaErrorInvalidValue;
-    if (!make_map_3d_bf16(&bmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, W * kRows))
+    KeySource ks;
+    if (!make_key_map(&map, a, D, kRows, &ks)) return cudaErrorInvalidValue;
+    if (!make_key_map(&bmap, a, D, W * kRows, &ks))
         return cudaErrorInvalidValue;
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,
                a.sum_s,  a.ld_ws, a.I,       a.R,    a.Z,      a.ld_out, a.status};
+    prm.ks = ks;
     auto kern = gram_tc_kernel<D, MB, W>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);

@@ -77,6 +77,7 @@ struct IParams {
     float* sum_s;
     int64_t ld_ws;
     DeviceStatus* status;
+    KeySource ks;  // contiguous keys, or the paged pool read through the table
     // bit c of colmask[k]: query row c exists and its query index c % n_obs
     // is >= k (so it sees a key k positions past N - n_obs); bit c of
     // lastmask: c is the last query row of its head.
@@ -170,9 +171,8 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort)))
                             break;
                         mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
-                        for (int c = 0; c < C::KC; ++c)
-                            tma_load_3d(sK + s * C::kBlockBytes + c * kChunkBytes, &kmap, &k_full[s],
-                                        c * kChunkElems, b * kRows, (int)p);
+                        load_key_rows(sK + s * C::kBlockBytes, kChunkBytes, C::KC, &kmap, &k_full[s],
+                                      p, b * kRows, kRows, prm.ks);
                         ++kk;
                     }
                 }
@@ -638,9 +638,8 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                     const int s = kk % C::kStages;
                     if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort))) break;
                     mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
-                    for (int c = 0; c < C::KC; ++c)
-                        tma_load_3d(sK + s * C::kBlockBytes + c * kChunkBytes, &kmap, &k_full[s],
-                                    c * kChunkElems, b * kRows, (int)p);
+                    load_key_rows(sK + s * C::kBlockBytes, kChunkBytes, C::KC, &kmap, &k_full[s], p,
+                                  b * kRows, kRows, prm.ks);
                     ++kk;
                 }
             }
@@ -952,8 +951,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     const int64_t grid = a.P < cap ? a.P : cap;
     const int T = (a.N + kRows - 1) / kRows;
     CUtensorMap kmap, qmap, smap;
-    if (!make_map_3d_bf16(&kmap, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, kRows))
-        return cudaErrorInvalidValue;
+    if (!make_key_map(&kmap, a, D, kRows, &prm.ks)) return cudaErrorInvalidValue;
     if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
         return cudaErrorInvalidValue;
     const int SC = R <= 32 ? 32 : 48;

@@ -19,10 +19,12 @@
 // |khat_i|^2 into sum_i and s as bf16 rows (hi, lo) that the importance MMA
 // multiplies with every key block anyway, which completes sum_i there.
 //
-// Paged input (kPaged): rows are found through the block table, and pass 1
-// also stores every row, bit for bit, into the contiguous copy Kc [P, N, d]
-// that the tensor-core stages then read (their TMA tiles rely on rows past N
-// reading as zero, which only the contiguous copy gives).
+// Paged input (key_stats_paged_kernel): rows are found through the block
+// table.  The rows past N in the problem's last block (stale space the
+// sequence has not filled) are set to zero, so that tiles read straight from
+// the pool see zeros past N as the contiguous tensor map's bounds give; when
+// the tensor-core stages do not read the pool (small blocks, fp32), pass 1 also
+// stores every row, bit for bit, into the contiguous copy Kc [P, N, d].
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 #include "rkv_paged.cuh"
@@ -63,19 +65,17 @@ struct Raw8 {
     RKV_DEV void to_float(float* o) const { load8(reinterpret_cast<const T*>(u), o); }
 };
 
-template <typename T, int D, bool kPaged>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
                  float* __restrict__ sum_s, int64_t ld, bool two_pass,
-                 __nv_bfloat16* __restrict__ s_rows, PagedIn pg, T* __restrict__ Kc,
-                 DeviceStatus* st) {
+                 __nv_bfloat16* __restrict__ s_rows) {
     constexpr int L = D / 8;                 // lanes per row
     constexpr int RPI = kThreads / L;        // rows per iteration of the CTA
     __shared__ float s_part[RPI][D];
     __shared__ float s_vec[D];
     const int64_t p = blockIdx.x;
     const T* Kp = K + (size_t)p * n_cap * D;
-    T* Kcp = kPaged ? Kc + (size_t)p * N * D : nullptr;
     const int sub = threadIdx.x % L;         // which 8 columns
     const int r0 = threadIdx.x / L;          // first row of this thread
     const int col = sub * 8;
@@ -86,7 +86,153 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
     // ---- pass 1: norms and the partial sums of khat
     for (int base = r0; base < N; base += RPI * kUnroll) {
         float v[kUnroll][8];
-        if constexpr (kPaged) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            if (i < N) {
+                load8(Kp + (size_t)i * D + col, v[u]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            float n2 = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) n2 = fmaf(v[u][t], v[u][t], n2);
+            n2 = group_sum<L>(n2);
+            const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
+            if (i < N) {
+                if (sub == 0) {
+                    inv_norm[p * ld + i] = inv;
+                    // |khat_i|^2, completed to sum_i by the importance kernel
+                    if (!two_pass) sum_s[p * ld + i] = (n2 * inv) * inv;
+                }
+#pragma unroll
+                for (int t = 0; t < 8; ++t) acc[t] = fmaf(v[u][t], inv, acc[t]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s_part[r0][col + t] = acc[t];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kThreads) {
+        float s = 0.f;
+#pragma unroll 8
+        for (int w = 0; w < RPI; ++w) s += s_part[w][c];
+        s_vec[c] = s;
+        if (!two_pass) {
+            // s as two bf16 rows (s ~= hi + lo to 2^-16), then 14 zero rows:
+            // extra B rows of the importance MMA, which then yields k_i . s
+            __nv_bfloat16* sr = s_rows + (size_t)p * kSRows * D;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(s);
+            sr[c] = hi;
+            sr[D + c] = __float2bfloat16_rn(s - __bfloat162float(hi));
+            for (int r = 2; r < kSRows; ++r) sr[r * D + c] = __float2bfloat16_rn(0.f);
+        }
+    }
+    if (!two_pass) return;
+    __syncthreads();
+    float sv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sv[t] = s_vec[col + t];
+    const T* Kp2 = Kp;
+    // ---- pass 2: sum_i = khat_i . s - |khat_i|^2
+    for (int base = r0; base < N; base += RPI * kUnroll) {
+        float v[kUnroll][8];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            if (i < N) {
+                load8(Kp2 + (size_t)i * D + col, v[u]);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = base + u * RPI;
+            float n2 = 0.f, ds = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                n2 = fmaf(v[u][t], v[u][t], n2);
+                ds = fmaf(v[u][t], sv[t], ds);
+            }
+            n2 = group_sum<L>(n2);
+            ds = group_sum<L>(ds);
+            const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
+            if (i < N && sub == 0) sum_s[p * ld + i] = ds * inv - (n2 * inv) * inv;
+        }
+    }
+}
+
+// The same statistics of paged keys: rows through the block table (the
+// sequence's ids staged in shared memory), the stale rows past N in the last
+// block zeroed.  kMode 1 also stores every row into the contiguous copy Kc;
+// kMode 2 reads in place.  Four CTAs per SM keep enough rows in flight, except
+// for the copying fp32 variant, which would spill there.
+template <typename T, int D, int kMode>
+__global__ void __launch_bounds__(kThreads, (kMode == 1 && sizeof(T) == 4) ? 2 : 4)
+key_stats_paged_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
+                 float* __restrict__ sum_s, int64_t ld, bool two_pass,
+                 __nv_bfloat16* __restrict__ s_rows, PagedIn pg, T* __restrict__ Kc,
+                 DeviceStatus* st) {
+    constexpr int L = D / 8;                 // lanes per row
+    constexpr int RPI = kThreads / L;        // rows per iteration of the CTA
+    __shared__ float s_part[RPI][D];
+    __shared__ float s_vec[D];
+    constexpr bool kPaged = kMode != 0;
+    const int64_t p = blockIdx.x;
+    const T* Kp = K + (size_t)p * n_cap * D;
+    T* Kcp = kMode == 1 ? Kc + (size_t)p * N * D : nullptr;
+    // paged: the sequence's block ids in shared memory (-1 for an id outside
+    // the pool), so that a row's address needs no global load
+    extern __shared__ int32_t s_tab[];
+    int64_t head_base = 0;
+    if constexpr (kPaged) {
+        const int nbk = (N + (1 << pg.log2bs) - 1) >> pg.log2bs;
+        const int64_t sq = p / pg.H;
+        head_base = p - sq * pg.H;
+        for (int b = threadIdx.x; b < nbk; b += kThreads) {
+            const int v = pg.table[sq * pg.max_blocks + b];
+            s_tab[b] = (unsigned)v < (unsigned)pg.num_blocks ? v : -1;
+        }
+        __syncthreads();
+    }
+    auto phys_row = [&](int r) -> int64_t {  // paged row index in the pool, or -1
+        const int blk = s_tab[r >> pg.log2bs];
+        return blk < 0 ? -1
+                       : (((int64_t)blk * pg.H + head_base) << pg.log2bs) |
+                             (int64_t)(r & ((1 << pg.log2bs) - 1));
+    };
+    if constexpr (kPaged) {
+        // zero the stale rows after N in the last block (this head's tile only)
+        const int bs = 1 << pg.log2bs;
+        const int tail_end = (N + bs - 1) / bs * bs;
+        for (int e = threadIdx.x; e < (tail_end - N) * L; e += kThreads) {
+            const int r = N + e / L, c8 = (e % L) * 8;
+            const int64_t pr = phys_row(r);
+            if (pr >= 0) {
+                Raw8<T> z{};
+                z.store(const_cast<T*>(K) + pr * D + c8);
+            }
+        }
+    }
+    const int sub = threadIdx.x % L;         // which 8 columns
+    const int r0 = threadIdx.x / L;          // first row of this thread
+    const int col = sub * 8;
+
+    float acc[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+    // ---- pass 1: norms and the partial sums of khat
+    for (int base = r0; base < N; base += RPI * kUnroll) {
+        float v[kUnroll][8];
+        if constexpr (kMode == 1) {
+            // rows through the table, each also stored into the contiguous copy
             Raw8<T> raw[kUnroll];
             bool ok[kUnroll];
 #pragma unroll
@@ -94,7 +240,7 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
                 const int i = base + u * RPI;
                 ok[u] = false;
                 if (i < N) {
-                    const int64_t pr = paged_phys_row(pg, p, i);
+                    const int64_t pr = phys_row(i);
                     if (pr >= 0) {
                         raw[u].load(K + pr * D + col);
                         ok[u] = true;
@@ -115,6 +261,33 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
                         Raw8<T> z{};
                         z.store(Kcp + (size_t)(base + u * RPI) * D + col);
                     }
+                }
+            }
+        } else if constexpr (kMode == 2) {
+            // paged rows read in place: every row's load issued before any is used
+            Raw8<T> raw[kUnroll];
+            bool ok[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i = base + u * RPI;
+                ok[u] = false;
+                if (i < N) {
+                    const int64_t pr = phys_row(i);
+                    if (pr >= 0) {
+                        raw[u].load(K + pr * D + col);
+                        ok[u] = true;
+                    } else if (sub == 0) {
+                        set_error(st, kDevErrIndex, (unsigned)i);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                if (ok[u]) {
+                    raw[u].to_float(v[u]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
                 }
             }
         } else {
@@ -173,6 +346,8 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
     for (int t = 0; t < 8; ++t) sv[t] = s_vec[col + t];
     // the paged rows are re-read from the contiguous copy (written above by
     // this CTA; the barrier makes them visible)
+    // (the paged two-pass case always has the contiguous copy: only the
+    // CUDA-core importance, which reads contiguous keys, asks for pass 2)
     const T* Kp2 = kPaged ? Kcp : Kp;
     // ---- pass 2: sum_i = khat_i . s - |khat_i|^2
     for (int base = r0; base < N; base += RPI * kUnroll) {
@@ -204,16 +379,29 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
     }
 }
 
+template <typename T, int D, int kMode>
+cudaError_t launch_paged(const ScoreArgs& a, cudaStream_t s) {
+    const size_t tab = sizeof(int32_t) * (size_t)((a.N + (1 << a.pg.log2bs) - 1) >> a.pg.log2bs);
+    cudaError_t e = cudaFuncSetAttribute(key_stats_paged_kernel<T, D, kMode>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tab);
+    if (e != cudaSuccess) return e;
+    key_stats_paged_kernel<T, D, kMode><<<(unsigned)a.P, kThreads, tab, s>>>(
+        static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
+        static_cast<__nv_bfloat16*>(a.s_rows), a.pg, static_cast<T*>(a.Kc), a.status);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
-    if (a.pg.table != nullptr)
-        key_stats_kernel<T, D, true><<<(unsigned)a.P, kThreads, 0, s>>>(
-            static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
-            static_cast<__nv_bfloat16*>(a.s_rows), a.pg, static_cast<T*>(a.Kc), a.status);
-    else
-        key_stats_kernel<T, D, false><<<(unsigned)a.P, kThreads, 0, s>>>(
-            static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
-            static_cast<__nv_bfloat16*>(a.s_rows), a.pg, nullptr, a.status);
+    if (a.pg.table != nullptr) {
+        // only bf16 pools are read in place by the tensor-core stages
+        if constexpr (sizeof(T) == 2)
+            if (a.Kc == nullptr) return launch_paged<T, D, 2>(a, s);
+        return launch_paged<T, D, 1>(a, s);
+    }
+    key_stats_kernel<T, D><<<(unsigned)a.P, kThreads, 0, s>>>(
+        static_cast<const T*>(a.K), a.n_cap, a.N, a.inv_norm, a.sum_s, a.ld_ws, a.stats_sum,
+        static_cast<__nv_bfloat16*>(a.s_rows));
     return cudaGetLastError();
 }
 

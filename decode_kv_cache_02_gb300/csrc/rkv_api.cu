@@ -87,6 +87,11 @@ constexpr size_t kAlign = 256;
 // the fused select + gather keeps a problem's scores, bucket keys and kept
 // indices in shared memory; larger problems take the separate kernels
 constexpr size_t kCompactSmemMax = 160 * 1024;
+// paged pools with blocks of at least 128 rows are read directly by the
+// tensor-core stages (one TMA box per 128-row tile); smaller blocks split a
+// tile into boxes too small to keep the producers ahead (64-row blocks made
+// the Gram ~25% slower), and take the contiguous key copy instead
+constexpr int kDirectLog2Block = 7;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Workspace {
@@ -238,7 +243,8 @@ int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, 
 // contiguous copy w.Kc, which the later stages read.
 int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
-               const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr) {
+               const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr,
+               bool* paged_direct = nullptr) {
     // I, R, Z as defined on the page (R may be null: not stored)
     ScoreArgs a{};
     a.K = K;
@@ -263,12 +269,25 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.ld_out = ld_out;
     a.status = w.status;
     ScoreArgs b = a;  // what the stages after the key statistics read
+    bool direct = false;
     if (pg) {
         a.pg = *pg;
-        a.Kc = w.Kc;
-        b.K = w.Kc;
-        b.n_cap = n_cached;
+        // the tensor-core stages read bf16 pools with blocks of at least 128
+        // rows straight through the table; otherwise the key statistics write
+        // a contiguous copy for them
+        direct = d->dtype == RKV_DTYPE_BF16 && pg->log2bs >= kDirectLog2Block &&
+                 (int64_t)pg->H * pg->num_blocks < ((int64_t)1 << 31) &&
+                 rkv::gram_tc_supported(b) && rkv::importance_tc_supported(b);
+        if (direct) {
+            b.pg = *pg;
+            b.paged_direct = true;
+        } else {
+            a.Kc = w.Kc;
+            b.K = w.Kc;
+            b.n_cap = n_cached;
+        }
     }
+    if (paged_direct) *paged_direct = direct;
     const bool gram_tc = rkv::gram_tc_supported(b);
     const bool imp_tc = rkv::importance_tc_supported(b);
     a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
@@ -605,14 +624,16 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     pg.H = desc->num_kv_heads;
     pg.num_blocks = desc->num_blocks;
     if (vf.zvar && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
+    bool direct = false;
     rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
-                    vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg);
+                    vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg, &direct);
     if (rc) return rc;
     rkv::VariantIn vin;
     if (vf.any()) vin = variant_in(*variant, vf, lambda, w, samples(variant, n_cached, budget));
     const int row_bytes = desc->head_dim * (int)es;
     cudaError_t e = timed(kCompactPaged, s, [&] {
-        return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, tail, budget, out_idx, w.Kc,
+        return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, tail, budget, out_idx,
+                                         direct ? nullptr : w.Kc,
                                          K_pool, V_pool, pg, row_bytes, w.status, s, vin);
     });
     if (e == cudaSuccess && n_free > 0)

@@ -19,6 +19,21 @@ struct PagedIn {
     int num_blocks = 0;
 };
 
+// Where the tensor-core kernels' TMA loads find the key rows: with table ==
+// nullptr the contiguous map (outer coordinate = problem); otherwise a map of
+// the paged pool (rows = the rows of one block, outer = block * H + head) read
+// one block (or, for blocks over 128 rows, 128 rows) at a time through the
+// table, blocks past the sequence's nb blocks (and invalid ids) read as zero.
+struct KeySource {
+    const int32_t* table = nullptr;
+    int max_blocks = 0;
+    int log2bs = 0;
+    int H = 1;
+    int nb = 0;          // blocks holding the problem's N rows
+    int num_blocks = 0;
+    int box_rows = 0;    // min(block size, 128)
+};
+
 // Everything the scoring kernels of one call need.
 struct ScoreArgs {
     const void* K;       // [P, n_cap, d]
@@ -43,6 +58,8 @@ struct ScoreArgs {
     // copy Kc [P, N, d], which the later stages read instead
     PagedIn pg;
     void* Kc = nullptr;
+    // paged keys read directly by the tensor-core stages (K is then the pool)
+    bool paged_direct = false;
 };
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "rkv_common.cuh"
+#include "rkv_internal.h"
 
 namespace rkv {
 namespace tc {
@@ -69,6 +70,34 @@ RKV_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+// TMA loads of key rows [r0, r0 + rows) of problem p into a 128-byte-swizzled
+// K-major tile at dst (KC chunks of 64 columns, chunk_bytes apart).  From the
+// contiguous map, one load per chunk; from a paged pool (ks.table set), one
+// load per block (box_rows rows each: sub-tiles start on 8-row, 1024-byte
+// boundaries, which keeps the swizzle phase), blocks past the sequence and
+// invalid ids at an outer coordinate past the pool, which reads as zeros.
+RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const CUtensorMap* map,
+                           uint64_t* bar, int64_t p, int r0, int rows, const KeySource& ks) {
+    if (ks.table == nullptr) {
+        for (int c = 0; c < KC; ++c) tma_load_3d(dst + c * chunk_bytes, map, bar, c * 64, r0, (int)p);
+        return;
+    }
+    const int64_t s = p / ks.H;
+    const int h = (int)(p - s * ks.H);
+    const int32_t* row = ks.table + s * ks.max_blocks;
+    for (int t = 0; t < rows; t += ks.box_rows) {
+        const int r = r0 + t;
+        const int lb = r >> ks.log2bs;
+        int z = ks.num_blocks * ks.H;
+        if (lb < ks.nb) {
+            const int blk = __ldg(row + lb);
+            if ((unsigned)blk < (unsigned)ks.num_blocks) z = blk * ks.H + h;
+        }
+        const int y = r & ((1 << ks.log2bs) - 1);
+        for (int c = 0; c < KC; ++c)
+            tma_load_3d(dst + c * chunk_bytes + t * 128, map, bar, c * 64, y, z);
+    }
 }
 RKV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 RKV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -159,6 +188,11 @@ bool make_map_3d_bf16(CUtensorMap* map, const void* base, int inner, int rows,
                       int box_rows);
 
 int sm_count();
+// The tensor map of a call's keys: the contiguous [P][N][D] map with boxes of
+// box_rows rows (ks: no table), or, for paged keys read directly, the pool map
+// [H * num_blocks][block size][D] with boxes of min(block size, 128) rows and
+// ks filled from the call's table.
+bool make_key_map(CUtensorMap* map, const ScoreArgs& a, int D, int box_rows, KeySource* ks);
 
 }  // namespace tc
 }  // namespace rkv

@@ -36,6 +36,22 @@ bool make_map_3d_bf16(CUtensorMap* map, const void* base, int inner, int rows, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_key_map(CUtensorMap* map, const ScoreArgs& a, int D, int box_rows, KeySource* ks) {
+    *ks = KeySource{};
+    if (!a.paged_direct)
+        return make_map_3d_bf16(map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, box_rows);
+    const int bs = 1 << a.pg.log2bs;
+    ks->table = a.pg.table;
+    ks->max_blocks = a.pg.max_blocks;
+    ks->log2bs = a.pg.log2bs;
+    ks->H = a.pg.H;
+    ks->nb = (a.N + bs - 1) / bs;
+    ks->num_blocks = a.pg.num_blocks;
+    ks->box_rows = bs < 128 ? bs : 128;
+    return make_map_3d_bf16(map, a.K, D, bs, (int64_t)a.pg.H * a.pg.num_blocks, D, (int64_t)bs * D,
+                            ks->box_rows);
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
