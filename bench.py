@@ -43,15 +43,15 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "ce17dc521018fad4a2d4bae5d959af39e5949c69e0c548e300f0fc0baa61c4bd", 314551296 / 1024),
-        "importance_tc": ("k_importance_tc.cu", "32bfb634d7ea8530623155077cdbee13ae230d967bb8603415098e8f904b022e", 329625856 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "0e195e5262769e197b8a0cad98677843c90d80e7d43bf5e88cfbc76f19f9e083", 324306176 / 1024),
-        "compact": ("k_compact.cu", "77c9483fefe942a991c5cef30afe670c95ffbdc7cc07356e45ae6bfafc5f4b0a", 1035702016 / 1024),
+        "key_stats": ("k_key_stats.cu", "06f09d0e82b37b03c9517036a1fb699f2399c6089c2fd04a00b01a6b04e52846", 314466816 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "5bf6de2ef0b928d287128e3c26fd2430faa608d61700f3fe7eeab53be70b6c1a", 329661952 / 1024),
+        "gram_tc": ("k_gram_tc.cu", "f72db5552b74c1a982f0ff3ebe0d211af51b2066be9b84b2f953aaac39803be7", 323260928 / 1024),
+        "compact": ("k_compact.cu", "07cb4d2667b517ae27ba64a5fc53edabd2aaf8802ecf10740fb9dc937eee86a0", 1035607808 / 1024),
     },
-    # the paged round (bs 16, 8 heads per block), same problems
+    # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
-        "key_stats_paged": ("k_key_stats.cu", "ce17dc521018fad4a2d4bae5d959af39e5949c69e0c548e300f0fc0baa61c4bd", 572683776 / 1024),
-        "compact_paged": ("k_compact.cu", "77c9483fefe942a991c5cef30afe670c95ffbdc7cc07356e45ae6bfafc5f4b0a", 973886208 / 1024),
+        "key_stats_paged": ("k_key_stats.cu", "06f09d0e82b37b03c9517036a1fb699f2399c6089c2fd04a00b01a6b04e52846", 315396864 / 1024),
+        "compact_paged": ("k_compact.cu", "07cb4d2667b517ae27ba64a5fc53edabd2aaf8802ecf10740fb9dc937eee86a0", 966369536 / 1024),
     },
 }
 
@@ -498,7 +498,7 @@ def run_paged(args, w):
     for k, v in kernels.items():
         per = v["ms"] / v["launches"] * 1e-3
         e = {"ms_per_launch": per * 1e3,
-             "traffic": measured_traffic(w.name + "_paged", k, P) if bs == 16 else None}
+             "traffic": measured_traffic(w.name + "_paged", k, P) if bs == 128 else None}
         if k in model:
             e["hbm_frac"] = model[k]["bytes"] / per / 1e9 / peaks["hbm_gbs"]
         if k == "gram_tc":
