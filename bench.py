@@ -36,11 +36,11 @@ from decode_kv_cache_02_gb300 import rkv, workloads as wl  # noqa: E402
 
 METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM roofline"
 
-# DRAM bytes (read + write) per problem measured by ncu on the Llama-8B-shaped
-# problems (profiles/kernels_llama8b_1024problems.md, 1,024 problems), with the
-# sha256 of the kernel source they were measured on; a changed source reports
-# traffic null.  Every kernel streams whole problems, so traffic scales with
-# the problem count.
+# DRAM bytes (read + write) per problem measured by ncu on a 1,024-problem
+# copy of the Llama-8B-shaped workload (the committed per-kernel ncu summaries),
+# with the sha256 of the kernel source they were measured on; a changed source
+# reports traffic null.  Every kernel streams whole problems, so traffic scales
+# with the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
         "key_stats": ("k_key_stats.cu", "06f09d0e82b37b03c9517036a1fb699f2399c6089c2fd04a00b01a6b04e52846", 314466816 / 1024),
@@ -178,7 +178,8 @@ def _barrier(world):
 
 def work_model(w: wl.Workload) -> dict:
     """Algorithmic bytes (HBM) / flops per launch of each kernel, for the
-    whole step (all P problems).  See the kernel table in the design doc."""
+    whole step (all P problems): what each kernel must read and write (or
+    the useful flops of the Gram's symmetric half), not what it happens to."""
     P, N, d, G, es = w.problems, w.n_cached, w.head_dim, w.gqa, (2 if w.dtype == "bf16" else 4)
     B, n_obs = w.budget, w.n_obs
     k_bytes = P * N * d * es
