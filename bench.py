@@ -755,6 +755,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llama8b_full", choices=list(wl.BY_NAME))
+    ap.add_argument("--config", type=int, default=None, choices=range(len(wl.WORKLOADS)),
+                    help="the workload by its position in the table (0 tiny .. 4 stream)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="seed of the synthetic inputs (default: the workload's own)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=6)
@@ -782,7 +786,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the step over a lambda/beta/tau/variant sweep, one line each")
     args = ap.parse_args()
-    w = wl.BY_NAME[args.workload]
+    w = wl.WORKLOADS[args.config] if args.config is not None else wl.BY_NAME[args.workload]
+    if args.seed is not None:
+        w = w.scaled(seed=args.seed)
     if args.problems:
         # a scaled copy: sequences of the workload's heads where the count
         # allows (blocks of a paged pool hold all heads of a sequence)

@@ -708,6 +708,15 @@ int rkv_gather(const rkv_desc* desc, const void* src, const int32_t* idx, int bu
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
+int rkv_selftest_wait_timeout(void* workspace, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+        return RKV_ERR_WORKSPACE;
+    return rkv::launch_wait_timeout(reinterpret_cast<DeviceStatus*>(workspace),
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RKV_OK
+               : RKV_ERR_CUDA;
+}
+
 int rkv_workspace_init(void* workspace, void* stream) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
         return RKV_ERR_WORKSPACE;

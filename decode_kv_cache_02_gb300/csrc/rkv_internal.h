@@ -141,4 +141,8 @@ cudaError_t launch_paged_release(int64_t S, int32_t* table, int max_blocks, int 
 cudaError_t launch_variant(int64_t P, int N, int n_obs, const VariantIn& v, float* Z,
                            float* I_out, float* R_out, int64_t ld_out, cudaStream_t s);
 
+// One bounded wait that nothing completes (the failure path of every wait):
+// records kDevErrTimeout in st after the wait limit (~1 s).
+cudaError_t launch_wait_timeout(DeviceStatus* st, cudaStream_t s);
+
 }  // namespace rkv

@@ -27,7 +27,7 @@ EXPORTED = [
     "rkv_workspace_init", "rkv_get_device_status", "rkv_strerror", "rkv_timing_enable",
     "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
     "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
-    "rkv_sentence_reps", "rkv_sentence_penalty",
+    "rkv_sentence_reps", "rkv_sentence_penalty", "rkv_selftest_wait_timeout",
 ]
 RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_DEVICE = 6
@@ -179,6 +179,8 @@ def load(path: str | None = None):
         lib.rkv_sentence_reps.restype = i32
         lib.rkv_sentence_penalty.argtypes = [ctypes.POINTER(_Sentences), vp]
         lib.rkv_sentence_penalty.restype = i32
+        lib.rkv_selftest_wait_timeout.argtypes = [vp, vp]
+        lib.rkv_selftest_wait_timeout.restype = i32
         lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
         lib.rkv_select.restype = i32
         lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
@@ -537,3 +539,10 @@ def rkv_sentence_penalty(sentences: Sentences, stream=None):
     _check(load().rkv_sentence_penalty(ctypes.byref(sc), _stream_ptr(stream)),
            "rkv_sentence_penalty")
     return sentences.penalty
+
+
+def rkv_selftest_wait_timeout(workspace, stream=None):
+    """Enqueues one bounded wait that nothing completes; afterwards
+    rkv_get_device_status(workspace) reports RKV_ERR_DEVICE."""
+    _check(load().rkv_selftest_wait_timeout(workspace.data_ptr(), _stream_ptr(stream)),
+           "rkv_selftest_wait_timeout")

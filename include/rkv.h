@@ -330,6 +330,13 @@ int rkv_compress_noalloc(const rkv_desc* desc, const void* K, const void* V, con
                          int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                          void* out_K, void* out_V, int32_t* out_idx, void* stream);
 
+/* Self-test of the failure path: enqueues one bounded wait that nothing
+ * completes (the primitive every wait of the kernels uses).  After its limit
+ * (about a second) it records a timeout in `workspace`, which
+ * rkv_get_device_status() then reports as RKV_ERR_DEVICE; the context stays
+ * usable.  Nothing hangs and nothing traps. */
+int rkv_selftest_wait_timeout(void* workspace, void* stream);
+
 /* Human-readable name of an RKV_* code. */
 const char* rkv_strerror(int code);
 

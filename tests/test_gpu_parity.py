@@ -242,6 +242,19 @@ def test_device_status_clean(cuda_ok):
     assert rkv.rkv_get_device_status(ws) == 0
 
 
+def test_bounded_wait_runs_out_and_is_reported(cuda_ok):
+    """A bounded wait that nothing completes ends with a recorded timeout
+    (no hang, no trap); the status is read once and cleared, and the context
+    still runs a compression round correctly afterwards."""
+    w = wl.BY_NAME["tiny"]
+    K, V, Q = wl.make_inputs(w, device=DEV)
+    ws = rkv.alloc_workspace(K, w.gqa, w.n_cached, w.n_obs)
+    rkv.rkv_selftest_wait_timeout(ws)
+    assert rkv.rkv_get_device_status(ws) == rkv.RKV_ERR_DEVICE
+    assert rkv.rkv_get_device_status(ws) == 0
+    _full_check(w, K, V, Q, list(range(w.problems)))
+
+
 def test_stream_rounds(cuda_ok):
     """Sustained decode stream (batch x layers x heads scaled down to 64
     problems, 40 rounds): the cache is compacted in place each round, and each
