@@ -618,9 +618,13 @@ def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent=None):
     oK = torch.empty((K.shape[0], B, K.shape[2]), dtype=K.dtype, pin_memory=True)
     oV = torch.empty_like(oK, pin_memory=True)
     oI = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True)
-    slots = [(K, V, Q, out_K, out_V, idx),
-             (torch.empty_like(K), torch.empty_like(V), torch.empty_like(Q), torch.empty_like(out_K),
-              torch.empty_like(out_V), torch.empty_like(idx))]
+    # the kept rows land in outputs of `budget` rows per problem, so that they
+    # come back as one contiguous copy
+    slots = [(K, V, Q, torch.empty_like(oK, device=K.device), torch.empty_like(oV, device=K.device),
+              idx),
+             (torch.empty_like(K), torch.empty_like(V), torch.empty_like(Q),
+              torch.empty_like(oK, device=K.device), torch.empty_like(oV, device=K.device),
+              torch.empty_like(idx))]
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     done_compute = [None, None]
@@ -650,8 +654,8 @@ def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent=None):
         e_out = ev()
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(e_c)
-            oK.copy_(dOK[:, :B], non_blocking=True)
-            oV.copy_(dOV[:, :B], non_blocking=True)
+            oK.copy_(dOK, non_blocking=True)
+            oV.copy_(dOV, non_blocking=True)
             oI.copy_(dI, non_blocking=True)
             e_out.record(d2h_s)
         done_d2h[sl] = e_out
@@ -684,7 +688,8 @@ def e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent=None):
     d2h = oK.numel() * oK.element_size() * 2 + oI.numel() * oI.element_size()
     return {"value": u_sum / (t_max * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": t_max / steps,
-            "pipelined": "2 buffer sets; copy-in, compute, copy-out on three streams"}
+            "pipelined": "2 buffer sets; copy-in, compute, copy-out on three streams",
+            "outputs": "budget rows per problem (contiguous copy-out)"}
 
 
 def run_stream(args, w):

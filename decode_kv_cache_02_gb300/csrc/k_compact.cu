@@ -281,8 +281,8 @@ template <bool kPaged>
 __global__ void __launch_bounds__(kThreads)
 compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
                int32_t* __restrict__ idx, const uint4* a_src, const uint4* b_src, uint4* a_dst,
-               uint4* b_dst, int n_cap, int vpr, int in_place, DeviceStatus* st, VariantIn var,
-               PagedIn pg) {
+               uint4* b_dst, int n_cap, int out_cap, int vpr, int in_place, DeviceStatus* st,
+               VariantIn var, PagedIn pg) {
     extern __shared__ uint32_t s_dyn[];
     const int C = N - n_obs, k = budget - n_obs;
     uint32_t* keys = s_dyn;                                         // [C]
@@ -427,6 +427,7 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
     }
     const int64_t base = (int64_t)p * n_cap * vpr;
     if (!in_place) {
+        const int64_t obase = (int64_t)p * out_cap * vpr;
         const int total = budget * vpr;
         for (int e0 = tid; e0 < total; e0 += kThreads * kCopyVecs) {
             uint4 va[kCopyVecs], vb[kCopyVecs];
@@ -450,8 +451,8 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
 #pragma unroll
             for (int t = 0; t < kCopyVecs; ++t) {
                 if (dst[t] >= 0) {
-                    a_dst[base + dst[t]] = va[t];
-                    if (b_dst) b_dst[base + dst[t]] = vb[t];
+                    a_dst[obase + dst[t]] = va[t];
+                    if (b_dst) b_dst[obase + dst[t]] = vb[t];
                 }
             }
         }
@@ -507,8 +508,8 @@ size_t compact_smem_bytes(int N, int n_obs, int budget, bool sentences) {
 
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
-                           void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
-                           cudaStream_t s, const VariantIn& var) {
+                           void* dst_b, int n_cap, int out_cap, int row_bytes, bool in_place,
+                           DeviceStatus* st, cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
     const size_t smem = compact_smem_bytes(N, n_obs, budget, var.pen != nullptr);
     cudaError_t e = cudaFuncSetAttribute(compact_kernel<false>,
@@ -517,7 +518,7 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
     compact_kernel<false><<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(src_a),
         static_cast<const uint4*>(src_b), static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), n_cap,
-        row_bytes / 16, in_place ? 1 : 0, st, var, PagedIn{});
+        in_place ? n_cap : out_cap, row_bytes / 16, in_place ? 1 : 0, st, var, PagedIn{});
     return cudaGetLastError();
 }
 
@@ -532,7 +533,7 @@ cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, 
     if (e != cudaSuccess) return e;
     compact_kernel<true><<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(kc), nullptr,
-        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), N, row_bytes / 16, 1, st, var,
+        static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), N, N, row_bytes / 16, 1, st, var,
         pg);
     return cudaGetLastError();
 }

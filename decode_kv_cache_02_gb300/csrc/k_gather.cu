@@ -25,7 +25,7 @@ constexpr int kUnroll = 4;
 __global__ void __launch_bounds__(kThreads)
 gather_oop_kernel(const uint4* __restrict__ a, const uint4* __restrict__ b, uint4* __restrict__ da,
                   uint4* __restrict__ db, const int32_t* __restrict__ idx, int64_t P, int n_cap,
-                  int budget, int vpr, int64_t total, DeviceStatus* st) {
+                  int out_cap, int budget, int vpr, int64_t total, DeviceStatus* st) {
     // element e -> (problem, kept row, vector)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t e0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e0 < total;
@@ -45,7 +45,7 @@ gather_oop_kernel(const uint4* __restrict__ a, const uint4* __restrict__ b, uint
                 if (s >= n_cap) set_error(st, kDevErrIndex, (unsigned)pr);
                 if (s >= 0 && s < n_cap) {
                     const int64_t src = ((int64_t)p * n_cap + s) * vpr + v;
-                    dst[t] = ((int64_t)p * n_cap + r) * vpr + v;
+                    dst[t] = ((int64_t)p * out_cap + r) * vpr + v;
                     va[t] = __ldg(a + src);
                     if (b) vb[t] = __ldg(b + src);
                 }
@@ -112,8 +112,8 @@ gather_inplace_kernel(uint4* a, uint4* b, const int32_t* __restrict__ idx, int n
 }  // namespace
 
 cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, void* dst_b,
-                          const int32_t* idx, int64_t P, int n_cap, int budget, int row_bytes,
-                          bool in_place, DeviceStatus* st, cudaStream_t s) {
+                          const int32_t* idx, int64_t P, int n_cap, int out_cap, int budget,
+                          int row_bytes, bool in_place, DeviceStatus* st, cudaStream_t s) {
     if (P == 0 || budget == 0) return cudaSuccess;
     const int vpr = row_bytes / 16;
     if (in_place) {
@@ -129,8 +129,8 @@ cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, voi
         if (blocks > cap) blocks = cap;
         gather_oop_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(
             static_cast<const uint4*>(src_a), static_cast<const uint4*>(src_b),
-            static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), idx, P, n_cap, budget, vpr, total,
-            st);
+            static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), idx, P, n_cap, out_cap, budget, vpr,
+            total, st);
     }
     return cudaGetLastError();
 }

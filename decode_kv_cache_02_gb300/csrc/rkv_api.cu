@@ -142,13 +142,16 @@ size_t elem_size(int dtype) { return dtype == RKV_DTYPE_BF16 ? 2 : 4; }
 
 int check_desc(const rkv_desc* d) {
     if (!d) return RKV_ERR_INVALID_ARG;
-    if (d->num_problems < 0 || d->n_capacity < 1) return RKV_ERR_INVALID_ARG;
+    if (d->num_problems < 0 || d->n_capacity < 1 || d->out_capacity < 0) return RKV_ERR_INVALID_ARG;
     if (d->num_problems > (int64_t)1 << 31) return RKV_ERR_INVALID_ARG;
     if (d->dtype != RKV_DTYPE_BF16 && d->dtype != RKV_DTYPE_FP32) return RKV_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return RKV_ERR_UNSUPPORTED;
     if (d->gqa_group < 1 || d->gqa_group > 16) return RKV_ERR_UNSUPPORTED;
     return RKV_OK;
 }
+
+// Rows per problem of the outputs of rkv_compress / rkv_gather.
+int out_cap(const rkv_desc* d) { return d->out_capacity > 0 ? d->out_capacity : d->n_capacity; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -428,23 +431,27 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t P = desc->num_problems;
+    const int ocap = out_cap(desc);
     if (n_cached < 1 || n_cached > desc->n_capacity || budget < 1 || budget > desc->n_capacity ||
-        n_obs < 1 || n_obs > budget || beta < 0)
+        budget > ocap || n_obs < 1 || n_obs > budget || beta < 0)
         return RKV_ERR_INVALID_ARG;
     const size_t es = elem_size(desc->dtype);
     const size_t bytes = (size_t)P * desc->n_capacity * desc->head_dim * es;
+    const size_t obytes = (size_t)P * ocap * desc->head_dim * es;
     if (P > 0) {
         if (!K || !V || !out_K || !out_V || !out_idx || !Q_obs) return RKV_ERR_INVALID_ARG;
         if (!aligned16(K) || !aligned16(V) || !aligned16(out_K) || !aligned16(out_V) ||
             !aligned16(Q_obs))
             return RKV_ERR_INVALID_ARG;
-        if (partial_overlap(out_K, bytes, K, bytes) || partial_overlap(out_V, bytes, V, bytes) ||
-            partial_overlap(out_K, bytes, V, bytes) || partial_overlap(out_V, bytes, K, bytes) ||
+        if (partial_overlap(out_K, obytes, K, bytes) || partial_overlap(out_V, obytes, V, bytes) ||
+            partial_overlap(out_K, obytes, V, bytes) || partial_overlap(out_V, obytes, K, bytes) ||
+            partial_overlap(out_K, obytes, out_V, obytes) ||
             (out_K == V) || (out_V == K) || (out_K == out_V && P > 0))
             return RKV_ERR_ALIAS;
     }
     const bool in_place = (out_K == K) && (out_V == V);
     if (!in_place && (out_K == K || out_V == V)) return RKV_ERR_ALIAS;  // mixed modes
+    if (in_place && ocap != desc->n_capacity) return RKV_ERR_INVALID_ARG;
     const int row_bytes = desc->head_dim * (int)es;
     if (n_cached <= budget) {
         // nothing to evict
@@ -457,8 +464,8 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
         });
         if (e == cudaSuccess && !in_place) {
             e = timed(kGather, s, [&] {
-                return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, budget,
-                                          row_bytes, false,
+                return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, ocap,
+                                          budget, row_bytes, false,
                                           reinterpret_cast<DeviceStatus*>(workspace), s);
             });
         }
@@ -491,7 +498,7 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
         if (vf.any()) vin = variant_in(*variant, vf, lambda, w, sample);
         e = timed(kCompact, s, [&] {
             return rkv::launch_compact(P, n_cached, w.Z, w.ld, tail, budget, out_idx, K, V, out_K,
-                                       out_V, desc->n_capacity, row_bytes, in_place, w.status, s,
+                                       out_V, desc->n_capacity, ocap, row_bytes, in_place, w.status, s,
                                        vin);
         });
     } else {
@@ -500,8 +507,8 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
         });
         if (e == cudaSuccess)
             e = timed(kGather, s, [&] {
-                return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, budget,
-                                          row_bytes, in_place, w.status, s);
+                return rkv::launch_gather(K, V, out_K, out_V, out_idx, P, desc->n_capacity, ocap,
+                                          budget, row_bytes, in_place, w.status, s);
             });
     }
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
@@ -693,17 +700,20 @@ int rkv_gather(const rkv_desc* desc, const void* src, const int32_t* idx, int bu
                void* stream) {
     int rc = check_desc(desc);
     if (rc) return rc;
-    if (budget < 1 || budget > desc->n_capacity) return RKV_ERR_INVALID_ARG;
+    const int ocap = out_cap(desc);
+    if (budget < 1 || budget > desc->n_capacity || budget > ocap) return RKV_ERR_INVALID_ARG;
     if (desc->num_problems == 0) return RKV_OK;
     if (!src || !dst || !idx || !aligned16(src) || !aligned16(dst)) return RKV_ERR_INVALID_ARG;
+    if (src == dst && ocap != desc->n_capacity) return RKV_ERR_INVALID_ARG;
     const size_t es = elem_size(desc->dtype);
     const size_t bytes = (size_t)desc->num_problems * desc->n_capacity * desc->head_dim * es;
-    if (partial_overlap(src, bytes, dst, bytes)) return RKV_ERR_ALIAS;
+    const size_t obytes = (size_t)desc->num_problems * ocap * desc->head_dim * es;
+    if (partial_overlap(src, bytes, dst, obytes)) return RKV_ERR_ALIAS;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = timed(kGather, s, [&] {
         return rkv::launch_gather(src, nullptr, dst, nullptr, idx, desc->num_problems,
-                                  desc->n_capacity, budget, desc->head_dim * (int)es, src == dst,
-                                  nullptr, s);
+                                  desc->n_capacity, ocap, budget, desc->head_dim * (int)es,
+                                  src == dst, nullptr, s);
     });
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }

@@ -73,10 +73,11 @@ cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_select(int64_t P, int N, const float* Z, int64_t ldz, int n_obs,
                           int budget, int32_t* idx, DeviceStatus* st, cudaStream_t s);
 
-// Copies kept rows of up to two tensors (b may be null).  row_bytes is a
+// Copies kept rows of up to two tensors (b may be null): sources hold n_cap
+// rows per problem, destinations out_cap (= n_cap in place).  row_bytes is a
 // multiple of 16; in_place means dst == src for both tensors.
 cudaError_t launch_gather(const void* src_a, const void* src_b, void* dst_a, void* dst_b,
-                          const int32_t* idx, int64_t P, int n_cap, int budget,
+                          const int32_t* idx, int64_t P, int n_cap, int out_cap, int budget,
                           int row_bytes, bool in_place, DeviceStatus* st, cudaStream_t s);
 
 // idx rows = 0..n-1 then -1 (nothing evicted).
@@ -121,8 +122,8 @@ cudaError_t launch_sentence_reps(const void* hidden, int dtype, const int32_t* t
 size_t compact_smem_bytes(int N, int n_obs, int budget, bool sentences = false);
 cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_obs, int budget,
                            int32_t* idx, const void* src_a, const void* src_b, void* dst_a,
-                           void* dst_b, int n_cap, int row_bytes, bool in_place, DeviceStatus* st,
-                           cudaStream_t s, const VariantIn& var = VariantIn{});
+                           void* dst_b, int n_cap, int out_cap, int row_bytes, bool in_place,
+                           DeviceStatus* st, cudaStream_t s, const VariantIn& var = VariantIn{});
 // The same on a paged pool, in place: kept K rows come from the contiguous
 // copy kc [P, N, d], kept V rows move inside v_pool; both land in the pool
 // rows of logical positions 0..budget-1.

@@ -43,7 +43,7 @@ class RkvError(RuntimeError):
 class _Desc(ctypes.Structure):
     _fields_ = [("num_problems", ctypes.c_int64), ("gqa_group", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_capacity", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("out_capacity", ctypes.c_int32)]
 
 
 class _Sentences(ctypes.Structure):
@@ -234,12 +234,14 @@ def _stream_ptr(stream) -> int:
     return int(s.cuda_stream)
 
 
-def make_desc(K: torch.Tensor, gqa_group: int) -> _Desc:
-    """Descriptor of a K (or V) tensor [P, n_capacity, head_dim]."""
+def make_desc(K: torch.Tensor, gqa_group: int, out=None) -> _Desc:
+    """Descriptor of a K (or V) tensor [P, n_capacity, head_dim], with the
+    outputs' rows per problem taken from `out` [P, out_capacity, head_dim]."""
     if K.dim() != 3:
         raise ValueError("K must be [P, n_capacity, head_dim]")
     P, n_cap, d = K.shape
-    return _Desc(P, int(gqa_group), d, n_cap, _dtype_code(K))
+    out_cap = 0 if out is None or out.dim() != 3 or out.shape[1] == n_cap else out.shape[1]
+    return _Desc(P, int(gqa_group), d, n_cap, _dtype_code(K), out_cap)
 
 
 def rkv_workspace_size(K: torch.Tensor, gqa_group: int, n_cached: int, n_obs: int) -> int:
@@ -264,7 +266,6 @@ def _compress_args(K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, 
             or Q_obs.shape[3] != K.shape[2]:
         raise ValueError("Q_obs must be [P, G, n_obs, d]")
     G = Q_obs.shape[1]
-    desc = make_desc(K, G)
     if out_K is None:
         out_K = torch.empty_like(K)
     if out_V is None:
@@ -275,9 +276,13 @@ def _compress_args(K, V, Q_obs, n_cached, budget, n_obs, out_K, out_V, out_idx, 
         workspace = alloc_workspace(K, G, max(n_cached, 1), n_obs)
     for t, n in ((out_K, "out_K"), (out_V, "out_V"), (out_idx, "out_idx")):
         _cuda(t, n)
-    if out_K.shape != K.shape or out_V.shape != K.shape or out_idx.shape != (K.shape[0], budget) \
-            or out_idx.dtype != torch.int32:
+    # outputs hold n_capacity rows per problem, or any count >= budget
+    if out_K.dim() != 3 or out_V.shape != out_K.shape or out_K.shape[0] != K.shape[0] \
+            or out_K.shape[2] != K.shape[2] or out_K.shape[1] < budget \
+            or out_K.dtype != K.dtype or out_V.dtype != K.dtype \
+            or out_idx.shape != (K.shape[0], budget) or out_idx.dtype != torch.int32:
         raise ValueError("output shapes")
+    desc = make_desc(K, G, out_K)
     return desc, out_K, out_V, out_idx, workspace
 
 
@@ -330,13 +335,15 @@ def rkv_compress_noalloc(K, V, Q_obs, n_cached: int, budget: int, n_obs: int = 8
         _cuda(t, n)
     if V.shape != K.shape or V.dtype != K.dtype or Q_obs.dtype != K.dtype or Q_obs.dim() != 4:
         raise ValueError("K, V, Q_obs must share shape/dtype; Q_obs is [P, G, n_obs, d]")
-    desc = make_desc(K, Q_obs.shape[1])
     if out_K is None:
         out_K = torch.empty_like(K)
     if out_V is None:
         out_V = torch.empty_like(V)
     if out_idx is None:
         out_idx = torch.empty((K.shape[0], budget), dtype=torch.int32, device=K.device)
+    if out_V.shape != out_K.shape:
+        raise ValueError("out_K and out_V must have the same shape")
+    desc = make_desc(K, Q_obs.shape[1], out_K)
     rc = load().rkv_compress_noalloc(ctypes.byref(desc), K.data_ptr(), V.data_ptr(),
                                      Q_obs.data_ptr(), int(n_cached), int(budget), int(n_obs),
                                      float(lam), int(beta), float(tau), out_K.data_ptr(),
@@ -405,9 +412,13 @@ def rkv_gather(src, idx, budget: int, dst=None, stream=None):
     _cuda(idx, "idx")
     if idx.dtype != torch.int32 or idx.shape != (src.shape[0], budget):
         raise ValueError("idx must be int32 [P, budget]")
-    desc = make_desc(src, 1)
     if dst is None:
         dst = torch.empty_like(src)
+    _cuda(dst, "dst")
+    if dst.dim() != 3 or dst.shape[0] != src.shape[0] or dst.shape[2] != src.shape[2] \
+            or dst.shape[1] < budget or dst.dtype != src.dtype:
+        raise ValueError("dst must be [P, >= budget, d] of src's dtype")
+    desc = make_desc(src, 1, dst)
     rc = load().rkv_gather(ctypes.byref(desc), src.data_ptr(), idx.data_ptr(), int(budget),
                            dst.data_ptr(), _stream_ptr(stream))
     _check(rc, "rkv_gather")

@@ -27,10 +27,14 @@
  * per kernel.
  *
  * Layouts (every array contiguous, row-major; element type `dtype`):
- *   K, V, out_K, out_V   [P, n_capacity, head_dim]; problem p starts at
+ *   K, V                 [P, n_capacity, head_dim]; problem p starts at
  *                        element p*n_capacity*head_dim.  head_dim*elem_size
  *                        must be a multiple of 16 bytes and every base pointer
  *                        16-byte aligned.
+ *   out_K, out_V         [P, out_capacity, head_dim] (out_capacity = 0 in the
+ *                        descriptor means n_capacity): an out-of-place call
+ *                        may write the kept rows into buffers of just
+ *                        `budget` rows per problem.
  *   Q_obs                [P, G, n_obs, head_dim]: query q of query head g of
  *                        problem p.  Query head g of the G that share the KV
  *                        head of problem p.
@@ -80,6 +84,9 @@ typedef struct {
     int32_t head_dim;     /* d, 64 or 128                                    */
     int32_t n_capacity;   /* rows allocated per problem in K/V/out_K/out_V   */
     int32_t dtype;        /* RKV_DTYPE_BF16 or RKV_DTYPE_FP32 (K, V, Q, out) */
+    int32_t out_capacity; /* rows per problem in out_K/out_V (and rkv_gather's
+                             dst); 0 = n_capacity.  Must be >= budget, and 0 or
+                             n_capacity for in-place compaction.             */
 } rkv_desc;
 
 /* Largest n_cached accepted by rkv_compress / rkv_score. */
@@ -91,7 +98,8 @@ size_t rkv_workspace_size(const rkv_desc* desc, int n_cached, int n_obs);
 
 /* One compression round (the whole step above) for all P problems.
  *   n_cached   rows in use per problem (merged cache + buffer), <= n_capacity
- *   budget     rows kept per problem, n_obs <= budget <= n_capacity
+ *   budget     rows kept per problem, n_obs <= budget <= n_capacity and
+ *              budget <= out_capacity
  *   n_obs      observation tokens (the newest n_obs rows), >= 1
  *   lambda, beta, tau   the parameters of Z, protection and similarity
  *   out_K/out_V  receive the kept rows in ascending original position in

@@ -115,6 +115,37 @@ def test_long_context_selection_paths(cuda_ok, n_cached, budget):
     _variant_check(w, K, V, Q, [0], True, 5)
 
 
+@pytest.mark.parametrize("n_cached,budget", [(1152, 1024), (14000, 13000), (900, 1024)])
+def test_outputs_of_budget_rows(cuda_ok, n_cached, budget):
+    """Outputs of just `budget` rows per problem (out_capacity = budget) get
+    the same kept rows, bit for bit, as outputs of the inputs' capacity: the
+    fused select + gather, the separate select and gather (long rows), the
+    copy when nothing is evicted, rkv_compress_noalloc and rkv_gather."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=n_cached, budget=budget, layers=1,
+                                           batch=1, kv_heads=3 if n_cached > 2000 else 16)
+    K, V, Q = wl.make_inputs(w, device=DEV, n_cap=max(n_cached, budget) + 40)
+    args = (w.n_cached, w.budget, w.n_obs, w.lam, w.beta, w.tau)
+    oK, oV, idx = rkv.rkv_compress(K, V, Q, *args)
+    P, d = K.shape[0], K.shape[2]
+    cK = torch.full((P, w.budget, d), 7.0, dtype=K.dtype, device=DEV)
+    cV = torch.full_like(cK, 7.0)
+    _, _, idx2 = rkv.rkv_compress(K, V, Q, *args, out_K=cK, out_V=cV)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+    kept = min(w.n_cached, w.budget)
+    assert torch.equal(cK[:, :kept], oK[:, :kept]) and torch.equal(cV[:, :kept], oV[:, :kept])
+    if kept < w.budget:  # rows past the kept ones are not touched
+        assert bool((cK[:, kept:] == 7.0).all()) and bool((cV[:, kept:] == 7.0).all())
+    if w.n_cached > w.budget:
+        nK = torch.empty_like(cK)
+        nV = torch.empty_like(cV)
+        rkv.rkv_compress_noalloc(K, V, Q, *args, out_K=nK, out_V=nV)
+        g = rkv.rkv_gather(V, idx, w.budget, dst=torch.empty_like(cV))
+        torch.cuda.synchronize()
+        assert torch.equal(nK, cK) and torch.equal(nV, cV)
+        assert torch.equal(g, cV)
+
+
 def _variant_check(w, K, V, Q, problems, softmax, window, in_place=False):
     """Variant scores through rkv_score_ex and the kept set and rows through
     rkv_compress_ex, against the oracle's base scores plus its variant."""

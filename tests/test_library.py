@@ -44,9 +44,9 @@ def test_strerror(lib):
     assert rkv.strerror(999) == "unknown error code"
 
 
-def _desc(P=4, G=4, d=128, n_cap=1152, dtype=0):
+def _desc(P=4, G=4, d=128, n_cap=1152, dtype=0, out_cap=0):
     from decode_kv_cache_02_gb300 import rkv
-    return rkv._Desc(P, G, d, n_cap, dtype)
+    return rkv._Desc(P, G, d, n_cap, dtype, out_cap)
 
 
 def test_workspace_size(lib):
@@ -84,6 +84,18 @@ def test_argument_errors_need_no_device(lib):
     assert lib.rkv_select(1, 100, fake, 8, 100, fake, None) == 1   # budget >= n
     assert lib.rkv_select(1, 100, fake, 9, 8, fake, None) == 1     # n_obs > budget
     assert lib.rkv_gather(ctypes.byref(d), fake, fake, 0, fake, None) == 1
+    # outputs of out_capacity rows per problem
+    assert call(desc=_desc(out_cap=-1)) == 1
+    assert call(desc=_desc(out_cap=1000)) == 1     # budget > out_capacity
+    assert call(desc=_desc(out_cap=1024), oK=fake, oV=fake + 2 ** 30, ws_bytes=1 << 40) == 1
+    #   (in place needs out_capacity = n_capacity)
+    assert call(desc=_desc(out_cap=1024), oK=fake + 2 ** 30 - 4 * 1024 * 256 + 256,
+                ws_bytes=1 << 40) == 4           # out_K's 1024-row problems run into V
+    assert call(desc=_desc(out_cap=1024), ws_bytes=10) == 3  # valid, reaches the workspace check
+    assert lib.rkv_gather(ctypes.byref(_desc(out_cap=100)), fake, fake, 200, fake + 2 ** 30,
+                          None) == 1             # budget > out_capacity
+    assert lib.rkv_gather(ctypes.byref(_desc(out_cap=1024)), fake, fake, 200, fake,
+                          None) == 1             # in place with another row count
 
 
 def test_variant_argument_errors(lib):
