@@ -36,10 +36,10 @@
 //   * warps 2..17 (512 threads, four per scheduler for latency hiding): the
 //     epilogue.  Warp w reads TMEM lanes 32*(w%4).. (one accumulator row per
 //     thread) and one 32-column quarter of the tile, then filters the 32x32
-//     sub-tile -- the largest raw accumulator (an integer max over the bits,
-//     valid for positive floats) times the largest inverse norm of the 32
-//     columns -- skips the sub-tile unless some S could exceed tau (in
-//     diagonal blocks the row's own column is left out of that maximum).  The
+//     sub-tile -- the largest accumulator of the row's 32 columns (returned by
+//     the TMEM load itself, tcgen05.ld.red .max) times the largest inverse
+//     norm of the 32 columns -- and skips the sub-tile unless some S could
+//     exceed tau (the sub-tile holding the row's own column always runs).  The
 //     exact path is branch-free: a per-lane hit mask, row sums in registers,
 //     popc for the newer count.
 //   * Row-side partials (sum of above-tau S, count of newer similar tokens)
@@ -151,21 +151,6 @@ RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// Largest of 32 raw fp32 accumulators compared as signed integers: exact for
-// the positive ones, and <= 0 when none is positive.  A tree of 3-input
-// maxima (depth 4) rather than a chain, for latency.
-RKV_DEV int raw_max32(const uint32_t (&r)[32]) {
-    int a[11];
-#pragma unroll
-    for (int t = 0; t < 10; ++t) a[t] = __vimax3_s32((int)r[3 * t], (int)r[3 * t + 1], (int)r[3 * t + 2]);
-    a[10] = max((int)r[30], (int)r[31]);
-    const int b0 = __vimax3_s32(a[0], a[1], a[2]);
-    const int b1 = __vimax3_s32(a[3], a[4], a[5]);
-    const int b2 = __vimax3_s32(a[6], a[7], a[8]);
-    const int b3 = max(a[9], a[10]);
-    return max(__vimax3_s32(b0, b1, b2), b3);
 }
 
 // ---------------------------------------------------------------- kernel --
@@ -416,11 +401,12 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                     // same warps
                     const int cgr = (cg + J) % kColGroups;
                     uint32_t r[kChunksPerWarp][32];
+                    float rmax[kChunksPerWarp];  // the row's largest accumulator per chunk
 #pragma unroll
                     for (int h = 0; h < kChunksPerWarp; ++h)
-                        tmem_ld_32cols(t_lane + (uint32_t)(acc * W * kRows + w * kRows +
-                                                           (cgr * kChunksPerWarp + h) * 32),
-                                       r[h]);
+                        tmem_ld_32cols_max(t_lane + (uint32_t)(acc * W * kRows + w * kRows +
+                                                               (cgr * kChunksPerWarp + h) * 32),
+                                           r[h], rmax[h]);
                     tmem_ld_wait();
                     if (w == W - 1) {
                         tc_fence_before();
@@ -441,10 +427,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
                             // quarter, at column e = lane
                             const bool self_chunk = diag && cq == q;
                             bool hot = self_chunk;  // S_ii > tau there anyway
-                            if (!hot) {
-                                const int mb = raw_max32(r[h]);
-                                hot = mb > 0 && __int_as_float(mb) * invmax[chunk] > thr;
-                            }
+                            // (rmax <= 0 never passes: thr > 0)
+                            if (!hot) hot = rmax[h] * invmax[chunk] > thr;
                             if (__any_sync(0xffffffffu, hot)) {
                                 const float4* iv4 = reinterpret_cast<const float4*>(inv + jb);
                                 uint32_t hits = 0;
