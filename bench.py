@@ -249,10 +249,18 @@ def cpu_oracle_sample(w: wl.Workload, K, Q, seconds: float = 15.0, max_problems:
     sc = oracle.score(Kh, Qh, w.n_obs, w.lam, w.beta, w.tau, nthreads=cores)
     oracle.select(sc["Z"], w.n_obs, w.budget)
     dt = time.perf_counter() - t0
+    # the same on one core, on a sample of about a tenth of the time
+    n1 = int(min(n, max(1, 0.1 * seconds / max(per_problem * cores, 1e-9))))
+    t0 = time.perf_counter()
+    sc1 = oracle.score(Kh[:n1], Qh[:n1], w.n_obs, w.lam, w.beta, w.tau, nthreads=1)
+    oracle.select(sc1["Z"], w.n_obs, w.budget)
+    dt1 = time.perf_counter() - t0
     return {"value": n * w.n_cached / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.problems} problems of {w.name} (N={w.n_cached}, d={w.head_dim}),"
                       f" scores + selection in fp64, {dt:.1f} s",
-            "seconds": dt, "problems": n}
+            "seconds": dt, "problems": n,
+            "one_core": {"value": n1 * w.n_cached / dt1, "unit": UNIT, "problems": n1,
+                         "seconds": dt1}}
 
 
 # ------------------------------------------------------------------ arms --
