@@ -264,7 +264,12 @@ key_stats_paged_kernel(const T* __restrict__ K, int n_cap, int N, float* __restr
                 }
             }
         } else if constexpr (kMode == 2) {
-            // paged rows read in place: every row's load issued before any is used
+            // paged rows read in place: every row's load issued before any is
+            // used.  Direct reads take blocks of >= 128 rows, and the batch's
+            // rows base + u*RPI lie in the 64-row window [base - r0, +64), so
+            // in one block: one table lookup per batch.
+            static_assert(RPI * kUnroll <= 128, "a batch must fit in one block");
+            const int64_t pr0 = base < N ? phys_row(base) : -1;
             Raw8<T> raw[kUnroll];
             bool ok[kUnroll];
 #pragma unroll
@@ -272,9 +277,8 @@ key_stats_paged_kernel(const T* __restrict__ K, int n_cap, int N, float* __restr
                 const int i = base + u * RPI;
                 ok[u] = false;
                 if (i < N) {
-                    const int64_t pr = phys_row(i);
-                    if (pr >= 0) {
-                        raw[u].load(K + pr * D + col);
+                    if (pr0 >= 0) {
+                        raw[u].load(K + (pr0 + u * RPI) * D + col);
                         ok[u] = true;
                     } else if (sub == 0) {
                         set_error(st, kDevErrIndex, (unsigned)i);
