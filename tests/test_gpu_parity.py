@@ -144,6 +144,16 @@ def test_outputs_of_budget_rows(cuda_ok, n_cached, budget):
         torch.cuda.synchronize()
         assert torch.equal(nK, cK) and torch.equal(nV, cV)
         assert torch.equal(g, cV)
+        # a scoring variant (Z formed in the select + gather, or the separate
+        # variant kernel for long rows) writes the same rows either way
+        vK, vV, vi = rkv.rkv_compress_ex(K, V, Q, *args, redundancy_softmax=True, pool_window=5)
+        bK = torch.empty_like(cK)
+        bV = torch.empty_like(cV)
+        _, _, vi2 = rkv.rkv_compress_ex(K, V, Q, *args, redundancy_softmax=True, pool_window=5,
+                                        out_K=bK, out_V=bV)
+        torch.cuda.synchronize()
+        assert torch.equal(vi, vi2)
+        assert torch.equal(bK, vK[:, :w.budget]) and torch.equal(bV, vV[:, :w.budget])
 
 
 def _variant_check(w, K, V, Q, problems, softmax, window, in_place=False):
