@@ -358,8 +358,10 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 // multiplied once and its logits stay in TMEM while the epilogue sweeps them
 // three times (row max, sum of exponentials, probabilities); the keys are
 // read from memory once.  TMEM is a ring of NS slots of SC columns (the query
-// rows, padded); sweep 3 releases a block's slot, so the MMAs of the next
-// problem run while this one is swept and the key stream keeps going.
+// rows, padded); sweep 2 writes each exponential back over its logit
+// (tcgen05.st), so sweep 3 only scales them, and sweep 3 releases a block's
+// slot, so the MMAs of the next problem run while this one is swept and the
+// key stream keeps going.
 // NS >= T keeps the ring free of deadlock (a problem never waits for one of
 // its own slots).  The query rows are double-buffered.
 //
@@ -419,15 +421,33 @@ RKV_DEV void tmem_ld_row_nowait(uint32_t taddr, uint32_t (&r)[SC]) {
     if constexpr (SC > 32) tmem_ld16_at<32, SC>(taddr, r);
 }
 
+// r[OFF .. OFF+15] into 16 TMEM columns
+template <int OFF, int RP>
+RKV_DEV void tmem_st16_at(uint32_t taddr, const uint32_t (&r)[RP]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(
+            taddr + (uint32_t)OFF),
+        "r"(r[OFF + 0]), "r"(r[OFF + 1]), "r"(r[OFF + 2]), "r"(r[OFF + 3]), "r"(r[OFF + 4]),
+        "r"(r[OFF + 5]), "r"(r[OFF + 6]), "r"(r[OFF + 7]), "r"(r[OFF + 8]), "r"(r[OFF + 9]),
+        "r"(r[OFF + 10]), "r"(r[OFF + 11]), "r"(r[OFF + 12]), "r"(r[OFF + 13]), "r"(r[OFF + 14]),
+        "r"(r[OFF + 15])
+        : "memory");
+}
+
+// the SC columns of one row back into TMEM
+template <int SC>
+RKV_DEV void tmem_st_row(uint32_t taddr, const uint32_t (&r)[SC]) {
+    tmem_st16_at<0, SC>(taddr, r);
+    tmem_st16_at<16, SC>(taddr, r);
+    if constexpr (SC > 32) tmem_st16_at<32, SC>(taddr, r);
+}
+
+RKV_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 RKV_DEV float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-RKV_DEV float lg2_approx(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -785,7 +805,6 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
         const int full_blocks = (lim + 1) / kRows;
         const unsigned long long lastmask = prm.lastmask;
         const float scale2 = prm.scale2;   // log2(e) / sqrt(d)
-        const float log2_nobs = lg2_approx((float)n_obs);
         uint32_t ub = 0, ke = 0;           // ub: ring index of the problem's block 0
         bool ok = true;
         for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ub += (uint32_t)T) {
@@ -825,42 +844,55 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
             mlo *= scale2;
             mhi *= scale2;
             broadcast_columns<SC>(m, mlo, mhi);
-            // ---- sweep 2: sum of exponentials
+            // ---- sweep 2: sum of exponentials; each exponential (0 where the
+            // query does not see the key) replaces its logit in TMEM, so that
+            // sweep 3 only scales them
             float sm[SC];
 #pragma unroll
             for (int c = 0; c < SC; ++c) sm[c] = 0.f;
             for (int b = grp; b < T; b += 2) {
                 const uint32_t slot = (ub + (uint32_t)b) % NS;
+                const uint32_t taddr = tmem + lane_off + slot * (uint32_t)SC;
                 tc_fence_after();
                 uint32_t r[SC];
-                tmem_ld_row_nowait<SC>(tmem + lane_off + slot * (uint32_t)SC, r);
+                tmem_ld_row_nowait<SC>(taddr, r);
                 tmem_ld_wait();
                 if (b < full_blocks) {
 #pragma unroll
-                    for (int c = 0; c < SC; ++c)
-                        sm[c] += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                    for (int c = 0; c < SC; ++c) {
+                        const float e = ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                        sm[c] += e;
+                        r[c] = __float_as_uint(e);
+                    }
                 } else {
                     const int j = b * kRows + row;
                     const unsigned long long vm =
                         j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
 #pragma unroll
-                    for (int c = 0; c < SC; ++c)
-                        if ((vm >> c) & 1ull)
-                            sm[c] += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                    for (int c = 0; c < SC; ++c) {
+                        const float e =
+                            ((vm >> c) & 1ull)
+                                ? ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]))
+                                : 0.f;
+                        sm[c] += e;
+                        r[c] = __float_as_uint(e);
+                    }
                 }
+                tmem_st_row<SC>(taddr, r);
             }
+            tmem_st_wait();
             post_partials<SC>(sm, redS, ew, OpAdd{});
             mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
-            // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(x - m')
+            // p / n_obs = e * (1 / (sum * n_obs)): m now holds the column scales
             {
                 float slo, shi;
                 fold_partials<SC>(redS, slo, shi, OpAdd{});
-                mlo += lg2_approx(slo) + log2_nobs;
-                if constexpr (SC > 32) mhi += lg2_approx(shi) + log2_nobs;
-                broadcast_columns<SC>(m, mlo, mhi);
+                const float ilo = 1.0f / (slo * (float)n_obs);
+                const float ihi = SC > 32 ? 1.0f / (shi * (float)n_obs) : 0.f;
+                broadcast_columns<SC>(m, ilo, ihi);
             }
             // ---- sweep 3: probabilities -> importance; frees the slot
             for (int b = grp; b < T; b += 2) {
@@ -872,28 +904,13 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 tmem_ld_wait();
                 tc_fence_before();
                 mbar_arrive_warp(&tmem_free[slot]);
-                const unsigned long long vm =
-                    b < full_blocks ? ~0ull
-                                    : (j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull));
                 float best = -INFINITY, acc = 0.f;
-                if (b < full_blocks) {
 #pragma unroll
-                    for (int c = 0; c < SC; ++c) {
-                        acc += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
-                        if (HEAD > 0 ? (c % (HEAD > 0 ? HEAD : 1) == HEAD - 1) : ((lastmask >> c) & 1ull)) {
-                            best = fmaxf(best, acc);  // last query row of a head
-                            acc = 0.f;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < SC; ++c) {
-                        if ((vm >> c) & 1ull)
-                            acc += ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
-                        if ((lastmask >> c) & 1ull) {
-                            best = fmaxf(best, acc);
-                            acc = 0.f;
-                        }
+                for (int c = 0; c < SC; ++c) {
+                    acc = fmaf(__uint_as_float(r[c]), m[c], acc);
+                    if (HEAD > 0 ? (c % (HEAD > 0 ? HEAD : 1) == HEAD - 1) : ((lastmask >> c) & 1ull)) {
+                        best = fmaxf(best, acc);  // last query row of a head
+                        acc = 0.f;
                     }
                 }
                 if (j < N) prm.I[p * prm.ld + j] = best;
