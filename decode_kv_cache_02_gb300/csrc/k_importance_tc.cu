@@ -13,8 +13,10 @@
 // RP = 48, fp32 accumulators in TMEM.  The s columns give k_i . s, which
 // completes the redundancy row sum sum_i = inv_i (k_i . s) - |khat_i|^2 (the
 // key-stats kernel leaves |khat_i|^2 in sum_i) without another pass over K.
-// One epilogue thread owns one key row of the block.  Two passes over the
-// problem's keys (the second is expected to hit L2):
+// One epilogue thread owns one key row of a block; two groups of four warps
+// take alternate blocks (the MMA order's even and odd accumulators), so two
+// warps per scheduler hide the latency of the exponentials.  Two passes over
+// the problem's keys (the second is expected to hit L2):
 //   pass 1  per-thread online (max, sum of exp) per query row, then a block
 //           reduction (warp shuffles + shared memory) to the row's max M_c and
 //           1 / sum_j exp(l - M_c);
@@ -41,8 +43,8 @@ using namespace tc;
 constexpr int kRows = 128;
 constexpr int kChunkElems = 64;
 constexpr int kChunkBytes = kRows * 128;
-constexpr int kThreads = 192;
-constexpr int kEpi = 128;
+constexpr int kThreads = 320;
+constexpr int kEpi = 256;  // two groups of four warps taking alternate key blocks
 constexpr int kAcc = 4;            // accumulators in flight
 constexpr int kAccCols = 64;       // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 256;
@@ -56,7 +58,7 @@ struct ICfg {
     static constexpr int kStages = D == 128 ? 5 : 10;
     static constexpr size_t kQOff = (size_t)kStages * kBlockBytes;
     static constexpr size_t kRedOff = kQOff + (size_t)KC * kQChunkBytes;
-    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 8 * RP;
+    static constexpr size_t kBarOff = kRedOff + sizeof(float) * 16 * RP;
     static constexpr int kNumBars = 2 * kStages + 2 + 2 * kAcc + 2;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
 };
@@ -96,6 +98,25 @@ RKV_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 
+// one TMEM column (no wait)
+RKV_DEV uint32_t tmem_ld_1col(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
+// 2^x and log2(x) by the approximate PTX instructions (flush-to-zero)
+RKV_DEV float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+RKV_DEV float lg2_fast(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <int D, int RP>
 __global__ void __launch_bounds__(kThreads, 1)
 importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -107,8 +128,8 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sK = smem;
     uint8_t* sQ = smem + C::kQOff;
-    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [4][RP]
-    float* redS = redM + 4 * RP;                                 // [4][RP]
+    float* redM = reinterpret_cast<float*>(smem + C::kRedOff);  // [8][RP]
+    float* redS = redM + 8 * RP;                                 // [8][RP]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* k_full = bars;
     uint64_t* k_empty = k_full + C::kStages;
@@ -136,7 +157,7 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         mbar_init(q_empty, 1);
         for (int a = 0; a < kAcc; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], kEpi / 32);
+            mbar_init(&acc_empty[a], kEpi / 64);  // the four warps of one group
         }
         mbar_init(epi_bar, kEpi / 32);
         mbar_init(drain_bar, 1);
@@ -228,11 +249,17 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             mbar_wait(drain_bar, 0, &never);
         }
     } else {
-        const int qd = warp & 3;
+        const int qd = warp & 3;            // TMEM lane quarter
+        const int ew = warp - 2;            // 0..7
+        const int grp = ew >> 2;            // takes the blocks of accumulator counter parity grp
         const int row = qd * 32 + lane;
         const uint32_t t_row = tmem + ((uint32_t)(qd * 32) << 16);
         const int lim = N - n_obs;  // key j is seen by query q iff j <= lim + q
-        const float inv_nobs = 1.0f / (float)n_obs;
+        // blocks whose rows all lie at or before N - n_obs: every query row
+        // sees every key there, no mask
+        const int full_blocks = (lim + 1) / kRows;
+        const float scale2 = prm.scale2;  // log2(e) / sqrt(d): logits in log2 units
+        const float log2_nobs = lg2_fast((float)n_obs);
         const unsigned long long lastmask = prm.lastmask;
         uint32_t ka = 0, ke = 0;
         bool ok = true;
@@ -243,41 +270,55 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                 m[c] = -INFINITY;
                 s[c] = 0.f;
             }
-            // ---- pass 1: online max / sum of exp per query row
-            for (int b = 0; b < T; ++b) {
-                const int a = ka % kAcc;
-                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (ka / kAcc) & 1, s_abort));
+            // ---- pass 1: online max / sum of exp per query row (log2 units)
+            const uint32_t ka1 = ka;  // accumulator counter of the pass's block 0
+            for (int b = (grp + (int)(ka1 & 1)) & 1; b < T; b += 2) {
+                const uint32_t kb = ka1 + (uint32_t)b;
+                const int a = kb % kAcc;
+                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (kb / kAcc) & 1, s_abort));
                 if (!ok) break;
                 tc_fence_after();
                 const int j = b * kRows + row;
                 const unsigned long long vm =
-                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                    b < full_blocks ? ~0ull
+                                    : (j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull));
 #pragma unroll
                 for (int cc = 0; cc < RP / 16; ++cc) {
                     uint32_t r[16];
                     tmem_ld_16cols(t_row + (uint32_t)(a * kAccCols + cc * 16), r);
                     tmem_ld_wait();
+                    if (b < full_blocks) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = cc * 16 + e;
-                        if ((vm >> c) & 1ull) {
-                            const float l = __uint_as_float(r[e]) * prm.scale;
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = cc * 16 + e;
+                            const float l = __uint_as_float(r[e]) * scale2;
                             const float mn = fmaxf(m[c], l);
-                            s[c] = s[c] * __expf(m[c] - mn) + __expf(l - mn);
+                            s[c] = fmaf(s[c], ex2_fast(m[c] - mn), ex2_fast(l - mn));
                             m[c] = mn;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = cc * 16 + e;
+                            if ((vm >> c) & 1ull) {
+                                const float l = __uint_as_float(r[e]) * scale2;
+                                const float mn = fmaxf(m[c], l);
+                                s[c] = fmaf(s[c], ex2_fast(m[c] - mn), ex2_fast(l - mn));
+                                m[c] = mn;
+                            }
                         }
                     }
                 }
                 tc_fence_before();
                 mbar_arrive_warp(&acc_empty[a]);
-                ++ka;
             }
             if (!ok) break;
+            ka = ka1 + (uint32_t)T;
             // ---- block reduction: row max, then the rescaled sums
 #pragma unroll
             for (int c = 0; c < RP; ++c) {
                 const float mx = warp_max(m[c]);
-                if (lane == 0) redM[qd * RP + c] = mx;
+                if (lane == 0) redM[ew * RP + c] = mx;
             }
             mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
@@ -285,61 +326,84 @@ importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             if (!ok) break;
 #pragma unroll
             for (int c = 0; c < RP; ++c) {
-                const float M = fmaxf(fmaxf(redM[c], redM[RP + c]), fmaxf(redM[2 * RP + c], redM[3 * RP + c]));
-                const float part = (m[c] == -INFINITY) ? 0.f : s[c] * __expf(m[c] - M);
+                float M = redM[c];
+#pragma unroll
+                for (int w = 1; w < kEpi / 32; ++w) M = fmaxf(M, redM[w * RP + c]);
+                const float part = (m[c] == -INFINITY) ? 0.f : s[c] * ex2_fast(m[c] - M);
                 const float ws = warp_sum(part);
-                if (lane == 0) redS[qd * RP + c] = ws;
+                if (lane == 0) redS[ew * RP + c] = ws;
                 m[c] = M;
             }
             mbar_arrive_warp(epi_bar);
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, ke & 1, s_abort));
             ++ke;
             if (!ok) break;
+            // fold 1 / (sum * n_obs) into the exponent: p / n_obs = exp2(l - m')
 #pragma unroll
-            for (int c = 0; c < RP; ++c)
-                s[c] = 1.0f / ((redS[c] + redS[RP + c]) + (redS[2 * RP + c] + redS[3 * RP + c]));
+            for (int c = 0; c < RP; ++c) {
+                float S = 0.f;
+#pragma unroll
+                for (int w = 0; w < kEpi / 32; ++w) S += redS[w * RP + c];
+                m[c] += lg2_fast(S) + log2_nobs;
+            }
             // ---- pass 2: probabilities -> importance
-            for (int b = 0; b < T; ++b) {
-                const int a = ka % kAcc;
-                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (ka / kAcc) & 1, s_abort));
+            const uint32_t ka2 = ka;
+            for (int b = (grp + (int)(ka2 & 1)) & 1; b < T; b += 2) {
+                const uint32_t kb = ka2 + (uint32_t)b;
+                const int a = kb % kAcc;
+                ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (kb / kAcc) & 1, s_abort));
                 if (!ok) break;
                 tc_fence_after();
                 const int j = b * kRows + row;
                 const unsigned long long vm =
-                    j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull);
+                    b < full_blocks ? ~0ull
+                                    : (j <= lim ? s_colmask[0] : (j < N ? s_colmask[j - lim] : 0ull));
                 float iv = 0.f, self = 0.f;
                 if (j < N) {
                     iv = prm.inv_norm[p * prm.ld_ws + j];
                     self = prm.sum_s[p * prm.ld_ws + j];
                 }
-                float best = -INFINITY, acc = 0.f, dot = 0.f;
+                // k_j . s: the two s columns (R, R + 1) of the accumulator
+                const uint32_t s_hi = tmem_ld_1col(t_row + (uint32_t)(a * kAccCols + prm.R));
+                const uint32_t s_lo = tmem_ld_1col(t_row + (uint32_t)(a * kAccCols + prm.R + 1));
+                float best = -INFINITY, acc = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < RP / 16; ++cc) {
                     uint32_t r[16];
                     tmem_ld_16cols(t_row + (uint32_t)(a * kAccCols + cc * 16), r);
                     tmem_ld_wait();
+                    if (b < full_blocks) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = cc * 16 + e;
-                        if ((vm >> c) & 1ull) {
-                            const float l = __uint_as_float(r[e]) * prm.scale;
-                            acc += __expf(l - m[c]) * s[c];
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = cc * 16 + e;
+                            acc += ex2_fast(fmaf(__uint_as_float(r[e]), scale2, -m[c]));
+                            if ((lastmask >> c) & 1ull) {  // last query row of a head
+                                best = fmaxf(best, acc);
+                                acc = 0.f;
+                            }
                         }
-                        if ((lastmask >> c) & 1ull) {  // last query row of a head
-                            best = fmaxf(best, acc * inv_nobs);
-                            acc = 0.f;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int c = cc * 16 + e;
+                            if ((vm >> c) & 1ull)
+                                acc += ex2_fast(fmaf(__uint_as_float(r[e]), scale2, -m[c]));
+                            if ((lastmask >> c) & 1ull) {
+                                best = fmaxf(best, acc);
+                                acc = 0.f;
+                            }
                         }
-                        if (c == prm.R || c == prm.R + 1) dot += __uint_as_float(r[e]);
                     }
                 }
+                const float dot = __uint_as_float(s_hi) + __uint_as_float(s_lo);
                 tc_fence_before();
                 mbar_arrive_warp(&acc_empty[a]);
-                ++ka;
                 if (j < N) {
                     prm.I[p * prm.ld + j] = best;
                     prm.sum_s[p * prm.ld_ws + j] = iv * dot - self;
                 }
             }
+            ka = ka2 + (uint32_t)T;
         }
         if (!ok) {
             *s_abort = 1;
@@ -444,12 +508,6 @@ RKV_DEV void tmem_st_row(uint32_t taddr, const uint32_t (&r)[SC]) {
 }
 
 RKV_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-RKV_DEV float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 struct OpMax {
     RKV_DEV float operator()(float a, float b) const { return fmaxf(a, b); }
@@ -860,7 +918,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                 if (b < full_blocks) {
 #pragma unroll
                     for (int c = 0; c < SC; ++c) {
-                        const float e = ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
+                        const float e = ex2_fast(fmaf(__uint_as_float(r[c]), scale2, -m[c]));
                         sm[c] += e;
                         r[c] = __float_as_uint(e);
                     }
@@ -872,7 +930,7 @@ importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
                     for (int c = 0; c < SC; ++c) {
                         const float e =
                             ((vm >> c) & 1ull)
-                                ? ex2_approx(fmaf(__uint_as_float(r[c]), scale2, -m[c]))
+                                ? ex2_fast(fmaf(__uint_as_float(r[c]), scale2, -m[c]))
                                 : 0.f;
                         sm[c] += e;
                         r[c] = __float_as_uint(e);
