@@ -43,14 +43,14 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # with the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "54f754774cbf516d43bc7bf926acacf4e3b721a7b9d99ea02eb4e8af742494fa", 314090496 / 1024),
+        "key_stats": ("k_key_stats.cu", "03897fc1bf8d43d84450d36afa083d6d16ef1ead924e20c4f9882ac2b9628bd2", 315437568 / 1024),
         "importance_tc": ("k_importance_tc.cu", "05779ee5a23e7a83691687af581eaf14ab8639e98c03fcf69af01bb3fe1ee170", 329676032 / 1024),
         "gram_tc": ("k_gram_tc.cu", "a1f22fe57dc911bcf1473e9384d3fd56fa116ec9d5a4da73ee4233057aced27d", 323257344 / 1024),
         "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", 1035325952 / 1024),
     },
     # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
-        "key_stats_paged": ("k_key_stats.cu", "54f754774cbf516d43bc7bf926acacf4e3b721a7b9d99ea02eb4e8af742494fa", 316516096 / 1024),
+        "key_stats_paged": ("k_key_stats.cu", "03897fc1bf8d43d84450d36afa083d6d16ef1ead924e20c4f9882ac2b9628bd2", 316715008 / 1024),
         "compact_paged": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", 966686464 / 1024),
     },
 }

@@ -65,8 +65,13 @@ struct Raw8 {
     RKV_DEV void to_float(float* o) const { load8(reinterpret_cast<const T*>(u), o); }
 };
 
+// Rows of one batch per thread in pass 1 of the contiguous kernel: kept packed
+// until each is reduced, so eight bf16 rows (32 registers) stay in flight.
+template <typename T>
+constexpr int kRowsInFlight = sizeof(T) == 2 ? 8 : 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ inv_norm,
                  float* __restrict__ sum_s, int64_t ld, bool two_pass,
                  __nv_bfloat16* __restrict__ s_rows) {
@@ -84,24 +89,27 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc[t] = 0.f;
     // ---- pass 1: norms and the partial sums of khat
-    for (int base = r0; base < N; base += RPI * kUnroll) {
-        float v[kUnroll][8];
+    constexpr int KU = kRowsInFlight<T>;
+    for (int base = r0; base < N; base += RPI * KU) {
+        Raw8<T> raw[KU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < KU; ++u) {
             const int i = base + u * RPI;
-            if (i < N) {
-                load8(Kp + (size_t)i * D + col, v[u]);
-            } else {
-#pragma unroll
-                for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
-            }
+            if (i < N) raw[u].load(Kp + (size_t)i * D + col);
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
+        for (int u = 0; u < KU; ++u) {
             const int i = base + u * RPI;
+            float v[8];
+            if (i < N) {
+                raw[u].to_float(v);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[t] = 0.f;
+            }
             float n2 = 0.f;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) n2 = fmaf(v[u][t], v[u][t], n2);
+            for (int t = 0; t < 8; ++t) n2 = fmaf(v[t], v[t], n2);
             n2 = group_sum<L>(n2);
             const float inv = 1.0f / fmaxf(sqrtf(n2), 1e-12f);
             if (i < N) {
@@ -111,7 +119,7 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
                     if (!two_pass) sum_s[p * ld + i] = (n2 * inv) * inv;
                 }
 #pragma unroll
-                for (int t = 0; t < 8; ++t) acc[t] = fmaf(v[u][t], inv, acc[t]);
+                for (int t = 0; t < 8; ++t) acc[t] = fmaf(v[t], inv, acc[t]);
             }
         }
     }
