@@ -82,7 +82,7 @@ typedef struct {
     int64_t num_problems; /* P = layers * sequences * kv_heads (>= 0)        */
     int32_t gqa_group;    /* G, query heads per KV head, 1..16               */
     int32_t head_dim;     /* d, 64 or 128                                    */
-    int32_t n_capacity;   /* rows allocated per problem in K/V/out_K/out_V   */
+    int32_t n_capacity;   /* rows allocated per problem in K and V           */
     int32_t dtype;        /* RKV_DTYPE_BF16 or RKV_DTYPE_FP32 (K, V, Q, out) */
     int32_t out_capacity; /* rows per problem in out_K/out_V (and rkv_gather's
                              dst); 0 = n_capacity.  Must be >= budget, and 0 or
@@ -303,8 +303,9 @@ int rkv_select(int64_t num_problems, int n, const float* Z, int n_obs, int budge
                int32_t* out_idx, void* stream);
 
 /* The copy alone: dst[p, r, :] = src[p, idx[p, r], :] for r < budget where
- * idx >= 0, src and dst laid out as K in `desc`; idx rows strictly ascending.
- * dst may equal src (in place) but must not overlap it otherwise. */
+ * idx >= 0; src laid out as K in `desc`, dst as out_K (out_capacity rows per
+ * problem); idx rows strictly ascending.  dst may equal src (in place, with
+ * out_capacity 0 or n_capacity) but must not overlap it otherwise. */
 int rkv_gather(const rkv_desc* desc, const void* src, const int32_t* idx, int budget,
                void* dst, void* stream);
 
