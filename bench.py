@@ -198,18 +198,35 @@ def work_model(w: wl.Workload) -> dict:
     }
 
 
-def roofline(kernels: dict, model: dict, peaks: dict, steps: int, w=None) -> dict:
+# a timed region shorter than this is a burst: the tensor-bound kernel is held
+# to the burst bf16 peak (measured over a short loop at full clocks), a longer
+# one to the sustained peak (a seconds-long loop under the power cap)
+SUSTAINED_REGION_MS = 1000.0
+
+
+def tensor_peak(peaks: dict, region_ms: float):
+    """(peak TFLOP/s, description) for a tensor-bound kernel timed inside a
+    region of region_ms milliseconds."""
+    if region_ms < SUSTAINED_REGION_MS:
+        return peaks["bf16_tflops"], ("bf16 burst (of " + peaks["source"] + "; timed region "
+                                      f"{region_ms:.0f} ms < {SUSTAINED_REGION_MS:.0f} ms)")
+    return peaks["bf16_tflops_sustained"], ("bf16 sustained (of " + peaks["source"] +
+                                            f"; timed region {region_ms:.0f} ms)")
+
+
+def roofline(kernels: dict, model: dict, peaks: dict, steps: int, w=None,
+             region_ms: float = 0.0) -> dict:
     """Roofline of the kernel with the largest device time."""
     name = max(kernels, key=lambda k: kernels[k]["ms"])
-    ms = kernels[name]["ms"] / max(1, kernels[name]["launches"]) if kernels[name]["launches"] \
-        else kernels[name]["ms"]
     per_launch_ms = kernels[name]["ms"] / max(1, kernels[name]["launches"])
     m = model.get(name, {})
     if name == "gram_tc":
         achieved = m["flops"] / (per_launch_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak, kind = tensor_peak(peaks, region_ms)
         r = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
-             "unit": "TFLOP/s", "peak_kind": "bf16 sustained (of " + peaks["source"] + ")"}
+             "unit": "TFLOP/s", "peak_kind": kind,
+             "frac_of_burst": achieved / peaks["bf16_tflops"],
+             "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     elif name == "gram_simt":
         achieved = m["flops"] / (per_launch_ms * 1e-3) / 1e12
         peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
@@ -223,8 +240,26 @@ def roofline(kernels: dict, model: dict, peaks: dict, steps: int, w=None) -> dic
     r["frac"] = r["achieved"] / r["peak"]
     r["ms_per_launch"] = per_launch_ms
     r["traffic"] = measured_traffic(w.name, name, w.problems) if w is not None else None
-    del ms
     return r
+
+
+def roofline_all(kernels: dict, model: dict, peaks: dict, w, region_ms: float) -> dict:
+    """Every kernel's time per launch with its fraction of the HBM roof (and
+    of the tensor roof for the Gram)."""
+    out = {}
+    for k, v in kernels.items():
+        if k not in model or not v["launches"]:
+            continue
+        per = v["ms"] / v["launches"] * 1e-3
+        m = model[k]
+        entry = {"ms_per_launch": per * 1e3, "traffic": measured_traffic(w.name, k, w.problems)}
+        if "bytes" in m:
+            entry["hbm_frac"] = m["bytes"] / per / 1e9 / peaks["hbm_gbs"]
+        if k == "gram_tc":
+            entry["tensor_frac"] = m["flops"] / per / 1e12 / tensor_peak(peaks, region_ms)[0]
+            entry["tensor_frac_of_burst"] = m["flops"] / per / 1e12 / peaks["bf16_tflops"]
+        out[k] = entry
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -446,7 +481,7 @@ def run_paged(args, w):
     n_free = rkv.rkv_paged_freed_per_seq(K_pool, table, N, w.budget)
     idx = torch.empty((S * H, w.budget), dtype=torch.int32, device=dev)
     freed = torch.empty((S, n_free), dtype=torch.int32, device=dev)
-    ws = torch.zeros(rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, N, w.n_obs),
+    ws = torch.zeros(rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, N, w.n_obs, w.beta),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     sent = _sentences(args, w, dev)
@@ -583,20 +618,9 @@ def run_ours(args, w):
             line["config"]["variant"]["sentences"] = {
                 "sequences": sent.reps.shape[0], "max_sentences": sent.reps.shape[1],
                 "hidden": sent.reps.shape[2], "tau": sent.tau}
-    line["roofline"] = roofline(kernels, model, peaks, args.steps, w)
+    line["roofline"] = roofline(kernels, model, peaks, args.steps, w, region_ms=elapsed)
     # all kernels' fractions, for the record
-    line["roofline_all"] = {}
-    for k, v in kernels.items():
-        if k not in model or not v["launches"]:
-            continue
-        per = v["ms"] / v["launches"] * 1e-3
-        m = model[k]
-        entry = {"ms_per_launch": per * 1e3, "traffic": measured_traffic(w.name, k, w.problems)}
-        if "bytes" in m:
-            entry["hbm_frac"] = m["bytes"] / per / 1e9 / peaks["hbm_gbs"]
-        if k == "gram_tc":
-            entry["tensor_frac"] = m["flops"] / per / 1e12 / peaks["bf16_tflops_sustained"]
-        line["roofline_all"][k] = entry
+    line["roofline_all"] = roofline_all(kernels, model, peaks, w, elapsed)
 
     if not args.no_e2e:
         line["e2e"] = e2e(args, w, K, V, Q, out_K, out_V, idx, ws, stream, world, sent)
@@ -720,6 +744,7 @@ def run_stream(args, w):
     ws = rkv.alloc_workspace(K, w.gqa, cap, w.n_obs)
     stream = torch.cuda.current_stream()
     n, rounds, total_ms, launches = 0, 0, 0.0, 0
+    work = {}  # algorithmic bytes / flops of every kernel, summed over the rounds
     rkv.rkv_timing_read(reset=True)
     with ClockSampler(local) as clocks:
         while src.t < w.gen_tokens:
@@ -740,6 +765,10 @@ def run_stream(args, w):
             s1.synchronize()
             total_ms += s0.elapsed_time(s1)
             rounds += 1
+            for k, m in work_model(w.scaled(n_cached=n)).items():
+                acc = work.setdefault(k, {})
+                for unit, v in m.items():
+                    acc[unit] = acc.get(unit, 0.0) + v
             n = w.budget
     timing = rkv.rkv_timing_read(reset=True)
     launches = sum(v[1] for v in timing.values())
@@ -759,7 +788,32 @@ def run_stream(args, w):
         "kernels_ms_total": {k: v[0] for k, v in timing.items() if v[1]},
         "clocks": clocks.summary(),
     }
+    # rooflines over the whole stream: each kernel's summed algorithmic work
+    # over its summed time (the work model is per round, so with `launches`
+    # set to 1 the per-launch figures are the stream's totals)
+    kernels = {k: {"ms": v[0], "launches": 1} for k, v in timing.items() if v[1]}
+    peaks = _peaks()
+    line["roofline"] = roofline(kernels, work, peaks, rounds, w, region_ms=total_ms)
+    line["roofline"]["traffic"] = None
+    line["roofline_all"] = roofline_all(kernels, work, peaks, w, total_ms)
+    for e in line["roofline_all"].values():
+        e["ms_total"] = e.pop("ms_per_launch")
+        e["traffic"] = None
     print(json.dumps(line), flush=True)
+
+
+def run_all_configs(args):
+    """One JSON line per workload of the table (tiny, Llama-8B layer, Llama-8B
+    full step, Qwen-14B step, decode stream), each with its rooflines; the
+    end-to-end and CPU legs are left to the single-workload runs."""
+    args.no_e2e = True
+    args.no_cpu_baseline = True
+    for w in wl.WORKLOADS:
+        if w.gen_tokens:
+            run_stream(args, w)
+        else:
+            run_ours(args, w)
+        torch.cuda.empty_cache()
 
 
 def main():
@@ -798,7 +852,12 @@ def main():
                     help="schedule: sampling temperature")
     ap.add_argument("--sweep", action="store_true",
                     help="time the step over a lambda/beta/tau/variant sweep, one line each")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="one line per workload (tiny .. stream), with rooflines")
     args = ap.parse_args()
+    if args.all_configs and args.impl == "ours":
+        run_all_configs(args)
+        return
     w = wl.WORKLOADS[args.config] if args.config is not None else wl.BY_NAME[args.workload]
     if args.seed is not None:
         w = w.scaled(seed=args.seed)

@@ -622,12 +622,13 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool gram_tc_supported(const ScoreArgs& a) {
+bool gram_tc_shape_ok(const ScoreArgs& a) {
     return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) && a.N >= 2 &&
            a.N <= kMaxBlocksLarge * kRows && a.P <= 0x7fffffff && (a.ld_ws % 4) == 0 &&
-           a.beta >= 0 && a.beta <= kNewerCap &&
-           encode_fn() != nullptr;
+           a.beta >= 0 && a.beta <= kNewerCap;
 }
+
+bool gram_tc_supported(const ScoreArgs& a) { return gram_tc_shape_ok(a) && encode_fn() != nullptr; }
 
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
     if (a.P == 0) return cudaSuccess;

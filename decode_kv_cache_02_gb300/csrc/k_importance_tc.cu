@@ -1071,10 +1071,14 @@ cudaError_t launch_d(const ScoreArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool importance_tc_supported(const ScoreArgs& a) {
+bool importance_tc_shape_ok(const ScoreArgs& a) {
     return a.dtype == RKV_DTYPE_BF16 && (a.d == 64 || a.d == 128) &&
            a.G * a.n_obs <= kMaxQueryRows && (a.G * a.n_obs) % 8 == 0 &&
-           a.N >= 2 && a.P <= 0x7fffffff && encode_fn() != nullptr;
+           a.N >= 2 && a.P <= 0x7fffffff;
+}
+
+bool importance_tc_supported(const ScoreArgs& a) {
+    return importance_tc_shape_ok(a) && encode_fn() != nullptr;
 }
 
 cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s) {

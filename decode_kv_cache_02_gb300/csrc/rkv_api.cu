@@ -247,7 +247,7 @@ int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, 
 int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
                float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
                const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr,
-               bool* paged_direct = nullptr) {
+               bool direct = false) {
     // I, R, Z as defined on the page (R may be null: not stored)
     ScoreArgs a{};
     a.K = K;
@@ -272,15 +272,11 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.ld_out = ld_out;
     a.status = w.status;
     ScoreArgs b = a;  // what the stages after the key statistics read
-    bool direct = false;
     if (pg) {
         a.pg = *pg;
-        // the tensor-core stages read bf16 pools with blocks of at least 128
-        // rows straight through the table; otherwise the key statistics write
-        // a contiguous copy for them
-        direct = d->dtype == RKV_DTYPE_BF16 && pg->log2bs >= kDirectLog2Block &&
-                 (int64_t)pg->H * pg->num_blocks < ((int64_t)1 << 31) &&
-                 rkv::gram_tc_supported(b) && rkv::importance_tc_supported(b);
+        // direct: the tensor-core stages read the pool straight through the
+        // table (paged_reads_pool); otherwise the key statistics write a
+        // contiguous copy for them
         if (direct) {
             b.pg = *pg;
             b.paged_direct = true;
@@ -290,7 +286,6 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
             b.n_cap = n_cached;
         }
     }
-    if (paged_direct) *paged_direct = direct;
     const bool gram_tc = rkv::gram_tc_supported(b);
     const bool imp_tc = rkv::importance_tc_supported(b);
     a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
@@ -424,6 +419,23 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
                     int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                     const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
                     void* workspace, size_t workspace_bytes, void* stream) {
+    return rkv::compress_call(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau,
+                              variant, out_K, out_V, out_idx, workspace, workspace_bytes, stream,
+                              false);
+}
+
+}  // extern "C"
+
+namespace rkv {
+
+// The body of rkv_compress_ex.  clear_status: once every argument check has
+// passed, the device error word at the start of the workspace is cleared
+// (enqueued before the first kernel), so a call that is rejected enqueues
+// nothing at all.
+int compress_call(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                  int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                  const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
+                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status) {
     VarFlags vf;
     int rc = check_variant(variant, &vf);
     if (rc) return rc;
@@ -459,6 +471,8 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
             workspace_bytes < kAlign)
             return RKV_ERR_WORKSPACE;
         if (P == 0) return RKV_OK;
+        if (clear_status && cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), s) != cudaSuccess)
+            return RKV_ERR_CUDA;
         cudaError_t e = timed(kIdentity, s, [&] {
             return rkv::launch_identity_idx(P, n_cached, budget, out_idx, s);
         });
@@ -481,6 +495,8 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
     const bool fused = rkv::compact_smem_bytes(n_cached, tail, budget,
                                                vf.zvar && variant->sentences) <= kCompactSmemMax;
     if (sample && !fused) return RKV_ERR_UNSUPPORTED;
+    if (clear_status && cudaMemsetAsync(w.status, 0, sizeof(DeviceStatus), s) != cudaSuccess)
+        return RKV_ERR_CUDA;
     if (!fused && (vf.zvar || tail > n_obs)) {
         rc = run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
                                 nullptr, nullptr, w.Z, w.ld, w, s);
@@ -514,9 +530,9 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
-// ---------------------------------------------------------------- paged --
+}  // namespace rkv
 
-}  // extern "C"
+// ---------------------------------------------------------------- paged --
 
 namespace {
 
@@ -553,16 +569,47 @@ size_t kc_bytes_for(const rkv_desc& flat, int n_cached) {
     return (size_t)flat.num_problems * n_cached * flat.head_dim * elem_size(flat.dtype);
 }
 
+// Whether the tensor-core stages read a paged pool straight through the
+// table (no contiguous key copy): bf16 pools with blocks of at least 128 rows
+// whose shapes the tensor-core importance and Gram take.  Smaller blocks split
+// a tile into boxes too small to keep the producers ahead (64-row blocks made
+// the Gram ~25% slower); they, fp32 pools and the CUDA-core paths read the
+// copy.
+bool paged_reads_pool(const rkv_paged_desc* d, const rkv_desc& flat, int n_cached, int n_obs,
+                      int beta) {
+    if (flat.dtype != RKV_DTYPE_BF16 || log2_exact(d->block_size) < kDirectLog2Block) return false;
+    if ((int64_t)d->num_kv_heads * d->num_blocks >= ((int64_t)1 << 31)) return false;
+    ScoreArgs b{};
+    b.P = flat.num_problems;
+    b.G = flat.gqa_group;
+    b.d = flat.head_dim;
+    b.N = n_cached;
+    b.n_obs = n_obs;
+    b.beta = beta;
+    b.dtype = flat.dtype;
+    b.ld_ws = row_pitch(n_cached);
+    return rkv::gram_tc_shape_ok(b) && rkv::importance_tc_shape_ok(b);
+}
+
+// The contiguous key copy a paged call needs (0 when the pool is read directly).
+size_t paged_kc_bytes(const rkv_paged_desc* d, const rkv_desc& flat, int n_cached, int n_obs,
+                      int beta) {
+    return paged_reads_pool(d, flat, n_cached, n_obs, beta) ? 0 : kc_bytes_for(flat, n_cached);
+}
+
 }  // namespace
 
 extern "C" {
 
-size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs) {
+size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs,
+                                int beta) {
     rkv_desc flat{};
     if (check_paged_desc(desc, &flat) != RKV_OK || n_cached < 1 || n_cached > flat.n_capacity ||
-        n_obs < 0)
+        n_obs < 0 || beta < 0)
         return 0;
-    return carve(nullptr, flat.num_problems, n_cached, kc_bytes_for(flat, n_cached)).bytes;
+    return carve(nullptr, flat.num_problems, n_cached,
+                 paged_kc_bytes(desc, flat, n_cached, n_obs, beta))
+        .bytes;
 }
 
 int rkv_paged_freed_per_seq(const rkv_paged_desc* desc, int n_cached, int budget) {
@@ -619,7 +666,17 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     if (rkv::compact_smem_bytes(n_cached, tail, budget, vf.zvar && variant->sentences) >
         kCompactSmemMax)
         return RKV_ERR_UNSUPPORTED;
-    const size_t kc = kc_bytes_for(flat, n_cached);
+    const bool direct = paged_reads_pool(desc, flat, n_cached, n_obs, beta);
+    const size_t kc = direct ? 0 : kc_bytes_for(flat, n_cached);
+    {
+        // the in-place read needs the tensor-core stages (the driver's
+        // tensor-map entry point); nothing else reads the pool directly
+        ScoreArgs b{};
+        b.P = P; b.G = flat.gqa_group; b.d = flat.head_dim; b.N = n_cached; b.n_obs = n_obs;
+        b.beta = beta; b.dtype = flat.dtype; b.ld_ws = row_pitch(n_cached);
+        if (direct && !(rkv::gram_tc_supported(b) && rkv::importance_tc_supported(b)))
+            return RKV_ERR_CUDA;
+    }
     if (workspace_bytes < carve(nullptr, P, n_cached, kc).bytes) return RKV_ERR_WORKSPACE;
     if (check_variant_sizes(variant, n_cached, n_obs, budget)) return RKV_ERR_INVALID_ARG;
     if (P == 0) return RKV_OK;
@@ -631,9 +688,8 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     pg.H = desc->num_kv_heads;
     pg.num_blocks = desc->num_blocks;
     if (vf.zvar && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
-    bool direct = false;
     rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
-                    vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg, &direct);
+                    vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg, direct);
     if (rc) return rc;
     rkv::VariantIn vin;
     if (vf.any()) vin = variant_in(*variant, vf, lambda, w, samples(variant, n_cached, budget));

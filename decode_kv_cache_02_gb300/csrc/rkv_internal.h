@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/rkv.h"
+
 namespace rkv {
 
 struct DeviceStatus;
@@ -64,9 +66,13 @@ struct ScoreArgs {
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_importance(const ScoreArgs& a, cudaStream_t s);
+// *_shape_ok: the sizes and parameters a tensor-core kernel takes;
+// *_supported: that, and the driver's tensor-map entry point is present.
+bool importance_tc_shape_ok(const ScoreArgs& a);
 bool importance_tc_supported(const ScoreArgs& a);
 cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_gram_simt(const ScoreArgs& a, cudaStream_t s);
+bool gram_tc_shape_ok(const ScoreArgs& a);
 bool gram_tc_supported(const ScoreArgs& a);
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);
 
@@ -145,5 +151,12 @@ cudaError_t launch_variant(int64_t P, int N, int n_obs, const VariantIn& v, floa
 // One bounded wait that nothing completes (the failure path of every wait):
 // records kDevErrTimeout in st after the wait limit (~1 s).
 cudaError_t launch_wait_timeout(DeviceStatus* st, cudaStream_t s);
+
+// rkv_compress_ex; with clear_status the workspace's device error word is
+// cleared (enqueued) once the arguments have passed every check.
+int compress_call(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
+                  int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
+                  const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
+                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status);
 
 }  // namespace rkv

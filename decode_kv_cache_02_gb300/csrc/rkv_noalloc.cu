@@ -10,44 +10,34 @@
 // file-scope __device__ array of fixed size, RKV_NOALLOC_SCRATCH_BYTES, which
 // every GPU that loads the library holds until the process exits.
 //
-// The array's name is only a host-side stand-in in host code, so the device
-// address is looked up with cudaGetSymbolAddress, once per device, on the
-// first call made while that device is current, and cached.  The call never
+// The array's name is only a host-side stand-in in host code, so every call
+// looks up the device address with cudaGetSymbolAddress on the current device
+// (a host-side lookup once the module is loaded; not caching it means a
+// context that was torn down and created again, which may place the module
+// elsewhere, is never written through a stale pointer).  The call never
 // allocates or frees device memory.  Every call shares the one array: its
-// device error word is cleared at the start of each call (the other scratch
-// regions are fully written before they are read), and two calls that may run
-// at the same time on the GPU (different streams, or different host threads)
-// race on it.
+// device error word is cleared by each call once the arguments have passed
+// their checks (the other scratch regions are fully written before they are
+// read), and two calls that may run at the same time on the GPU (different
+// streams, or different host threads) race on it.  The error word is read
+// back, and cleared, by rkv_noalloc_device_status.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "../../include/rkv.h"
 #include "rkv_common.cuh"
+#include "rkv_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RKV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array on the current device.
 cudaError_t scratch_for_current_device(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -63,9 +53,19 @@ extern "C" int rkv_compress_noalloc(const rkv_desc* desc, const void* K, const v
     if (need > (size_t)RKV_NOALLOC_SCRATCH_BYTES) return RKV_ERR_TOO_LARGE;
     void* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return RKV_ERR_CUDA;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, sizeof(rkv::DeviceStatus), s) != cudaSuccess)
-        return RKV_ERR_CUDA;
-    return rkv_compress(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau, out_K,
-                        out_V, out_idx, scratch, (size_t)RKV_NOALLOC_SCRATCH_BYTES, stream);
+    return rkv::compress_call(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau,
+                              nullptr, out_K, out_V, out_idx, scratch,
+                              (size_t)RKV_NOALLOC_SCRATCH_BYTES, stream, true);
+}
+
+extern "C" int rkv_noalloc_device_status(void* stream) {
+    void* scratch = nullptr;
+    if (scratch_for_current_device(&scratch) != cudaSuccess) return RKV_ERR_CUDA;
+    return rkv_get_device_status(scratch, stream);
+}
+
+extern "C" int rkv_noalloc_selftest_wait_timeout(void* stream) {
+    void* scratch = nullptr;
+    if (scratch_for_current_device(&scratch) != cudaSuccess) return RKV_ERR_CUDA;
+    return rkv_selftest_wait_timeout(scratch, stream);
 }

@@ -28,6 +28,7 @@ EXPORTED = [
     "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
     "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
     "rkv_sentence_reps", "rkv_sentence_penalty", "rkv_selftest_wait_timeout",
+    "rkv_noalloc_device_status", "rkv_noalloc_selftest_wait_timeout",
 ]
 RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_DEVICE = 6
@@ -168,7 +169,7 @@ def load(path: str | None = None):
                                      vp]
         lib.rkv_score_ex.restype = i32
         pdp = ctypes.POINTER(_PagedDesc)
-        lib.rkv_paged_workspace_size.argtypes = [pdp, i32, i32]
+        lib.rkv_paged_workspace_size.argtypes = [pdp, i32, i32, i32]
         lib.rkv_paged_workspace_size.restype = sz
         lib.rkv_paged_freed_per_seq.argtypes = [pdp, i32, i32]
         lib.rkv_paged_freed_per_seq.restype = i32
@@ -181,6 +182,10 @@ def load(path: str | None = None):
         lib.rkv_sentence_penalty.restype = i32
         lib.rkv_selftest_wait_timeout.argtypes = [vp, vp]
         lib.rkv_selftest_wait_timeout.restype = i32
+        lib.rkv_noalloc_device_status.argtypes = [vp]
+        lib.rkv_noalloc_device_status.restype = i32
+        lib.rkv_noalloc_selftest_wait_timeout.argtypes = [vp]
+        lib.rkv_noalloc_selftest_wait_timeout.restype = i32
         lib.rkv_select.argtypes = [i64, i32, vp, i32, i32, vp, vp]
         lib.rkv_select.restype = i32
         lib.rkv_gather.argtypes = [dp, vp, vp, i32, vp, vp]
@@ -466,9 +471,12 @@ def make_paged_desc(K_pool: torch.Tensor, block_table: torch.Tensor, gqa_group: 
 
 
 def rkv_paged_workspace_size(K_pool, block_table, gqa_group: int, n_cached: int,
-                             n_obs: int) -> int:
+                             n_obs: int, beta: int = 2) -> int:
+    """Workspace bytes of rkv_paged_compress for these arguments (no
+    contiguous key copy when the tensor-core stages read the pool in place)."""
     desc = make_paged_desc(K_pool, block_table, gqa_group)
-    return int(load().rkv_paged_workspace_size(ctypes.byref(desc), int(n_cached), int(n_obs)))
+    return int(load().rkv_paged_workspace_size(ctypes.byref(desc), int(n_cached), int(n_obs),
+                                               int(beta)))
 
 
 def rkv_paged_freed_per_seq(K_pool, block_table, n_cached: int, budget: int) -> int:
@@ -505,7 +513,7 @@ def rkv_paged_compress(K_pool, V_pool, Q_obs, block_table, n_cached: int, budget
     if out_freed is None:
         out_freed = torch.empty((desc.num_seqs, n_free), dtype=torch.int32, device=K_pool.device)
     if workspace is None:
-        n = rkv_paged_workspace_size(K_pool, block_table, G, max(n_cached, 1), n_obs)
+        n = rkv_paged_workspace_size(K_pool, block_table, G, max(n_cached, 1), n_obs, beta)
         if n == 0:
             raise ValueError("invalid workspace request")
         workspace = torch.zeros(n, dtype=torch.uint8, device=K_pool.device)
@@ -557,3 +565,15 @@ def rkv_selftest_wait_timeout(workspace, stream=None):
     rkv_get_device_status(workspace) reports RKV_ERR_DEVICE."""
     _check(load().rkv_selftest_wait_timeout(workspace.data_ptr(), _stream_ptr(stream)),
            "rkv_selftest_wait_timeout")
+
+
+def rkv_noalloc_device_status(stream=None) -> int:
+    """Synchronises the stream; returns RKV_OK or the device error code
+    recorded in rkv_compress_noalloc's static scratch (and clears it)."""
+    return int(load().rkv_noalloc_device_status(_stream_ptr(stream)))
+
+
+def rkv_noalloc_selftest_wait_timeout(stream=None):
+    """rkv_selftest_wait_timeout on rkv_compress_noalloc's static scratch."""
+    _check(load().rkv_noalloc_selftest_wait_timeout(_stream_ptr(stream)),
+           "rkv_noalloc_selftest_wait_timeout")

@@ -91,12 +91,35 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
+WALK_CHUNK = 128  # tokens per batched step of the walk
+
+
+def _walk_matrices(n: int, device):
+    """For the walk over n tokens after a known value x: the tokens are
+    x_u = RHO^(u+1) * x + c * sum_{v <= u} RHO^(u-v) * e_v (u = 0..n-1, c =
+    sqrt(1 - RHO^2)); returns the lower-triangular [n, n] matrix of the
+    innovations' weights and the [n] weights of x (fp32)."""
+    c = math.sqrt(1.0 - RHO * RHO)
+    u = torch.arange(n, dtype=torch.float64)
+    lag = u[:, None] - u[None, :]
+    L = torch.where(lag >= 0, c * RHO ** lag.clamp(min=0), torch.zeros((), dtype=torch.float64))
+    return L.float().to(device), (RHO ** (u + 1)).float().to(device)
+
+
 def _ar1_walk_(k: torch.Tensor) -> torch.Tensor:
     """In place: k[:, 0] stays, k[:, t] = rho*k[:, t-1] + sqrt(1-rho^2)*k[:, t]
-    (the incoming values are the innovations).  Stationary variance 1."""
-    c = math.sqrt(1.0 - RHO * RHO)
-    for t in range(1, k.shape[1]):
-        k[:, t].mul_(c).add_(k[:, t - 1], alpha=RHO)
+    (the incoming values are the innovations).  Stationary variance 1.
+    Evaluated WALK_CHUNK tokens at a time in closed form (one batched matmul
+    per chunk) rather than token by token."""
+    T = k.shape[1]
+    if T < 2:
+        return k
+    L, pw = _walk_matrices(min(WALK_CHUNK, T - 1), k.device)
+    t0 = 1
+    while t0 < T:
+        n = min(WALK_CHUNK, T - t0)
+        k[:, t0:t0 + n] = torch.matmul(L[:n, :n], k[:, t0:t0 + n]) + pw[:n, None] * k[:, t0 - 1:t0]
+        t0 += n
     return k
 
 
@@ -164,13 +187,9 @@ def observation_queries(k_last: torch.Tensor, G: int, n_obs: int,
     """Q_obs [P, G, n_obs, d]: for each query head an independent continuation
     of the AR(1) walk for n_obs steps from the last cached key."""
     P, d = k_last.shape
-    c = math.sqrt(1.0 - RHO * RHO)
-    q = torch.empty(P, G, n_obs, d, device=k_last.device)
-    prev = k_last.float()[:, None, :].expand(P, G, d)
-    for t in range(n_obs):
-        prev = RHO * prev + c * torch.randn(P, G, d, generator=g, device=k_last.device)
-        q[:, :, t] = prev
-    return q
+    L, pw = _walk_matrices(n_obs, k_last.device)
+    e = torch.randn(P, G, n_obs, d, generator=g, device=k_last.device)
+    return torch.matmul(L, e) + pw[:, None] * k_last.float()[:, None, None, :]
 
 
 class StreamSource:

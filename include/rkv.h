@@ -276,10 +276,16 @@ typedef struct {
     int32_t dtype;              /* RKV_DTYPE_BF16 or RKV_DTYPE_FP32           */
 } rkv_paged_desc;
 
-/* Workspace bytes rkv_paged_compress needs (0 if the arguments are invalid):
- * the scratch of rkv_compress plus one contiguous copy of the P problems'
- * keys [P, n_cached, head_dim]. */
-size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs);
+/* Workspace bytes rkv_paged_compress needs for these arguments (0 if they
+ * are invalid).  bf16 pools with blocks of at least 128 rows are read in
+ * place by the tensor-core stages when the call's shapes fit them (n_cached
+ * <= 4352, gqa_group * n_obs a multiple of 8 up to 128, beta <= 63): then the
+ * size equals rkv_workspace_size() of the same problems.  Otherwise (blocks
+ * under 128 rows, fp32 pools, the CUDA-core paths) it adds one contiguous
+ * copy of the P problems' keys [P, n_cached, head_dim], which the key
+ * statistics write for the later stages. */
+size_t rkv_paged_workspace_size(const rkv_paged_desc* desc, int n_cached, int n_obs,
+                                int beta);
 
 /* Blocks freed per sequence: ceil(n_cached/bs) - ceil(budget/bs), or 0 when
  * n_cached <= budget; -1 if the arguments are invalid. */
@@ -329,15 +335,29 @@ int rkv_get_device_status(void* workspace, void* stream);
  * enqueued (16 MiB holds the scratch of about 700 thousand token slots, e.g.
  * one Llama-8B layer at batch 64 with N = 1152, or 195 problems of 4096).
  * Never allocates or frees device memory.
- * The first call on each device, made with that device current, looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that first
- * call before any stream capture.  All calls share the array (its error word
- * is cleared at the start of each call and not reported), so calls that may
- * overlap on the GPU race and must be serialised by the caller. */
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress, a host-side lookup).  The first lookup on a device
+ * may load the library's device code there; make the first call on each
+ * device before any stream capture: if the lookup fails (for instance because
+ * a capture forbids loading code), the call returns RKV_ERR_CUDA and enqueues
+ * nothing.  All calls share the array.  Once a call's arguments pass their
+ * checks it clears the array's device error word (enqueued on `stream` before
+ * its kernels); a rejected call enqueues nothing.  Calls that may overlap on
+ * the GPU race on the array and must be serialised by the caller. */
 #define RKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 int rkv_compress_noalloc(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
                          int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                          void* out_K, void* out_V, int32_t* out_idx, void* stream);
+
+/* rkv_get_device_status for rkv_compress_noalloc's static scratch on the
+ * current device: synchronises `stream`, returns RKV_ERR_DEVICE if a kernel
+ * recorded an error there since the last read (and clears it), RKV_OK
+ * otherwise. */
+int rkv_noalloc_device_status(void* stream);
+
+/* rkv_selftest_wait_timeout on the static scratch of the current device (the
+ * error word that rkv_noalloc_device_status reads). */
+int rkv_noalloc_selftest_wait_timeout(void* stream);
 
 /* Self-test of the failure path: enqueues one bounded wait that nothing
  * completes (the primitive every wait of the kernels uses).  After its limit

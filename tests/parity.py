@@ -5,8 +5,9 @@ absolute; kept sets identical except tokens whose oracle score lies within
 2e-3 of the k-th largest oracle score, or whose protection/similarity depends
 on a threshold-borderline pair (|S_ij - tau| < 1e-5); gathered rows
 bit-exact for the GPU's own indices.  Scoring variants (the redundancy
-softmax puts R near 1/C) take the same 2e-3 relative to each problem's scale
-max_i |X*_i|, which is never looser than the absolute bound there.
+softmax puts R near 1/C) take the same 2e-3 scaled by each problem's scale
+min(1, max_i |X*_i|): tighter than the absolute bound where the values are
+small, and never looser than it (a sentence penalty can push |Z*| past 1).
 """
 from __future__ import annotations
 
@@ -31,20 +32,21 @@ def score_errors(gpu: dict, sc: dict, C: int) -> dict:
 
 def scaled_score_errors(gpu: dict, sc: dict, C: int) -> dict:
     """Max over problems of the error of I, R, Z over the candidates relative
-    to the problem's scale max_i |X*_i| (for scoring variants whose values
-    are ~1/C, where an absolute 2e-3 would compare nothing)."""
+    to the problem's scale min(1, max_i |X*_i|) (for scoring variants whose
+    values are ~1/C, where an absolute 2e-3 would compare nothing; capped at
+    1 so the bound is never looser than the absolute one)."""
     out = {}
     for name in ("I", "R", "Z"):
         g = gpu[name].detach().cpu().double().numpy()[:, :C]
         ref = sc[name][:, :C]
-        scale = np.maximum(np.abs(ref).max(axis=1), 1e-300)
+        scale = np.clip(np.abs(ref).max(axis=1), 1e-300, 1.0)
         out[name] = float((np.abs(g - ref).max(axis=1) / scale).max())
     return out
 
 
 def scaled_band(sc: dict, C: int, rel: float = KEPT_BAND) -> np.ndarray:
-    """Per-problem tie band rel * max_i |Z*_i| over the candidates."""
-    return rel * np.abs(sc["Z"][:, :C]).max(axis=1)
+    """Per-problem tie band rel * min(1, max_i |Z*_i|) over the candidates."""
+    return rel * np.minimum(np.abs(sc["Z"][:, :C]).max(axis=1), 1.0)
 
 
 def check_observation_scores(gpu: dict, C: int):

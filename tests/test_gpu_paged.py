@@ -53,7 +53,8 @@ def _make_paged(w, bs, extra=5, seed=0, tail_garbage=True):
 def _paged_check(w, bs, problems=None, softmax=False, window=1, **kw):
     K_pool, V_pool, Q, table = _make_paged(w, bs, **kw)
     K0, V0, T0 = _raw(K_pool), _raw(V_pool), table.cpu().numpy()
-    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs)
+    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs,
+                                           w.beta)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
     idx, freed = rkv.rkv_paged_compress(K_pool, V_pool, Q, table, w.n_cached, w.budget, w.n_obs,
                                         w.lam, w.beta, w.tau, redundancy_softmax=softmax,
@@ -130,7 +131,8 @@ def test_paged_bad_block_id_is_reported():
                                            kv_heads=2, head_dim=64)
     K_pool, V_pool, Q, table = _make_paged(w, 16)
     table[1, 3] = K_pool.shape[0] + 11
-    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs)
+    ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs,
+                                           w.beta)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
     rkv.rkv_paged_compress(K_pool, V_pool, Q, table, w.n_cached, w.budget, w.n_obs,
                            workspace=ws)

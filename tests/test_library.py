@@ -136,9 +136,23 @@ def test_paged_sizes_and_argument_errors(lib):
     assert lib.rkv_paged_freed_per_seq(ctypes.byref(D(bs=12)), 1152, 1024) == -1  # not 2^k
     assert lib.rkv_paged_freed_per_seq(ctypes.byref(D(mb=10)), 1152, 1024) == -1  # > capacity
     flat = lib.rkv_workspace_size(ctypes.byref(_desc(P=32, n_cap=1152)), 1152, 8)
-    assert lib.rkv_paged_workspace_size(ctypes.byref(d), 1152, 8) == \
-        flat + (32 * 1152 * 128 * 2 + 255) // 256 * 256
-    assert lib.rkv_paged_workspace_size(ctypes.byref(D(bs=0)), 1152, 8) == 0
+    copy = (32 * 1152 * 128 * 2 + 255) // 256 * 256  # contiguous keys [P, N, d] bf16
+    # blocks under 128 rows: the key statistics write a contiguous copy
+    assert lib.rkv_paged_workspace_size(ctypes.byref(d), 1152, 8, 2) == flat + copy
+    # bf16 blocks of 128 rows or more are read in place by the tensor-core
+    # stages: exactly the contiguous call's workspace
+    for bs in (128, 256, 1024):
+        big = D(bs=bs, mb=(1152 + bs - 1) // bs, nb=4 * ((1152 + bs - 1) // bs))
+        assert lib.rkv_paged_workspace_size(ctypes.byref(big), 1152, 8, 2) == flat
+        assert lib.rkv_paged_workspace_size(ctypes.byref(big), 1152, 8, 63) == flat
+        # beta past the tensor-core Gram's cap and fp32 pools take the copy
+        assert lib.rkv_paged_workspace_size(ctypes.byref(big), 1152, 8, 64) == flat + copy
+        big32 = D(bs=bs, mb=(1152 + bs - 1) // bs, nb=4 * ((1152 + bs - 1) // bs), dtype=1)
+        flat32 = lib.rkv_workspace_size(ctypes.byref(_desc(P=32, n_cap=1152, dtype=1)), 1152, 8)
+        assert lib.rkv_paged_workspace_size(ctypes.byref(big32), 1152, 8, 2) == \
+            flat32 + 2 * copy
+    assert lib.rkv_paged_workspace_size(ctypes.byref(D(bs=0)), 1152, 8, 2) == 0
+    assert lib.rkv_paged_workspace_size(ctypes.byref(d), 1152, 8, -1) == 0
     fake = 1 << 20
     v = rkv._Variant(0, 1)
     call = lambda desc, n=1152, budget=1024, K=fake, V=fake + 2 ** 36, ws_bytes=1 << 40: \

@@ -36,6 +36,19 @@ def test_ar1_neighbour_similarity_and_repeats():
     assert abs(frac - w.repeat_prob) < 0.08
 
 
+def test_walk_closed_form_equals_recurrence():
+    # the chunked closed form of the walk against the recurrence applied token
+    # by token, across several chunks and a ragged tail
+    g = torch.Generator().manual_seed(5)
+    e = torch.randn(3, 2 * wl.WALK_CHUNK + 37, 16, generator=g, dtype=torch.float64)
+    ref = e.clone()
+    c = math.sqrt(1.0 - wl.RHO ** 2)
+    for t in range(1, ref.shape[1]):
+        ref[:, t] = wl.RHO * ref[:, t - 1] + c * ref[:, t]
+    got = wl._ar1_walk_(e.float().clone())
+    assert torch.allclose(got.double(), ref, atol=1e-5, rtol=0)
+
+
 def test_tiny_has_noisy_copies():
     w = wl.BY_NAME["tiny"]
     K, _, _ = wl.make_inputs(w)
