@@ -1,6 +1,7 @@
 // k_gram_tc.cu -- thresholded key Gram on the sm_103a tensor cores (tcgen05,
 // TMEM accumulators, TMA-fed shared memory), with recency protection, R and
-// Z computed in the epilogue.  The Gram itself never leaves the SM.
+// Z computed in the epilogue, for N <= 2048 (longer rows: k_gram_tc_pairs.cu).
+// The Gram itself never leaves the SM.
 //
 // R-KV review (yoonschallenge.tistory.com/1236): summary-table row
 // "redundancy" (cosine similarity of key vectors in one head; the beta most
@@ -30,9 +31,10 @@
 //     cp.async.bulk.tensor (3-D map [P][N][d], 128B swizzle, rows past N
 //     zero-filled); the problem's inverse norms arrive by cp.async.bulk into a
 //     double buffer one problem ahead.  No multicast.
-//   * warp 1: owns all 512 TMEM columns (four 128x128 fp32 accumulators); one
+//   * warp 1: owns all 512 TMEM columns (two 128x256 fp32 accumulators); one
 //     lane issues tcgen05.mma.cta_group::1.kind::f16 (bf16 x bf16 -> fp32,
-//     M = N = 128, K = 16 per instruction, exact products) and tcgen05.commit.
+//     M = 128, N = 256 -- two column blocks per instruction -- K = 16 per
+//     instruction, exact products) and tcgen05.commit.
 //   * warps 2..17 (512 threads, four per scheduler for latency hiding): the
 //     epilogue.  Warp w reads TMEM lanes 32*(w%4).. (one accumulator row per
 //     thread) and one 32-column quarter of the tile, then filters the 32x32
@@ -635,7 +637,8 @@ cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
     if (a.N <= kMaxBlocksSmall * kRows)
         return a.d == 128 ? launch_t<128, kMaxBlocksSmall, 2>(a, s)
                           : launch_t<64, kMaxBlocksSmall, 2>(a, s);
-    return a.d == 128 ? launch_t<128, kMaxBlocksLarge, 1>(a, s) : launch_t<64, kMaxBlocksLarge, 1>(a, s);
+    // longer rows: row pairs against streamed block pairs (k_gram_tc_pairs.cu)
+    return launch_gram_tc_pairs(a, s);
 }
 
 }  // namespace rkv

@@ -75,6 +75,8 @@ cudaError_t launch_gram_simt(const ScoreArgs& a, cudaStream_t s);
 bool gram_tc_shape_ok(const ScoreArgs& a);
 bool gram_tc_supported(const ScoreArgs& a);
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);
+// the tensor-core Gram for 2048 < N <= 4352 (launch_gram_tc dispatches to it)
+cudaError_t launch_gram_tc_pairs(const ScoreArgs& a, cudaStream_t s);
 
 cudaError_t launch_select(int64_t P, int N, const float* Z, int64_t ldz, int n_obs,
                           int budget, int32_t* idx, DeviceStatus* st, cudaStream_t s);
