@@ -158,7 +158,7 @@ RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
 // ---------------------------------------------------------------- kernel --
 template <int D, int MB, int W>
 __global__ void __launch_bounds__(kThreads, 1)
-gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap bmap,
+gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ KeyMaps bmap,
                const Params prm) {
     using C = Cfg<D, MB, W>;
     constexpr int kAccBufs = C::kAccBufs;
@@ -215,8 +215,8 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         mbar_init(drain_bar, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap))
-                     : "memory");
+        prefetch_key_maps(&tmap);
+        prefetch_key_maps(&bmap);
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, kTmemCols);
@@ -604,7 +604,7 @@ gram_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
 template <int D, int MB, int W>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D, MB, W>;
-    CUtensorMap map, bmap;
+    KeyMaps map, bmap;
     KeySource ks;
     if (!make_key_map(&map, a, D, kRows, &ks)) return cudaErrorInvalidValue;
     if (!make_key_map(&bmap, a, D, W * kRows, &ks))

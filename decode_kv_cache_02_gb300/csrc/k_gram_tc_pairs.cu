@@ -267,7 +267,7 @@ RKV_DEV float subtile(uint32_t (&r)[32], const float* inv, int* s_sim,
 // ---------------------------------------------------------------- kernel --
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-gram_tc_pairs_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm) {
+gram_tc_pairs_kernel(const __grid_constant__ KeyMaps tmap, const Params prm) {
     using C = Cfg<D>;
     constexpr int kMaxRows = C::kMaxRows;
     constexpr int MB = kMaxBlocks;
@@ -310,8 +310,7 @@ gram_tc_pairs_kernel(const __grid_constant__ CUtensorMap tmap, const Params prm)
         mbar_init(drain_bar, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap))
-                     : "memory");
+        prefetch_key_maps(&tmap);
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, kTmemCols);
@@ -621,7 +620,7 @@ template <int D>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D>;
     static_assert(C::kSmemBytes <= 232448, "shared memory over the per-CTA limit");
-    CUtensorMap map;
+    KeyMaps map;
     KeySource ks;
     if (!make_key_map(&map, a, D, kPairRows, &ks)) return cudaErrorInvalidValue;
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,

@@ -119,7 +119,7 @@ RKV_DEV float lg2_fast(float x) {
 
 template <int D, int RP>
 __global__ void __launch_bounds__(kThreads, 1)
-importance_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+importance_tc_kernel(const __grid_constant__ KeyMaps kmap,
                      const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap smap, const IParams prm) {
     using C = ICfg<D, RP>;
@@ -625,7 +625,7 @@ RKV_DEV float row_dot(const uint8_t* blk, int r, const float* s32) {
 // head's last row is known at compile time; HEAD == 0 reads it from lastmask.
 template <int D, int SC, int HEAD>
 __global__ void __launch_bounds__(kRThreads, 1)
-importance_tcr_kernel(const __grid_constant__ CUtensorMap kmap,
+importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                       const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap smap, const IParams prm) {
     using C = RCfg<D, SC>;
@@ -1025,7 +1025,8 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     const int64_t cap = (int64_t)sm_count();
     const int64_t grid = a.P < cap ? a.P : cap;
     const int T = (a.N + kRows - 1) / kRows;
-    CUtensorMap kmap, qmap, smap;
+    KeyMaps kmap;
+    CUtensorMap qmap, smap;
     if (!make_key_map(&kmap, a, D, kRows, &prm.ks)) return cudaErrorInvalidValue;
     if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
         return cudaErrorInvalidValue;

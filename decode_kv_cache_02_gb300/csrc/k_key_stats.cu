@@ -20,11 +20,9 @@
 // multiplies with every key block anyway, which completes sum_i there.
 //
 // Paged input (key_stats_paged_kernel): rows are found through the block
-// table.  The rows past N in the problem's last block (stale space the
-// sequence has not filled) are set to zero, so that tiles read straight from
-// the pool see zeros past N as the contiguous tensor map's bounds give; when
-// the tensor-core stages do not read the pool (small blocks, fp32), pass 1 also
-// stores every row, bit for bit, into the contiguous copy Kc [P, N, d].
+// table; rows past N are neither read nor written.  When the tensor-core
+// stages do not read the pool (small blocks, fp32), pass 1 also stores every
+// row, bit for bit, into the contiguous copy Kc [P, N, d].
 #include "rkv_common.cuh"
 #include "rkv_internal.h"
 #include "rkv_paged.cuh"
@@ -178,8 +176,8 @@ key_stats_kernel(const T* __restrict__ K, int n_cap, int N, float* __restrict__ 
 }
 
 // The same statistics of paged keys: rows through the block table (the
-// sequence's ids staged in shared memory), the stale rows past N in the last
-// block zeroed.  kMode 1 also stores every row into the contiguous copy Kc;
+// sequence's ids staged in shared memory).  kMode 1 also stores every row into
+// the contiguous copy Kc;
 // kMode 2 reads in place.  Four CTAs per SM keep enough rows in flight, except
 // for the copying fp32 variant, which would spill there.
 template <typename T, int D, int kMode>
@@ -216,19 +214,6 @@ key_stats_paged_kernel(const T* __restrict__ K, int n_cap, int N, float* __restr
                        : (((int64_t)blk * pg.H + head_base) << pg.log2bs) |
                              (int64_t)(r & ((1 << pg.log2bs) - 1));
     };
-    if constexpr (kPaged) {
-        // zero the stale rows after N in the last block (this head's tile only)
-        const int bs = 1 << pg.log2bs;
-        const int tail_end = (N + bs - 1) / bs * bs;
-        for (int e = threadIdx.x; e < (tail_end - N) * L; e += kThreads) {
-            const int r = N + e / L, c8 = (e % L) * 8;
-            const int64_t pr = phys_row(r);
-            if (pr >= 0) {
-                Raw8<T> z{};
-                z.store(const_cast<T*>(K) + pr * D + c8);
-            }
-        }
-    }
     const int sub = threadIdx.x % L;         // which 8 columns
     const int r0 = threadIdx.x / L;          // first row of this thread
     const int col = sub * 8;

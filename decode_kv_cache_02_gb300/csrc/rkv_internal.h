@@ -26,6 +26,9 @@ struct PagedIn {
 // the paged pool (rows = the rows of one block, outer = block * H + head) read
 // one block (or, for blocks over 128 rows, 128 rows) at a time through the
 // table, blocks past the sequence's nb blocks (and invalid ids) read as zero.
+// The sequence's last block is read through a second map of the pool whose
+// row extent is tail_rows, so its rows past N read as zero too and the pool's
+// unfilled space is never touched.
 struct KeySource {
     const int32_t* table = nullptr;
     int max_blocks = 0;
@@ -33,7 +36,7 @@ struct KeySource {
     int H = 1;
     int nb = 0;          // blocks holding the problem's N rows
     int num_blocks = 0;
-    int box_rows = 0;    // min(block size, 128)
+    int tail_rows = 0;   // rows of the last block before N (0: the block is full)
 };
 
 // Everything the scoring kernels of one call need.

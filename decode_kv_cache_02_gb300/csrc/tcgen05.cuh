@@ -71,22 +71,34 @@ RKV_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// The tensor maps of a call's keys: `main` for every load but the last block
+// of a paged sequence whose rows stop before the block's end, which goes
+// through `tail` (the same pool, a row extent of KeySource::tail_rows).
+struct alignas(64) KeyMaps {
+    CUtensorMap main;
+    CUtensorMap tail;
+};
+
 // TMA loads of key rows [r0, r0 + rows) of problem p into a 128-byte-swizzled
 // K-major tile at dst (KC chunks of 64 columns, chunk_bytes apart).  From the
 // contiguous map, one load per chunk; from a paged pool (ks.table set), one
-// load per block (box_rows rows each: sub-tiles start on 8-row, 1024-byte
+// load per block of min(block size, 128) rows (sub-tiles start on 8-row, 1024-byte
 // boundaries, which keeps the swizzle phase), blocks past the sequence and
-// invalid ids at an outer coordinate past the pool, which reads as zeros.
-RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const CUtensorMap* map,
+// invalid ids at an outer coordinate past the pool, which reads as zeros, and
+// the rows past N of the sequence's last block through the tail map, which
+// reads them as zeros as well.
+RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps* maps,
                            uint64_t* bar, int64_t p, int r0, int rows, const KeySource& ks) {
     if (ks.table == nullptr) {
-        for (int c = 0; c < KC; ++c) tma_load_3d(dst + c * chunk_bytes, map, bar, c * 64, r0, (int)p);
+        for (int c = 0; c < KC; ++c)
+            tma_load_3d(dst + c * chunk_bytes, &maps->main, bar, c * 64, r0, (int)p);
         return;
     }
     const int64_t s = p / ks.H;
     const int h = (int)(p - s * ks.H);
     const int32_t* row = ks.table + s * ks.max_blocks;
-    for (int t = 0; t < rows; t += ks.box_rows) {
+    const int box = ks.log2bs < 7 ? 1 << ks.log2bs : 128;  // rows per TMA box
+    for (int t = 0; t < rows; t += box) {
         const int r = r0 + t;
         const int lb = r >> ks.log2bs;
         int z = ks.num_blocks * ks.H;
@@ -95,6 +107,7 @@ RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const CUtensor
             if ((unsigned)blk < (unsigned)ks.num_blocks) z = blk * ks.H + h;
         }
         const int y = r & ((1 << ks.log2bs) - 1);
+        const CUtensorMap* map = &maps->main + (lb == ks.nb - 1 && ks.tail_rows > 0 ? 1 : 0);
         for (int c = 0; c < KC; ++c)
             tma_load_3d(dst + c * chunk_bytes + t * 128, map, bar, c * 64, y, z);
     }
@@ -205,11 +218,17 @@ bool make_map_3d_bf16(CUtensorMap* map, const void* base, int inner, int rows,
                       int box_rows);
 
 int sm_count();
-// The tensor map of a call's keys: the contiguous [P][N][D] map with boxes of
+// The tensor maps of a call's keys: the contiguous [P][N][D] map with boxes of
 // box_rows rows (ks: no table), or, for paged keys read directly, the pool map
-// [H * num_blocks][block size][D] with boxes of min(block size, 128) rows and
-// ks filled from the call's table.
-bool make_key_map(CUtensorMap* map, const ScoreArgs& a, int D, int box_rows, KeySource* ks);
+// [H * num_blocks][block size][D] with boxes of min(block size, 128) rows, its
+// copy with a row extent of the last block's rows before N, and ks filled from
+// the call's table.
+bool make_key_map(KeyMaps* maps, const ScoreArgs& a, int D, int box_rows, KeySource* ks);
+// One prefetch of each of a call's key maps.
+RKV_DEV void prefetch_key_maps(const KeyMaps* maps) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps->main)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps->tail)) : "memory");
+}
 
 }  // namespace tc
 }  // namespace rkv

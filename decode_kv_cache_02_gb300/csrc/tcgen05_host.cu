@@ -36,10 +36,14 @@ bool make_map_3d_bf16(CUtensorMap* map, const void* base, int inner, int rows, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_key_map(CUtensorMap* map, const ScoreArgs& a, int D, int box_rows, KeySource* ks) {
+bool make_key_map(KeyMaps* maps, const ScoreArgs& a, int D, int box_rows, KeySource* ks) {
     *ks = KeySource{};
-    if (!a.paged_direct)
-        return make_map_3d_bf16(map, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, box_rows);
+    if (!a.paged_direct) {
+        if (!make_map_3d_bf16(&maps->main, a.K, D, a.N, a.P, D, (int64_t)a.n_cap * D, box_rows))
+            return false;
+        maps->tail = maps->main;  // not used without a table
+        return true;
+    }
     const int bs = 1 << a.pg.log2bs;
     ks->table = a.pg.table;
     ks->max_blocks = a.pg.max_blocks;
@@ -47,9 +51,17 @@ bool make_key_map(CUtensorMap* map, const ScoreArgs& a, int D, int box_rows, Key
     ks->H = a.pg.H;
     ks->nb = (a.N + bs - 1) / bs;
     ks->num_blocks = a.pg.num_blocks;
-    ks->box_rows = bs < 128 ? bs : 128;
-    return make_map_3d_bf16(map, a.K, D, bs, (int64_t)a.pg.H * a.pg.num_blocks, D, (int64_t)bs * D,
-                            ks->box_rows);
+    const int rem = a.N - (ks->nb - 1) * bs;  // rows of the last block before N
+    ks->tail_rows = rem < bs ? rem : 0;
+    const int64_t outer = (int64_t)a.pg.H * a.pg.num_blocks;
+    const int box = bs < 128 ? bs : 128;
+    if (!make_map_3d_bf16(&maps->main, a.K, D, bs, outer, D, (int64_t)bs * D, box))
+        return false;
+    if (ks->tail_rows == 0) {
+        maps->tail = maps->main;
+        return true;
+    }
+    return make_map_3d_bf16(&maps->tail, a.K, D, ks->tail_rows, outer, D, (int64_t)bs * D, box);
 }
 
 int sm_count() {

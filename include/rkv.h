@@ -260,11 +260,10 @@ int rkv_score_ex(const rkv_desc* desc, const void* K, const void* Q_obs, int n_c
  * the last kept block are left as they were.  The blocks past the kept ones,
  * entries ceil(budget/bs) .. ceil(n_cached/bs) - 1 of each row, are no longer
  * used: their ids are written to out_freed [num_seqs, n_free] (n_free =
- * rkv_paged_freed_per_seq()) and the table entries are set to -1.  The K rows
- * after n_cached in each sequence's last block (space it has not filled yet)
- * are set to zero, so the tensor-core stages can read the pool directly.
- * Blocks not named by the first ceil(n_cached/bs) entries of any row are not
- * touched. */
+ * rkv_paged_freed_per_seq()) and the table entries are set to -1.  Rows after
+ * n_cached in each sequence's last block (space it has not filled yet) are
+ * neither read nor written, and blocks not named by the first
+ * ceil(n_cached/bs) entries of any row are not touched. */
 typedef struct {
     int64_t num_seqs;           /* S, rows of the block table (>= 0)         */
     int32_t num_kv_heads;       /* H, heads per block; P = S * H problems     */

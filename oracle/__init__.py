@@ -308,8 +308,8 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
     H, bs, d] (any element type; rows move as they are); the keys are scored
     from ``K_f64`` = the float values of K_pool's logical rows.  Returns
     dict(idx, scores, K_pool, V_pool, table, freed): the oracle's kept set and
-    the expected state after the round (the K rows after n_cached in each
-    sequence's last block zeroed), with the rows moved by ``idx_used``
+    the expected state after the round (rows after n_cached in each
+    sequence's last block left as they were), with the rows moved by ``idx_used``
     (default: the oracle's own kept set; a GPU test passes the GPU's, so that
     exact score ties cannot change which rows are compared)."""
     K_pool = np.asarray(K_pool)
@@ -326,11 +326,6 @@ def paged_compress(K_pool, V_pool, Q, table, n_cached: int, budget: int, n_obs: 
     Kp, Vp, new_table = K_pool.copy(), V_pool.copy(), table.copy()
     freed = np.zeros((S, 0), dtype=np.int32)
     if n_cached > budget:
-        # the K rows after n_cached in each sequence's last block (space the
-        # sequence has not filled yet) are set to zero by the round
-        nb = -(-n_cached // bs)
-        for s_ in range(S):
-            Kp[table[s_, nb - 1], :, n_cached - (nb - 1) * bs:] = 0
         K_log = paged_rows(K_pool, table, n_cached)
         V_log = paged_rows(V_pool, table, n_cached)
         for s_ in range(S):

@@ -106,6 +106,15 @@ def test_paged_block_sizes(bs):
     _paged_check(w, bs)
 
 
+def test_paged_long_rows_block256():
+    """Rows past 2048 (the long-row Gram) read in place from 256-row blocks,
+    the last one partly filled (N = 2500: 196 of its rows before N; the rest
+    hold large values that no stage may read)."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=2500, budget=2200, layers=1, batch=2,
+                                           kv_heads=2)
+    _paged_check(w, 256)
+
+
 def test_paged_fp32_cuda_core_path():
     """fp32 keys take the CUDA-core importance and Gram on the contiguous copy."""
     w = wl.BY_NAME["tiny"].scaled(batch=2)

@@ -439,12 +439,9 @@ def test_paged_round_equals_contiguous_round():
     assert np.all(out["table"][:, nb_keep:nb_old] == -1)
     np.testing.assert_array_equal(out["table"][:, :nb_keep], table[:, :nb_keep])
     untouched = sorted(set(range(K_pool.shape[0])) - set(table[:, :nb_keep].ravel().tolist()))
-    last_old = table[:, nb_old - 1]
-    tail = N - (nb_old - 1) * bs
-    np.testing.assert_array_equal(out["K_pool"][last_old, :, tail:], 0)  # unfilled space zeroed
-    K_exp = K_pool.copy()
-    K_exp[last_old, :, tail:] = 0
-    np.testing.assert_array_equal(out["K_pool"][untouched], K_exp[untouched])
+    # the unfilled space after N in the old last block is among them
+    assert set(table[:, nb_old - 1].tolist()) <= set(untouched)
+    np.testing.assert_array_equal(out["K_pool"][untouched], K_pool[untouched])
     np.testing.assert_array_equal(out["V_pool"][untouched], V_pool[untouched])
     last = table[:, nb_keep - 1]
     np.testing.assert_array_equal(out["K_pool"][last, :, B % bs:], K_pool[last, :, B % bs:])
