@@ -16,7 +16,10 @@
 // One epilogue thread owns one key row of a block; two groups of four warps
 // take alternate blocks (the MMA order's even and odd accumulators), so two
 // warps per scheduler hide the latency of the exponentials.  Two passes over
-// the problem's keys (the second is expected to hit L2):
+// the problem's keys; the second reads the blocks in reverse order, so the
+// ones the first read last (the most likely to be in L2) come first, and the
+// first pass's copies ask L2 to keep their lines (evict_last), the second's to
+// drop them first:
 //   pass 1  per-thread online (max, sum of exp) per query row, then a block
 //           reduction (warp shuffles + shared memory) to the row's max M_c and
 //           1 / sum_j exp(l - M_c);
@@ -187,13 +190,15 @@ importance_tc_kernel(const __grid_constant__ KeyMaps kmap,
                 }
                 ++kq;
                 for (int pass = 0; ok && pass < 2; ++pass) {
-                    for (int b = 0; b < T; ++b) {
+                    const uint64_t policy = pass == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
+                    for (int i = 0; i < T; ++i) {
+                        const int b = pass == 0 ? i : T - 1 - i;
                         const int s = kk % C::kStages;
                         if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort)))
                             break;
                         mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
                         load_key_rows(sK + s * C::kBlockBytes, kChunkBytes, C::KC, &kmap, &k_full[s],
-                                      p, b * kRows, kRows, prm.ks);
+                                      p, b * kRows, kRows, prm.ks, policy);
                         ++kk;
                     }
                 }
@@ -346,10 +351,11 @@ importance_tc_kernel(const __grid_constant__ KeyMaps kmap,
                 for (int w = 0; w < kEpi / 32; ++w) S += redS[w * RP + c];
                 m[c] += lg2_fast(S) + log2_nobs;
             }
-            // ---- pass 2: probabilities -> importance
+            // ---- pass 2: probabilities -> importance (blocks in reverse order)
             const uint32_t ka2 = ka;
-            for (int b = (grp + (int)(ka2 & 1)) & 1; b < T; b += 2) {
-                const uint32_t kb = ka2 + (uint32_t)b;
+            for (int i = (grp + (int)(ka2 & 1)) & 1; i < T; i += 2) {
+                const uint32_t kb = ka2 + (uint32_t)i;
+                const int b = T - 1 - i;
                 const int a = kb % kAcc;
                 ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[a], (kb / kAcc) & 1, s_abort));
                 if (!ok) break;

@@ -71,10 +71,34 @@ RKV_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// The same load with an L2 cache policy (createpolicy): how long the copied
+// lines should stay in L2 relative to other traffic.
+RKV_DEV void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+        "l"(policy)
+        : "memory");
+}
+// L2 policies for key streams read twice: the first read asks the lines to
+// stay (evict_last), the second lets them go first (evict_first).
+RKV_DEV uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+RKV_DEV uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // The tensor maps of a call's keys: `main` for every load but the last block
 // of a paged sequence whose rows stop before the block's end, which goes
 // through `tail` (the same pool, a row extent of KeySource::tail_rows).
-struct alignas(64) KeyMaps {
+struct KeyMaps {
     CUtensorMap main;
     CUtensorMap tail;
 };
@@ -87,11 +111,17 @@ struct alignas(64) KeyMaps {
 // invalid ids at an outer coordinate past the pool, which reads as zeros, and
 // the rows past N of the sequence's last block through the tail map, which
 // reads them as zeros as well.
+// policy != 0: every copy carries that L2 cache policy.
 RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps* maps,
-                           uint64_t* bar, int64_t p, int r0, int rows, const KeySource& ks) {
+                           uint64_t* bar, int64_t p, int r0, int rows, const KeySource& ks,
+                           uint64_t policy = 0) {
     if (ks.table == nullptr) {
-        for (int c = 0; c < KC; ++c)
-            tma_load_3d(dst + c * chunk_bytes, &maps->main, bar, c * 64, r0, (int)p);
+        for (int c = 0; c < KC; ++c) {
+            if (policy)
+                tma_load_3d_hint(dst + c * chunk_bytes, &maps->main, bar, c * 64, r0, (int)p, policy);
+            else
+                tma_load_3d(dst + c * chunk_bytes, &maps->main, bar, c * 64, r0, (int)p);
+        }
         return;
     }
     const int64_t s = p / ks.H;
@@ -108,8 +138,12 @@ RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps*
         }
         const int y = r & ((1 << ks.log2bs) - 1);
         const CUtensorMap* map = &maps->main + (lb == ks.nb - 1 && ks.tail_rows > 0 ? 1 : 0);
-        for (int c = 0; c < KC; ++c)
-            tma_load_3d(dst + c * chunk_bytes + t * 128, map, bar, c * 64, y, z);
+        for (int c = 0; c < KC; ++c) {
+            if (policy)
+                tma_load_3d_hint(dst + c * chunk_bytes + t * 128, map, bar, c * 64, y, z, policy);
+            else
+                tma_load_3d(dst + c * chunk_bytes + t * 128, map, bar, c * 64, y, z);
+        }
     }
 }
 RKV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
