@@ -76,6 +76,7 @@ constexpr int kColGroups = kEpiWarps / 4;        // warps sharing one TMEM lane 
 constexpr int kChunksPerWarp = 4 / kColGroups;   // 32-column chunks per warp per tile
 constexpr int kNewerCap = 255 / kColGroups;      // per-group cap of the newer count
 constexpr int kThreads = 64 + kEpiThreads;  // producer warp, MMA warp, epilogue
+constexpr int kDotWarps = 2;  // with the statistics folded into importance: k_i . s
 constexpr uint32_t kTmemCols = 512;  // all of TMEM: 4 accumulators of 128 columns or 2 of 256
 constexpr int kPrefetch = 5;  // finalize rows per thread loaded at problem start (N <= 1280)
 
@@ -102,7 +103,7 @@ struct Cfg {
     static constexpr size_t kNewerOff = kSimOff + sizeof(float) * kInvFloats;
     static constexpr size_t kInvMaxOff = kNewerOff + kInvFloats;  // one byte per row
     static constexpr size_t kBarOff = kInvMaxOff + 2 * sizeof(float) * kMaxBlocks * 4;
-    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * 4 + 4 + 2;
+    static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * 4 + 4 + 2 + 4;
     static constexpr size_t kSmemBytes = 1024 + kBarOff + 8 * kNumBars + 16;
 };
 
@@ -156,10 +157,13 @@ RKV_DEV void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
 }
 
 // ---------------------------------------------------------------- kernel --
-template <int D, int MB, int W>
-__global__ void __launch_bounds__(kThreads, 1)
+// kDot: two more warps complete sum_i = inv_i (k_i . s) - |khat_i|^2 from each
+// row block while it sits in shared memory as the A operand (the importance
+// kernel then takes the key statistics and no pass over K is spent on them).
+template <int D, int MB, int W, bool kDot>
+__global__ void __launch_bounds__(kThreads + (kDot ? 32 * kDotWarps : 0), 1)
 gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ KeyMaps bmap,
-               const Params prm) {
+               const Params prm, const float* __restrict__ s32) {
     using C = Cfg<D, MB, W>;
     constexpr int kAccBufs = C::kAccBufs;
     constexpr int kMaxBlocks = C::kMaxBlocks;
@@ -186,7 +190,11 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
     uint64_t* inv_empty = inv_full + 2;         // [2]
     uint64_t* epi_bar = inv_empty + 2;
     uint64_t* drain_bar = epi_bar + 1;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    // kDot: a problem's sum_i are written (sum_ready) / the epilogue has read
+    // them (sum_free), one pair per problem parity
+    uint64_t* sum_ready = drain_bar + 1;  // [2]
+    uint64_t* sum_free = sum_ready + 2;   // [2]
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sum_free + 2);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,7 +205,7 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kAStages; ++s) {
             mbar_init(&a_full[s], 1);
-            mbar_init(&a_empty[s], 1);
+            mbar_init(&a_empty[s], kDot ? 1 + kDotWarps : 1);  // the MMAs, and the dot warps
         }
         for (int s = 0; s < C::kBStages; ++s) {
             mbar_init(&b_full[s], 1);
@@ -213,6 +221,10 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
         }
         mbar_init(epi_bar, kEpiWarps);
         mbar_init(drain_bar, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&sum_ready[t], kDotWarps);
+            mbar_init(&sum_free[t], kEpiWarps);
+        }
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_key_maps(&tmap);
@@ -338,6 +350,59 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
             volatile int never = 0;
             mbar_wait(drain_bar, 0, &never);
         }
+    } else if (kDot && warp >= 2 + kEpiWarps) {
+        // -------------------------------------------------------- dot warps --
+        // rows dw * 64 + lane and + 32 of each row block, read from the A slot
+        // in the MMA's order; the slot is released by the MMAs' commit and one
+        // arrival per dot warp
+        // kDot: s = sum_j khat_j in fp32 per problem (16 D / 2 floats apart)
+        // from the importance kernel; sum_s holds |khat_i|^2, turned into
+        // sum_i in place
+        __shared__ float s_vec[kDotWarps][D];
+        float* sum_w = const_cast<float*>(prm.sum_s);
+        const int dw = warp - (2 + kEpiWarps);
+        uint32_t ka = 0, kprob = 0;
+        bool ok = true;
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kprob) {
+            __syncwarp();  // the previous problem's reads of s_vec are done
+            for (int c = lane; c < D; c += 32) s_vec[dw][c] = s32[p * (16 * D / 2) + c];
+            __syncwarp();
+            for (int I = 0; ok && I < T; ++I, ++ka) {
+                // inverse norms and |khat_i|^2 of the two rows, on their way
+                const int i0 = I * kRows + dw * 64 + lane, i1 = i0 + 32;
+                float iv[2] = {0.f, 0.f}, kh[2] = {0.f, 0.f};
+                if (i0 < N) {
+                    iv[0] = prm.inv_norm[p * prm.ld_ws + i0];
+                    kh[0] = sum_w[p * prm.ld_ws + i0];
+                }
+                if (i1 < N) {
+                    iv[1] = prm.inv_norm[p * prm.ld_ws + i1];
+                    kh[1] = sum_w[p * prm.ld_ws + i1];
+                }
+                const int sa = ka % C::kAStages;
+                ok = __all_sync(0xffffffffu, mbar_wait(&a_full[sa], (ka / C::kAStages) & 1, s_abort));
+                if (!ok) break;
+                const uint8_t* blk = sA + sa * C::kBlockBytes;
+                const float d0 = row_dot_lean<C::KC>(blk, dw * 64 + lane, s_vec[dw]);
+                const float d1 = row_dot_lean<C::KC>(blk, dw * 64 + 32 + lane, s_vec[dw]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_empty[sa]);
+                if (i0 < N) sum_w[p * prm.ld_ws + i0] = iv[0] * d0 - kh[0];
+                if (i1 < N) sum_w[p * prm.ld_ws + i1] = iv[1] * d1 - kh[1];
+            }
+            if (!ok) break;
+            // this problem's sum_i are in memory (release at CTA scope), once
+            // the epilogue has read the ones of two problems back
+            const int sb = kprob & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&sum_free[sb], ((kprob >> 1) & 1) ^ 1, s_abort));
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sum_ready[sb]);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            set_error(prm.status, kDevErrTimeout, 4u);
+        }
     } else {
         // ------------------------------------------------------- epilogue --
         const int et = threadIdx.x - 64;      // 0..255
@@ -348,7 +413,7 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
         const int Cn = N - prm.n_obs;
         const bool tau_pos = prm.tau > 0.f;
         const float inv_nm1 = 1.0f / (float)(N - 1);
-        uint32_t kacc = 0, kepi = 0, kinv = 0;
+        uint32_t kacc = 0, kepi = 0, kinv = 0, kprob = 0;
         bool ok = true;
         for (int x = et; x < kInvFloats; x += kEpiThreads) s_sim[x] = 0;
         for (int x = et; x < kInvFloats / 4; x += kEpiThreads) s_newer[x] = 0u;
@@ -559,6 +624,19 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
             ok = __all_sync(0xffffffffu, mbar_wait(epi_bar, kepi & 1, s_abort));
             ++kepi;
             if (!ok) break;
+            if (kDot) {
+                // sum_i of this problem comes from the dot warps
+                const int sb = kprob & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sum_ready[sb], (kprob >> 1) & 1, s_abort));
+                if (!ok) break;
+#pragma unroll
+                for (int u = 0; u < kPrefetch; ++u) {
+                    const int i = et + u * kEpiThreads;
+                    pre_tot[u] = i < Cn ? prm.sum_s[p * prm.ld_ws + i] : 0.f;
+                }
+                mbar_arrive_warp(&sum_free[sb]);
+            }
+            ++kprob;
             // finalize this thread's rows, then clear exactly what it read
             auto finalize_row = [&](int i, float tot, float imp) {
                 const float sim_i = (float)s_sim[i] * (1.0f / kSimScale);
@@ -601,7 +679,7 @@ gram_tc_kernel(const __grid_constant__ KeyMaps tmap, const __grid_constant__ Key
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int D, int MB, int W>
+template <int D, int MB, int W, bool kDot>
 cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     using C = Cfg<D, MB, W>;
     KeyMaps map, bmap;
@@ -612,13 +690,14 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     Params prm{a.P,      a.N,     a.n_obs,   a.beta, a.lambda, a.tau,    a.inv_norm,
                a.sum_s,  a.ld_ws, a.I,       a.R,    a.Z,      a.ld_out, a.status};
     prm.ks = ks;
-    auto kern = gram_tc_kernel<D, MB, W>;
+
+    auto kern = gram_tc_kernel<D, MB, W, kDot>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t sms = sm_count();
     const int64_t grid = a.P < sms ? a.P : sms;
-    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(map, bmap, prm);
+    kern<<<(unsigned)grid, kThreads + (kDot ? 32 * kDotWarps : 0), C::kSmemBytes, s>>>(map, bmap, prm, static_cast<const float*>(a.s_rows));
     return cudaGetLastError();
 }
 
@@ -632,11 +711,16 @@ bool gram_tc_shape_ok(const ScoreArgs& a) {
 
 bool gram_tc_supported(const ScoreArgs& a) { return gram_tc_shape_ok(a) && encode_fn() != nullptr; }
 
+bool gram_tc_rows(const ScoreArgs& a) { return gram_tc_shape_ok(a) && a.N <= kMaxBlocksSmall * kRows; }
+
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s) {
     if (a.P == 0) return cudaSuccess;
     if (a.N <= kMaxBlocksSmall * kRows)
-        return a.d == 128 ? launch_t<128, kMaxBlocksSmall, 2>(a, s)
-                          : launch_t<64, kMaxBlocksSmall, 2>(a, s);
+        return a.fused_stats
+                   ? (a.d == 128 ? launch_t<128, kMaxBlocksSmall, 2, true>(a, s)
+                                 : launch_t<64, kMaxBlocksSmall, 2, true>(a, s))
+                   : (a.d == 128 ? launch_t<128, kMaxBlocksSmall, 2, false>(a, s)
+                                 : launch_t<64, kMaxBlocksSmall, 2, false>(a, s));
     // longer rows: row pairs against streamed block pairs (k_gram_tc_pairs.cu)
     return launch_gram_tc_pairs(a, s);
 }

@@ -78,11 +78,15 @@ struct IParams {
     int64_t ld;
     // sum_i = inv_i (k_i . s) - |khat_i|^2: the key-stats kernel leaves
     // |khat_i|^2 in sum_s, this kernel completes it
-    const float* inv_norm;
+    float* inv_norm;  // written by the resident variant with the statistics folded in
     float* sum_s;
     int64_t ld_ws;
     DeviceStatus* status;
     KeySource ks;  // contiguous keys, or the paged pool read through the table
+    // resident variant with the key statistics folded in: s = sum_j khat_j
+    // (fp32) per problem, stride ld_s floats
+    float* s32;
+    int64_t ld_s;
     // bit c of colmask[k]: query row c exists and its query index c % n_obs
     // is >= k (so it sees a key k positions past N - n_obs); bit c of
     // lastmask: c is the last query row of its head.
@@ -583,32 +587,9 @@ RKV_DEV void broadcast_columns(float (&v)[SC], float lo, float hi) {
     for (int c = 32; c < SC; ++c) v[c] = __shfl_sync(0xffffffffu, hi, c - 32);
 }
 
-// Eight bf16 of a 128-byte-swizzled K-major tile: 16-byte unit u of row r
-// sits at unit u ^ (r mod 8) of the row (the TMA 128-byte swizzle).
-RKV_DEV uint4 swizzled_unit(const uint8_t* tile, int r, int u) {
-    return *reinterpret_cast<const uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
-}
-
-// the two bf16 of a 32-bit word as a packed fp32 pair (low element first)
-RKV_DEV unsigned long long bf16x2_to_f32x2(uint32_t w) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
-    return r;
-}
-
-// acc.xy += a.xy * b.xy on packed fp32 pairs
-RKV_DEV void fma_f32x2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
-RKV_DEV float f32x2_sum(unsigned long long v) {
-    return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
-}
-
-// k . s over the D elements of row r of a key block (KC swizzled chunks of
-// 64), s in fp32; four packed accumulators keep the FMA chains short
+// |k|^2 over the D elements of row r of a key block (fp32, packed FMAs)
 template <int KC>
-RKV_DEV float row_dot(const uint8_t* blk, int r, const float* s32) {
+RKV_DEV float row_norm2(const uint8_t* blk, int r) {
     unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int c = 0; c < KC; ++c) {
@@ -616,20 +597,27 @@ RKV_DEV float row_dot(const uint8_t* blk, int r, const float* s32) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const uint4 k = swizzled_unit(tile, r, u);
-            const ulonglong2 s01 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8);
-            const ulonglong2 s23 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8 + 4);
-            fma_f32x2(acc[0], bf16x2_to_f32x2(k.x), s01.x);
-            fma_f32x2(acc[1], bf16x2_to_f32x2(k.y), s01.y);
-            fma_f32x2(acc[2], bf16x2_to_f32x2(k.z), s23.x);
-            fma_f32x2(acc[3], bf16x2_to_f32x2(k.w), s23.y);
+            const unsigned long long k0 = bf16x2_to_f32x2(k.x), k1 = bf16x2_to_f32x2(k.y);
+            const unsigned long long k2 = bf16x2_to_f32x2(k.z), k3 = bf16x2_to_f32x2(k.w);
+            fma_f32x2(acc[0], k0, k0);
+            fma_f32x2(acc[1], k1, k1);
+            fma_f32x2(acc[2], k2, k2);
+            fma_f32x2(acc[3], k3, k3);
         }
     }
     return (f32x2_sum(acc[0]) + f32x2_sum(acc[1])) + (f32x2_sum(acc[2]) + f32x2_sum(acc[3]));
 }
 
+RKV_DEV void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // HEAD > 0: the query rows form SC / HEAD heads of HEAD rows (R == SC), so a
 // head's last row is known at compile time; HEAD == 0 reads it from lastmask.
-template <int D, int SC, int HEAD>
+// kStats: the key statistics are taken here too (no separate pass over K):
+// the dot warps write inv_i and |khat_i|^2 for every key and s = sum_j khat_j
+// per problem, and leave k_i . s to the Gram kernel.
+template <int D, int SC, int HEAD, bool kStats>
 __global__ void __launch_bounds__(kRThreads, 1)
 importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                       const __grid_constant__ CUtensorMap qmap,
@@ -681,7 +669,7 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
         }
         for (int q = 0; q < 2; ++q) {
             mbar_init(&q_full[q], 1);
-            mbar_init(&q_empty[q], 1 + kRDotWarps);
+            mbar_init(&q_empty[q], kStats ? 1 : 1 + kRDotWarps);  // the dot warps read s
         }
         for (int b = 0; b < kRMaxSlots; ++b) {
             mbar_init(&blk_full[b], 1);
@@ -705,7 +693,7 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
         if (lane == 0) {
             uint32_t kk = 0, kq = 0;
             bool ok = true;
-            const uint32_t q_tx = (uint32_t)(C::KC * (prm.R + kSRows) * 128);
+            const uint32_t q_tx = (uint32_t)(C::KC * (prm.R + (kStats ? 0 : kSRows)) * 128);
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
                 const int qb = kq & 1;
                 if (!(ok = mbar_wait(&q_empty[qb], ((kq >> 1) & 1) ^ 1, s_abort))) break;
@@ -714,8 +702,9 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                 for (int c = 0; c < C::KC; ++c) {
                     tma_load_3d(b_buf + c * C::kQChunkBytes, &qmap, &q_full[qb], c * kChunkElems, 0,
                                 (int)p);
-                    tma_load_3d(b_buf + C::KC * C::kQChunkBytes + c * C::kSChunkBytes, &smap,
-                                &q_full[qb], c * kChunkElems, 0, (int)p);
+                    if (!kStats)
+                        tma_load_3d(b_buf + C::KC * C::kQChunkBytes + c * C::kSChunkBytes, &smap,
+                                    &q_full[qb], c * kChunkElems, 0, (int)p);
                 }
                 ++kq;
                 for (int b = 0; b < T; ++b) {
@@ -776,6 +765,76 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
             mma_commit(drain_bar);
             volatile int never = 0;
             mbar_wait(drain_bar, 0, &never);
+        }
+    } else if (kStats && warp >= 2 + kREpi / 32) {
+        // ---- statistics warps: inv_i = 1 / max(|k_i|, eps) and |khat_i|^2 of
+        // row dw * 32 + lane of every key block, and s = sum_j khat_j: lane l
+        // adds columns l * CPL .. l * CPL + CPL - 1 of the warp's 32 rows (each
+        // row's inv_i handed over by shuffle); the four warps' partial s meet
+        // in shared memory at the problem's end, in a fixed order
+        constexpr int CPL = D / 32;
+        const int dw = warp - (2 + kREpi / 32);
+        const int r0 = dw * 32 + lane;
+        const int c0 = lane * CPL;  // this lane's first column of s
+        const int cchunk = c0 / kChunkElems, cunit = (c0 % kChunkElems) >> 3, celem = c0 & 7;
+        uint32_t kk = 0;
+        bool ok = true;
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+            float sacc[CPL];
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) sacc[t] = 0.f;
+            for (int b = 0; b < T; ++b, ++kk) {
+                const int st = kk % C::kStages;
+                ok = __all_sync(0xffffffffu, mbar_wait(&k_full[st], (kk / C::kStages) & 1, s_abort));
+                if (!ok) break;
+                const uint8_t* blk = sK + st * C::kBlockBytes;
+                const int j0 = b * kRows + r0;
+                const float n2 = row_norm2<C::KC>(blk, r0);
+                // rows past N are TMA zero fill; they add nothing to s
+                const float inv = j0 < N ? 1.0f / fmaxf(sqrtf(n2), 1e-12f) : 0.f;
+                const uint8_t* tile = blk + cchunk * kChunkBytes;
+#pragma unroll 8
+                for (int rr = 0; rr < 32; ++rr) {
+                    const float iv = __shfl_sync(0xffffffffu, inv, rr);
+                    const int r = dw * 32 + rr;
+                    const uint8_t* src = tile + r * 128 + ((cunit ^ (r & 7)) << 4) + celem * 2;
+                    if constexpr (CPL == 4) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(src);
+                        sacc[0] = fmaf(__uint_as_float(v.x << 16), iv, sacc[0]);
+                        sacc[1] = fmaf(__uint_as_float(v.x & 0xffff0000u), iv, sacc[1]);
+                        sacc[2] = fmaf(__uint_as_float(v.y << 16), iv, sacc[2]);
+                        sacc[3] = fmaf(__uint_as_float(v.y & 0xffff0000u), iv, sacc[3]);
+                    } else {
+                        const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+                        sacc[0] = fmaf(__uint_as_float(v << 16), iv, sacc[0]);
+                        sacc[1] = fmaf(__uint_as_float(v & 0xffff0000u), iv, sacc[1]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&k_empty[st]);
+                if (j0 < N) {
+                    prm.inv_norm[p * prm.ld_ws + j0] = inv;
+                    // |khat_i|^2; the Gram kernel completes sum_i from it
+                    prm.sum_s[p * prm.ld_ws + j0] = (n2 * inv) * inv;
+                }
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int t = 0; t < CPL; ++t) sDot[dw * D + c0 + t] = sacc[t];
+            named_bar_sync(1, 32 * kRDotWarps);
+            if (dw == 0) {
+                for (int c = lane; c < D; c += 32) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kRDotWarps; ++w) v += sDot[w * D + c];
+                    prm.s32[p * prm.ld_s + c] = v;
+                }
+            }
+            named_bar_sync(1, 32 * kRDotWarps);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            set_error(prm.status, kDevErrTimeout, 25u);
         }
     } else if (warp >= 2 + kREpi / 32) {
         // ---- dot warps: sum_i = inv_i (k_i . s) - |khat_i|^2 (the key-stats
@@ -1041,17 +1100,22 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
         // s rows hi, lo for the dot warps
         if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, kSRows))
             return cudaErrorInvalidValue;
+        // with the statistics folded in, s (fp32) goes where the s rows were
+        prm.s32 = static_cast<float*>(a.s_rows);
+        prm.ld_s = (int64_t)16 * D / 2;
+        const bool st = a.fused_stats;
         if (SC == 32) {
             using RC = RCfg<D, 32>;
-            auto kern = (R == 32 && a.n_obs == 8) ? importance_tcr_kernel<D, 32, 8>
-                                                  : importance_tcr_kernel<D, 32, 0>;
+            auto kern = (R == 32 && a.n_obs == 8)
+                            ? (st ? importance_tcr_kernel<D, 32, 8, true> : importance_tcr_kernel<D, 32, 8, false>)
+                            : (st ? importance_tcr_kernel<D, 32, 0, true> : importance_tcr_kernel<D, 32, 0, false>);
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)RC::kSmemBytes);
             if (e != cudaSuccess) return e;
             kern<<<(unsigned)grid, kRThreads, RC::kSmemBytes, s>>>(kmap, qmap, smap, prm);
         } else {
             using RC = RCfg<D, 48>;
-            auto kern = importance_tcr_kernel<D, 48, 0>;
+            auto kern = st ? importance_tcr_kernel<D, 48, 0, true> : importance_tcr_kernel<D, 48, 0, false>;
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)RC::kSmemBytes);
             if (e != cudaSuccess) return e;
@@ -1086,6 +1150,12 @@ bool importance_tc_shape_ok(const ScoreArgs& a) {
 
 bool importance_tc_supported(const ScoreArgs& a) {
     return importance_tc_shape_ok(a) && encode_fn() != nullptr;
+}
+
+bool importance_tc_resident(const ScoreArgs& a) {
+    int ns = 0;
+    return importance_tc_shape_ok(a) &&
+           resident_ring((a.N + kRows - 1) / kRows, a.G * a.n_obs <= 32 ? 32 : 48, &ns);
 }
 
 cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s) {

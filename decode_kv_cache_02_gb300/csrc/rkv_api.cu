@@ -289,8 +289,14 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     const bool gram_tc = rkv::gram_tc_supported(b);
     const bool imp_tc = rkv::importance_tc_supported(b);
     a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
-    cudaError_t e = timed(pg ? kKeyStatsPaged : kKeyStats, s,
-                          [&] { return rkv::launch_key_stats(a, s); });
+    // contiguous keys whose rows fit the resident importance kernel and the
+    // one-row-block Gram: the importance kernel takes the key statistics and
+    // the Gram completes sum_i, so no pass over K is spent on the statistics
+    b.fused_stats = !pg && gram_tc && imp_tc && rkv::importance_tc_resident(b) &&
+                    rkv::gram_tc_rows(b);
+    cudaError_t e = b.fused_stats ? cudaSuccess
+                                  : timed(pg ? kKeyStatsPaged : kKeyStats, s,
+                                          [&] { return rkv::launch_key_stats(a, s); });
     if (e == cudaSuccess) {
         if (imp_tc)
             e = timed(kImportanceTc, s, [&] { return rkv::launch_importance_tc(b, s); });

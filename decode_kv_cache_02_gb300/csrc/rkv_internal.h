@@ -65,6 +65,10 @@ struct ScoreArgs {
     void* Kc = nullptr;
     // paged keys read directly by the tensor-core stages (K is then the pool)
     bool paged_direct = false;
+    // the key statistics come from the resident importance kernel (inv_i,
+    // |khat_i|^2, s in fp32 at s_rows) and the Gram completes sum_i; no
+    // separate statistics pass
+    bool fused_stats = false;
 };
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
@@ -73,10 +77,14 @@ cudaError_t launch_importance(const ScoreArgs& a, cudaStream_t s);
 // *_supported: that, and the driver's tensor-map entry point is present.
 bool importance_tc_shape_ok(const ScoreArgs& a);
 bool importance_tc_supported(const ScoreArgs& a);
+// the importance kernel that keeps a problem's logits in TMEM takes this shape
+bool importance_tc_resident(const ScoreArgs& a);
 cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_gram_simt(const ScoreArgs& a, cudaStream_t s);
 bool gram_tc_shape_ok(const ScoreArgs& a);
 bool gram_tc_supported(const ScoreArgs& a);
+// the one-row-block Gram (N <= 2048), which can complete sum_i itself
+bool gram_tc_rows(const ScoreArgs& a);
 cudaError_t launch_gram_tc(const ScoreArgs& a, cudaStream_t s);
 // the tensor-core Gram for 2048 < N <= 4352 (launch_gram_tc dispatches to it)
 cudaError_t launch_gram_tc_pairs(const ScoreArgs& a, cudaStream_t s);

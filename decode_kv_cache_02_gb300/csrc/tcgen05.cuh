@@ -146,6 +146,75 @@ RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps*
         }
     }
 }
+// Eight bf16 of a 128-byte-swizzled K-major tile: 16-byte unit u of row r
+// sits at unit u ^ (r mod 8) of the row (the TMA 128-byte swizzle).
+RKV_DEV uint4 swizzled_unit(const uint8_t* tile, int r, int u) {
+    return *reinterpret_cast<const uint4*>(tile + r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// the two bf16 of a 32-bit word as a packed fp32 pair (low element first)
+RKV_DEV unsigned long long bf16x2_to_f32x2(uint32_t w) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+
+// acc.xy += a.xy * b.xy on packed fp32 pairs
+RKV_DEV void fma_f32x2(unsigned long long& acc, unsigned long long a, unsigned long long b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+RKV_DEV float f32x2_sum(unsigned long long v) {
+    return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+}
+
+// k . s over the D elements of row r of a key block (KC swizzled chunks of
+// 64), s in fp32; four packed accumulators keep the FMA chains short
+// (chunks of 128 rows x 128 bytes, kChunkBytes apart)
+template <int KC>
+RKV_DEV float row_dot(const uint8_t* blk, int r, const float* s32) {
+    constexpr int kChunkBytes = 128 * 128;
+    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < KC; ++c) {
+        const uint8_t* tile = blk + c * kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint4 k = swizzled_unit(tile, r, u);
+            const ulonglong2 s01 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8);
+            const ulonglong2 s23 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8 + 4);
+            fma_f32x2(acc[0], bf16x2_to_f32x2(k.x), s01.x);
+            fma_f32x2(acc[1], bf16x2_to_f32x2(k.y), s01.y);
+            fma_f32x2(acc[2], bf16x2_to_f32x2(k.z), s23.x);
+            fma_f32x2(acc[3], bf16x2_to_f32x2(k.w), s23.y);
+        }
+    }
+    return (f32x2_sum(acc[0]) + f32x2_sum(acc[1])) + (f32x2_sum(acc[2]) + f32x2_sum(acc[3]));
+}
+
+// The same dot product one 64-column chunk at a time, for kernels whose
+// other warps leave little register room.
+template <int KC>
+RKV_DEV float row_dot_lean(const uint8_t* blk, int r, const float* s32) {
+    constexpr int kChunkBytes = 128 * 128;
+    unsigned long long acc[2] = {0ull, 0ull};
+#pragma unroll 1
+    for (int c = 0; c < KC; ++c) {
+        const uint8_t* tile = blk + c * kChunkBytes;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint4 k = swizzled_unit(tile, r, u);
+            const ulonglong2 s01 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8);
+            const ulonglong2 s23 = *reinterpret_cast<const ulonglong2*>(s32 + c * 64 + u * 8 + 4);
+            fma_f32x2(acc[0], bf16x2_to_f32x2(k.x), s01.x);
+            fma_f32x2(acc[1], bf16x2_to_f32x2(k.y), s01.y);
+            fma_f32x2(acc[0], bf16x2_to_f32x2(k.z), s23.x);
+            fma_f32x2(acc[1], bf16x2_to_f32x2(k.w), s23.y);
+        }
+    }
+    return f32x2_sum(acc[0]) + f32x2_sum(acc[1]);
+}
+
 RKV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 RKV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 RKV_DEV void tmem_alloc(uint32_t* dst, uint32_t ncols) {
