@@ -452,6 +452,21 @@ constexpr int kRThreads = 64 + kREpi + 32 * kRDotWarps;
 constexpr uint32_t kRTmemCols = 512;
 constexpr int kRMaxSlots = 16;
 constexpr int kSRows = 2;  // s_hi, s_lo: the rows of s the dot warps read
+constexpr uint32_t kSAccCols = 32;  // two s accumulators of 16 columns (statistics mode, d = 128)
+
+// Shared-memory descriptor of a key block read as an MN-major operand (its
+// rows are keys, the contraction runs over them): 128-byte swizzle atoms of
+// 64 consecutive dimensions x 8 keys (1024 bytes), the next 8 keys 1024 bytes
+// on (stride), the next 64 dimensions one chunk (16 KB) on (leading).
+RKV_DEV uint64_t sdesc_sw128_mn(const void* p) {
+    const uint64_t a = smem_u32(p);
+    uint64_t d = (a >> 4) & 0x3FFFull;
+    d |= (uint64_t)(kChunkBytes >> 4) << 16;  // leading byte offset: the next 64 dimensions
+    d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: the next 8 keys
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
 constexpr size_t kSmemLimit = 232448;  // 227 KB of opt-in shared memory per CTA
 
 template <int D, int SC>
@@ -461,12 +476,17 @@ struct RCfg {
     static constexpr int kQChunkBytes = SC * 128;
     static constexpr int kSChunkBytes = 1024;  // kSRows rows used; 1024-byte aligned
     static constexpr int kBBytes = KC * (kQChunkBytes + kSChunkBytes);  // one problem's B operands
-    static constexpr int kFixedBars = 4 + 2 * kRMaxSlots + 2;
+    // two tiles of the s MMA's B operand (inv_hi, inv_lo of a block's keys,
+    // 14 zero rows): 16 rows x 128 keys bf16, 128-byte swizzle
+    static constexpr int kInvTileBytes = 2 * 16 * 128;
+    static constexpr int kFixedBars = 4 + 2 * kRMaxSlots + 2 + 8;
     static constexpr size_t kRedBytes = sizeof(float) * (16 * SC + kRDotWarps * D);
-    static constexpr size_t kFixed = 1024 + 2 * (size_t)kBBytes + kRedBytes + 8 * kFixedBars + 16;
+    static constexpr size_t kFixed =
+        1024 + 2 * (size_t)kInvTileBytes + 2 * (size_t)kBBytes + kRedBytes + 8 * kFixedBars + 16;
     static constexpr int kFit = (int)((kSmemLimit - kFixed) / (kBlockBytes + 16));
     static constexpr int kStages = kFit < 12 ? kFit : 12;
-    static constexpr size_t kBOff = (size_t)kStages * kBlockBytes;
+    static constexpr size_t kInvOff = (size_t)kStages * kBlockBytes;
+    static constexpr size_t kBOff = kInvOff + 2 * (size_t)kInvTileBytes;
     static constexpr size_t kRedOff = kBOff + 2 * (size_t)kBBytes;
     static constexpr size_t kBarOff = kRedOff + kRedBytes;
     static constexpr int kNumBars = 2 * kStages + kFixedBars;
@@ -640,9 +660,21 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
     uint64_t* tmem_free = blk_full + kRMaxSlots;  // [kRMaxSlots]
     uint64_t* epi_bar = tmem_free + kRMaxSlots;
     uint64_t* drain_bar = epi_bar + 1;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    // statistics mode at d = 128: s = sum_j khat_j on the tensor core
+    uint64_t* inv_full = drain_bar + 1;    // [2] a block's inv rows written
+    uint64_t* inv_empty = inv_full + 2;    // [2] their s MMAs done
+    uint64_t* sacc_full = inv_empty + 2;   // [2] a problem's s accumulated
+    uint64_t* sacc_empty = sacc_full + 2;  // [2] read by the dot warps
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sacc_empty + 2);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
     __shared__ unsigned long long s_colmask[kMaxObs + 1];
+    // kSMma: s = K_blk^T (inv_hi + inv_lo) per block, accumulated in TMEM
+    // (lanes = dimensions, two 16-column accumulators after the logit ring):
+    // A = the key block read MN-major, B = the block's inverse norms as two
+    // bf16 rows (hi, lo) and 14 zero rows
+    constexpr bool kSMma = kStats && D == 128;
+    uint8_t* sInv = smem + C::kInvOff;  // [2][C::kInvTileBytes]
+    const uint32_t sacc_col = kRTmemCols - kSAccCols;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = prm.N, n_obs = prm.n_obs;
@@ -650,6 +682,13 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
     for (int k = threadIdx.x; k <= n_obs && k <= kMaxObs; k += blockDim.x) s_colmask[k] = prm.colmask[k];
     const int T = (N + kRows - 1) / kRows;
 
+    if (kSMma) {
+        // the s MMA's B tiles: rows 2..15 stay zero, rows 0 and 1 are rewritten
+        // for every block
+        for (int i = threadIdx.x; i < 2 * C::kInvTileBytes / 16; i += blockDim.x)
+            reinterpret_cast<uint4*>(sInv)[i] = make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     // query rows R .. SC-1 of both B buffers are never loaded: zero them once
     // (their logit columns are never used, zeros keep them finite)
     if (prm.R < SC) {
@@ -677,6 +716,12 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
         }
         mbar_init(epi_bar, kREpi / 32);
         mbar_init(drain_bar, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&inv_full[t], kRDotWarps);
+            mbar_init(&inv_empty[t], 1);
+            mbar_init(&sacc_full[t], 1);
+            mbar_init(&sacc_empty[t], kRDotWarps);
+        }
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -730,12 +775,17 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_q = idesc_bf16(kRows, SC);
+            // the s MMA: M = 128 dimensions (A transposed: MN-major), N = 16
+            constexpr uint32_t idesc_s = idesc_bf16(128, 16) | (1u << 15);
             uint32_t u = 0, kp = 0;
             bool ok = true;
             for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
                 const int qb = kp & 1;
                 if (!(ok = mbar_wait(&q_full[qb], (kp >> 1) & 1, s_abort))) break;
                 const uint8_t* b_buf = sB + qb * C::kBBytes;
+                const int sbuf = kp & 1;
+                // the dot warps have read this accumulator's previous problem
+                if (kSMma && !(ok = mbar_wait(&sacc_empty[sbuf], ((kp >> 1) & 1) ^ 1, s_abort))) break;
                 for (int b = 0; b < T; ++b, ++u) {
                     const int s = u % C::kStages;
                     if (!(ok = mbar_wait(&k_full[s], (u / C::kStages) & 1, s_abort))) break;
@@ -752,8 +802,25 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                         for (int k = 0; k < kChunkElems / 16; ++k)
                             mma_bf16(d_q, ad + 2 * k, bq + 2 * k, idesc_q, (c | k) != 0);
                     }
-                    mma_commit(&k_empty[s]);
                     mma_commit(&blk_full[slot]);
+                    if (kSMma) {
+                        // s += K_blk^T (inv_hi, inv_lo): 16 keys per instruction
+                        const int t = u & 1;
+                        if (!(ok = mbar_wait(&inv_full[t], (u >> 1) & 1, s_abort))) break;
+                        tc_fence_after();
+                        const uint8_t* inv_tile = sInv + t * C::kInvTileBytes;
+#pragma unroll
+                        for (int ks = 0; ks < kRows / 16; ++ks) {
+                            const uint64_t ad = sdesc_sw128_mn(sK + s * C::kBlockBytes + ks * 2048);
+                            const uint64_t bd =
+                                sdesc_sw128(inv_tile + (ks >> 2) * (16 * 128)) + 2 * (ks & 3);
+                            mma_bf16(tmem + sacc_col + (uint32_t)(sbuf * 16), ad, bd, idesc_s,
+                                     (b | ks) != 0);
+                        }
+                        mma_commit(&inv_empty[t]);
+                        if (b == T - 1) mma_commit(&sacc_full[sbuf]);
+                    }
+                    mma_commit(&k_empty[s]);
                 }
                 if (!ok) break;
                 mma_commit(&q_empty[qb]);
@@ -777,9 +844,14 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
         const int r0 = dw * 32 + lane;
         const int c0 = lane * CPL;  // this lane's first column of s
         const int cchunk = c0 / kChunkElems, cunit = (c0 % kChunkElems) >> 3, celem = c0 & 7;
-        uint32_t kk = 0;
+        uint32_t kk = 0, kp = 0;
         bool ok = true;
-        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x) {
+        // kSMma: this lane's key in the inverse-norm tiles (row 0 hi, row 1 lo;
+        // 16-byte unit u of row r at unit u ^ r)
+        const int ichunk = r0 >> 6, iel = r0 & 63;
+        const int ioff0 = ichunk * 16 * 128 + (((iel >> 3) ^ 0) << 4) + (iel & 7) * 2;
+        const int ioff1 = ichunk * 16 * 128 + 128 + (((iel >> 3) ^ 1) << 4) + (iel & 7) * 2;
+        for (int64_t p = blockIdx.x; ok && p < prm.P; p += gridDim.x, ++kp) {
             float sacc[CPL];
 #pragma unroll
             for (int t = 0; t < CPL; ++t) sacc[t] = 0.f;
@@ -792,26 +864,45 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                 const float n2 = row_norm2<C::KC>(blk, r0);
                 // rows past N are TMA zero fill; they add nothing to s
                 const float inv = j0 < N ? 1.0f / fmaxf(sqrtf(n2), 1e-12f) : 0.f;
-                const uint8_t* tile = blk + cchunk * kChunkBytes;
-#pragma unroll 8
-                for (int rr = 0; rr < 32; ++rr) {
-                    const float iv = __shfl_sync(0xffffffffu, inv, rr);
-                    const int r = dw * 32 + rr;
-                    const uint8_t* src = tile + r * 128 + ((cunit ^ (r & 7)) << 4) + celem * 2;
-                    if constexpr (CPL == 4) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(src);
-                        sacc[0] = fmaf(__uint_as_float(v.x << 16), iv, sacc[0]);
-                        sacc[1] = fmaf(__uint_as_float(v.x & 0xffff0000u), iv, sacc[1]);
-                        sacc[2] = fmaf(__uint_as_float(v.y << 16), iv, sacc[2]);
-                        sacc[3] = fmaf(__uint_as_float(v.y & 0xffff0000u), iv, sacc[3]);
-                    } else {
-                        const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-                        sacc[0] = fmaf(__uint_as_float(v << 16), iv, sacc[0]);
-                        sacc[1] = fmaf(__uint_as_float(v & 0xffff0000u), iv, sacc[1]);
+                if constexpr (kSMma) {
+                    // inv as bf16 hi + lo into the block's B tile for the s MMA
+                    const int t = kk & 1;
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&inv_empty[t], ((kk >> 1) & 1) ^ 1, s_abort));
+                    if (!ok) break;
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(inv);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(inv - __bfloat162float(hi));
+                    uint8_t* tile_t = sInv + t * C::kInvTileBytes;
+                    *reinterpret_cast<__nv_bfloat16*>(tile_t + ioff0) = hi;
+                    *reinterpret_cast<__nv_bfloat16*>(tile_t + ioff1) = lo;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&inv_full[t]);
+                        mbar_arrive(&k_empty[st]);
                     }
+                } else {
+                    const uint8_t* tile = blk + cchunk * kChunkBytes;
+#pragma unroll 8
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const float iv = __shfl_sync(0xffffffffu, inv, rr);
+                        const int r = dw * 32 + rr;
+                        const uint8_t* src = tile + r * 128 + ((cunit ^ (r & 7)) << 4) + celem * 2;
+                        if constexpr (CPL == 4) {
+                            const uint2 v = *reinterpret_cast<const uint2*>(src);
+                            sacc[0] = fmaf(__uint_as_float(v.x << 16), iv, sacc[0]);
+                            sacc[1] = fmaf(__uint_as_float(v.x & 0xffff0000u), iv, sacc[1]);
+                            sacc[2] = fmaf(__uint_as_float(v.y << 16), iv, sacc[2]);
+                            sacc[3] = fmaf(__uint_as_float(v.y & 0xffff0000u), iv, sacc[3]);
+                        } else {
+                            const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+                            sacc[0] = fmaf(__uint_as_float(v << 16), iv, sacc[0]);
+                            sacc[1] = fmaf(__uint_as_float(v & 0xffff0000u), iv, sacc[1]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&k_empty[st]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&k_empty[st]);
                 if (j0 < N) {
                     prm.inv_norm[p * prm.ld_ws + j0] = inv;
                     // |khat_i|^2; the Gram kernel completes sum_i from it
@@ -819,18 +910,35 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                 }
             }
             if (!ok) break;
+            if constexpr (kSMma) {
+                // s of this warp's 32 dimensions (its TMEM lane quarter), once
+                // the problem's s MMAs are done
+                const int sbuf = kp & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sacc_full[sbuf], (kp >> 1) & 1, s_abort));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + sacc_col +
+                                       (uint32_t)(sbuf * 16);
+                const uint32_t shi = tmem_ld_1col(taddr), slo = tmem_ld_1col(taddr + 1);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive_warp(&sacc_empty[sbuf]);
+                prm.s32[p * prm.ld_s + (warp & 3) * 32 + lane] =
+                    __uint_as_float(shi) + __uint_as_float(slo);
+            } else {
 #pragma unroll
-            for (int t = 0; t < CPL; ++t) sDot[dw * D + c0 + t] = sacc[t];
-            named_bar_sync(1, 32 * kRDotWarps);
-            if (dw == 0) {
-                for (int c = lane; c < D; c += 32) {
-                    float v = 0.f;
+                for (int t = 0; t < CPL; ++t) sDot[dw * D + c0 + t] = sacc[t];
+                named_bar_sync(1, 32 * kRDotWarps);
+                if (dw == 0) {
+                    for (int c = lane; c < D; c += 32) {
+                        float v = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kRDotWarps; ++w) v += sDot[w * D + c];
-                    prm.s32[p * prm.ld_s + c] = v;
+                        for (int w = 0; w < kRDotWarps; ++w) v += sDot[w * D + c];
+                        prm.s32[p * prm.ld_s + c] = v;
+                    }
                 }
+                named_bar_sync(1, 32 * kRDotWarps);
             }
-            named_bar_sync(1, 32 * kRDotWarps);
         }
         if (!ok) {
             *s_abort = 1;
@@ -1053,8 +1161,9 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
 
 // Ring size of the resident variant for T key blocks of SC logit columns:
 // as many slots as TMEM holds; false when a problem does not fit.
-bool resident_ring(int T, int SC, int* ns) {
-    int n = (int)kRTmemCols / SC;
+bool resident_ring(int T, int SC, int* ns, bool s_mma) {
+    // with the s MMA, its two 16-column accumulators take the last 32 columns
+    int n = (int)(kRTmemCols - (s_mma ? kSAccCols : 0)) / SC;
     if (n > kRMaxSlots) n = kRMaxSlots;
     if (T > n) return false;
     *ns = n;
@@ -1096,7 +1205,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     if (!make_map_3d_bf16(&qmap, a.Q, D, R, a.P, D, (int64_t)R * D, R))
         return cudaErrorInvalidValue;
     const int SC = R <= 32 ? 32 : 48;
-    if (resident_ring(T, SC, &prm.ns)) {
+    if (resident_ring(T, SC, &prm.ns, a.fused_stats && D == 128)) {
         // s rows hi, lo for the dot warps
         if (!make_map_3d_bf16(&smap, a.s_rows, D, 16, a.P, D, (int64_t)16 * D, kSRows))
             return cudaErrorInvalidValue;
@@ -1155,7 +1264,7 @@ bool importance_tc_supported(const ScoreArgs& a) {
 bool importance_tc_resident(const ScoreArgs& a) {
     int ns = 0;
     return importance_tc_shape_ok(a) &&
-           resident_ring((a.N + kRows - 1) / kRows, a.G * a.n_obs <= 32 ? 32 : 48, &ns);
+           resident_ring((a.N + kRows - 1) / kRows, a.G * a.n_obs <= 32 ? 32 : 48, &ns, a.d == 128);
 }
 
 cudaError_t launch_importance_tc(const ScoreArgs& a, cudaStream_t s) {
