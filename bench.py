@@ -37,20 +37,26 @@ from decode_kv_cache_02_gb300 import rkv, workloads as wl  # noqa: E402
 METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM roofline"
 
 # DRAM bytes (read + write) per problem measured by ncu on a 1,024-problem
-# copy of the Llama-8B-shaped workload (the committed per-kernel ncu summaries),
+# copy of the Llama-8B-shaped workload and a 768-problem copy of the
+# Qwen-14B-shaped one (the committed per-kernel ncu summaries),
 # with the sha256 of the kernel source they were measured on; a changed source
 # reports traffic null.  Every kernel streams whole problems, so traffic scales
 # with the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "key_stats": ("k_key_stats.cu", "03897fc1bf8d43d84450d36afa083d6d16ef1ead924e20c4f9882ac2b9628bd2", 315437568 / 1024),
-        "importance_tc": ("k_importance_tc.cu", "05779ee5a23e7a83691687af581eaf14ab8639e98c03fcf69af01bb3fe1ee170", 329676032 / 1024),
-        "gram_tc": ("k_gram_tc.cu", "a1f22fe57dc911bcf1473e9384d3fd56fa116ec9d5a4da73ee4233057aced27d", 323257344 / 1024),
-        "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", 1035325952 / 1024),
+        "importance_tc": ("k_importance_tc.cu", "9bfd3c1bdfb57b7f5e91f4c4d056f95d05bcd45d6cfedcfd56964d7a8790a5ba", (310468352 + 12898304) / 1024),
+        "gram_tc": ("k_gram_tc.cu", "6a17a059df70301d9e6d9c8b93c6b7a3c86d7e6a07a2edaa71413527997b4fea", (317357824 + 9674496) / 1024),
+        "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", (541691648 + 494446592) / 1024),
+    },
+    # the Qwen-14B-shaped step, captured on 768 problems (K 830 MB)
+    "qwen14b": {
+        "key_stats": ("k_key_stats.cu", "95b35392fb1c978ea7baa169ce85d537de074573cfd2711b5af30a594ca84177", (830589000 + 31737000) / 768),
+        "importance_tc": ("k_importance_tc.cu", "9bfd3c1bdfb57b7f5e91f4c4d056f95d05bcd45d6cfedcfd56964d7a8790a5ba", (1207313000 + 25321000) / 768),
+        "gram_tc": ("k_gram_tc_pairs.cu", "dab1c4a2a6a9ea890616f2f0e167444f8cf9c095bb971a59f270ebc27c8d7e1e", (3799878000 + 34044000) / 768),
+        "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", (1623769000 + 1577997000) / 768),
     },
     # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
-        "key_stats_paged": ("k_key_stats.cu", "03897fc1bf8d43d84450d36afa083d6d16ef1ead924e20c4f9882ac2b9628bd2", 316715008 / 1024),
         "compact_paged": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", 966686464 / 1024),
     },
 }
