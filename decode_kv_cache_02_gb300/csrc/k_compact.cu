@@ -17,10 +17,18 @@
 //           is ranked exactly (directly for up to 32 keys, else radix passes
 //           over its compacted keys); a block scan in index order places each
 //           kept index.
-//   copy    16-byte vectors, several in flight per thread.  In place, rows
+//   copy    by the TMA engine, through a ring of shared-memory stages: per
+//           chunk of 32 output rows, each run of consecutive kept source rows
+//           is one bulk load per tensor into the chunk's stage, and once the
+//           stage is full one bulk store per tensor writes the chunk to its
+//           contiguous output rows.  One warp keeps several chunks in flight
+//           while the CTA's other warps have left, so a few SMs move the rows
+//           at a rate that otherwise takes most of them.  In place, rows
 //           before the first evicted token are skipped and the rest move in
-//           ascending chunks, each read completely before any of it is written
-//           (kept indices are ascending and idx[r] >= r).
+//           ascending chunks: kept indices ascend and idx[r] >= r, so a chunk's
+//           sources lie at or after its own rows and after every earlier
+//           chunk's, and each chunk is stored only after its loads and those
+//           of every earlier chunk have landed.
 //   paged   the same chunked in-place order through the block table: kept V
 //           rows move inside the pool, kept K rows come from the contiguous
 //           copy the key statistics wrote (so K's reads never meet its
@@ -29,6 +37,7 @@
 #include "rkv_internal.h"
 #include "rkv_paged.cuh"
 #include "rkv_variant.cuh"
+#include "tcgen05.cuh"
 #include "../../include/rkv.h"
 
 namespace rkv {
@@ -277,12 +286,132 @@ __device__ __forceinline__ void take_top(uint32_t* keys, int C, uint32_t uk, uin
     }
 }
 
+// ------------------------------------------------------- bulk row copy --
+constexpr int kChunkRows = 32;     // output rows per stage (one per lane)
+constexpr int kMaxStages = 8;
+constexpr size_t kStageTarget = 112 * 1024;  // shared memory per CTA with the stages
+
+RKV_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(tc::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
+        : "memory");
+}
+RKV_DEV void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(tc::smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+RKV_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// every committed store group but the newest has read its shared memory
+RKV_DEV void bulk_wait_read_but_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+RKV_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Output rows [r0, budget) of one problem from source rows sidx[r] (one warp).
+// a / b: the two tensors (b may be null), rows of rb bytes, sources n_cap rows
+// per problem; stages: S buffers of kChunkRows rows per tensor, full: their
+// mbarriers (count 1, fresh).  Lane 0 issues and waits for every store.
+RKV_DEV void copy_rows_bulk(const int32_t* sidx, int r0, int budget, int n_cap,
+                            const uint8_t* a_src, const uint8_t* b_src, uint8_t* a_dst,
+                            uint8_t* b_dst, int rb, uint8_t* stages, uint64_t* full, int S,
+                            volatile int* abort_flag, DeviceStatus* st) {
+    const int lane = threadIdx.x & 31;
+    const int nch = (budget - r0 + kChunkRows - 1) / kChunkRows;
+    const int tensors = b_src ? 2 : 1;
+    const size_t tbytes = (size_t)kChunkRows * rb;  // one tensor's part of a stage
+    auto stage = [&](int ch) { return stages + (size_t)(ch % S) * tensors * tbytes; };
+    // loads of chunk ch: lane l holds row r0 + 32 ch + l
+    auto issue = [&](int ch) {
+        const int r = r0 + ch * kChunkRows + lane;
+        const int src = r < budget ? sidx[r] : -1;
+        const bool ok = src >= 0 && src < n_cap;
+        if (r < budget && !ok) set_error(st, kDevErrIndex, (unsigned)r);
+        const int prev = __shfl_up_sync(0xffffffffu, src, 1);
+        const bool start = ok && (lane == 0 || prev != src - 1);
+        const unsigned cont = __ballot_sync(0xffffffffu, ok && !start);
+        const unsigned okm = __ballot_sync(0xffffffffu, ok);
+        const unsigned after = lane < 31 ? cont >> (lane + 1) : 0u;
+        const int len = __ffs(~after);  // this row and the run's rows after it
+        uint64_t* bar = &full[ch % S];
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)(__popc(okm) * rb * tensors));
+        __syncwarp();
+        if (start) {
+            uint8_t* d = stage(ch) + (size_t)lane * rb;
+            bulk_load(d, a_src + (size_t)src * rb, (uint32_t)(len * rb), bar);
+            if (b_src) bulk_load(d + tbytes, b_src + (size_t)src * rb, (uint32_t)(len * rb), bar);
+        }
+        return okm;
+    };
+    unsigned okm[kMaxStages];
+    const int pre = nch < S ? nch : S;
+    for (int ch = 0; ch < pre; ++ch) okm[ch] = issue(ch);
+    bool ok = true;
+    int waited = 0;    // chunks whose loads are known to have landed
+    int issued = pre;  // chunks whose loads have been issued
+    for (int ch = 0; ch < nch; ++ch) {
+        const int sl = ch % S;
+        if (lane == 0) {
+            ok = tc::mbar_wait(&full[sl], (uint32_t)(ch / S) & 1u, abort_flag);
+            if (!ok) {
+                set_error(st, kDevErrTimeout, 0x300u);
+                *abort_flag = 1;
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        waited = ch + 1;
+        if (lane == 0) {
+            const size_t o = (size_t)(r0 + ch * kChunkRows) * rb;
+            const unsigned m = okm[sl];
+            if (m == 0xffffffffu || (m & (m + 1u)) == 0u) {
+                // the chunk's rows are a prefix of it (the last chunk may be short)
+                const uint32_t n = (uint32_t)__popc(m) * (uint32_t)rb;
+                if (n) {
+                    bulk_store(a_dst + o, stage(ch), n);
+                    if (b_src) bulk_store(b_dst + o, stage(ch) + tbytes, n);
+                }
+            } else {
+                for (int l = 0; l < kChunkRows; ++l)
+                    if (m >> l & 1u) {
+                        bulk_store(a_dst + o + (size_t)l * rb, stage(ch) + (size_t)l * rb, rb);
+                        if (b_src)
+                            bulk_store(b_dst + o + (size_t)l * rb,
+                                       stage(ch) + tbytes + (size_t)l * rb, rb);
+                    }
+            }
+            bulk_commit();
+        }
+        // the stage of chunk ch - 1 takes chunk ch - 1 + S once its store has read it
+        const int nxt = ch - 1 + S;
+        if (ch >= 1 && nxt < nch) {
+            if (lane == 0) bulk_wait_read_but_one();
+            __syncwarp();
+            okm[nxt % S] = issue(nxt);
+            issued = nxt + 1;
+        }
+    }
+    if (!ok && lane == 0) {
+        // loads still in flight land before the shared memory is given up
+        // (each wait bounded again)
+        for (int ch = waited; ch < issued; ++ch) {
+            const long long t0 = clock64();
+            while (!tc::mbar_try_wait(&full[ch % S], (uint32_t)(ch / S) & 1u) &&
+                   clock64() - t0 < tc::kWaitCycles) {
+            }
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
 template <bool kPaged>
 __global__ void __launch_bounds__(kThreads)
 compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int budget,
                int32_t* __restrict__ idx, const uint4* a_src, const uint4* b_src, uint4* a_dst,
                uint4* b_dst, int n_cap, int out_cap, int vpr, int in_place, DeviceStatus* st,
-               VariantIn var, PagedIn pg) {
+               VariantIn var, PagedIn pg, int stages, uint32_t stage_off) {
     extern __shared__ uint32_t s_dyn[];
     const int C = N - n_obs, k = budget - n_obs;
     uint32_t* keys = s_dyn;                                         // [C]
@@ -426,6 +555,38 @@ compact_kernel(const float* __restrict__ Z, int64_t ldz, int N, int n_obs, int b
         return;
     }
     const int64_t base = (int64_t)p * n_cap * vpr;
+    if (stages > 0) {
+        __shared__ uint64_t s_full[kMaxStages];
+        __shared__ int s_abort;
+        if (tid >= 32) return;  // one warp moves the rows
+        int r0 = 0;
+        if (in_place) {
+            // first row r0 with sidx[r0] != r0 (sidx[r] == r holds exactly on a prefix)
+            int l = 0, h = budget;
+            while (l < h) {
+                const int mid = (l + h) >> 1;
+                if (sidx[mid] == mid) l = mid + 1;
+                else h = mid;
+            }
+            r0 = l;
+        }
+        if (tid == 0) {
+            for (int i = 0; i < stages; ++i) tc::mbar_init(&s_full[i], 1);
+            s_abort = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        const int rb = vpr * 16;
+        const int64_t ob = in_place ? base : (int64_t)p * out_cap * vpr;
+        uint8_t* stage_mem = reinterpret_cast<uint8_t*>(s_dyn) + stage_off;
+        if (r0 < budget)
+            copy_rows_bulk(sidx, r0, budget, n_cap, reinterpret_cast<const uint8_t*>(a_src + base),
+                           b_src ? reinterpret_cast<const uint8_t*>(b_src + base) : nullptr,
+                           reinterpret_cast<uint8_t*>(a_dst + ob),
+                           b_dst ? reinterpret_cast<uint8_t*>(b_dst + ob) : nullptr, rb, stage_mem,
+                           s_full, stages, &s_abort, st);
+        return;
+    }
     if (!in_place) {
         const int64_t obase = (int64_t)p * out_cap * vpr;
         const int total = budget * vpr;
@@ -511,14 +672,22 @@ cudaError_t launch_compact(int64_t P, int N, const float* Z, int64_t ldz, int n_
                            void* dst_b, int n_cap, int out_cap, int row_bytes, bool in_place,
                            DeviceStatus* st, cudaStream_t s, const VariantIn& var) {
     if (P == 0 || budget == 0) return cudaSuccess;
-    const size_t smem = compact_smem_bytes(N, n_obs, budget, var.pen != nullptr);
+    const size_t sel = compact_smem_bytes(N, n_obs, budget, var.pen != nullptr);
+    // the stages of the bulk copy after the selection's arrays, 128-byte aligned
+    const size_t off = (sel + 127) / 128 * 128;
+    const size_t stage_bytes = (size_t)kChunkRows * row_bytes * (src_b ? 2 : 1);
+    int stages = off < kStageTarget ? (int)((kStageTarget - off) / stage_bytes) : 0;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) stages = 0;  // too little room: the register copy
+    const size_t smem = stages ? off + stages * stage_bytes : sel;
     cudaError_t e = cudaFuncSetAttribute(compact_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     compact_kernel<false><<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(src_a),
         static_cast<const uint4*>(src_b), static_cast<uint4*>(dst_a), static_cast<uint4*>(dst_b), n_cap,
-        in_place ? n_cap : out_cap, row_bytes / 16, in_place ? 1 : 0, st, var, PagedIn{});
+        in_place ? n_cap : out_cap, row_bytes / 16, in_place ? 1 : 0, st, var, PagedIn{}, stages,
+        (uint32_t)off);
     return cudaGetLastError();
 }
 
@@ -534,7 +703,7 @@ cudaError_t launch_compact_paged(int64_t P, int N, const float* Z, int64_t ldz, 
     compact_kernel<true><<<(unsigned)P, kThreads, smem, s>>>(
         Z, ldz, N, n_obs, budget, idx, static_cast<const uint4*>(kc), nullptr,
         static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), N, N, row_bytes / 16, 1, st, var,
-        pg);
+        pg, 0, 0u);
     return cudaGetLastError();
 }
 

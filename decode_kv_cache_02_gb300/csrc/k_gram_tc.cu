@@ -695,7 +695,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t sms = sm_count();
+    const int64_t sms = a.sms > 0 ? a.sms : sm_count();
     const int64_t grid = a.P < sms ? a.P : sms;
     kern<<<(unsigned)grid, kThreads + (kDot ? 32 * kDotWarps : 0), C::kSmemBytes, s>>>(map, bmap, prm, static_cast<const float*>(a.s_rows));
     return cudaGetLastError();

@@ -630,7 +630,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t sms = sm_count();
+    const int64_t sms = a.sms > 0 ? a.sms : sm_count();
     const int64_t grid = a.P < sms ? a.P : sms;
     kern<<<(unsigned)grid, kThreads, C::kSmemBytes, s>>>(map, prm);
     return cudaGetLastError();

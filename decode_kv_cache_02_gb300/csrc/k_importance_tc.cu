@@ -1196,7 +1196,7 @@ cudaError_t launch_t(const ScoreArgs& a, cudaStream_t s) {
     }
     for (int c = 0; c < R; ++c)
         if (c % a.n_obs == a.n_obs - 1) prm.lastmask |= 1ull << c;
-    const int64_t cap = (int64_t)sm_count();
+    const int64_t cap = a.sms > 0 ? a.sms : (int64_t)sm_count();
     const int64_t grid = a.P < cap ? a.P : cap;
     const int T = (a.N + kRows - 1) / kRows;
     KeyMaps kmap;

@@ -14,6 +14,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <array>
+#include <map>
+#include <mutex>
 #include <vector>
 
 #include "../../include/rkv.h"
@@ -49,20 +52,25 @@ const char* const kKernelNames[kNumKernels] = {
     "sentence_penalty", "sentence_reps"};
 
 // ---------------------------------------------------------------- timing --
+// Events belong to the context they were created in, and a stream records
+// only its own context's events: each pool is kept per context (nullptr: the
+// caller's), the one current while the launch is enqueued.
 struct TimedLaunch {
     int kernel;
     cudaEvent_t start, stop;
+    const void* ctx;
 };
 bool g_timing = false;
 std::vector<TimedLaunch> g_pending;
 double g_total_ms[kNumKernels];
 int64_t g_launches[kNumKernels];
-std::vector<cudaEvent_t> g_event_pool;
+std::map<const void*, std::vector<cudaEvent_t>> g_event_pool;
 
-cudaEvent_t take_event() {
-    if (!g_event_pool.empty()) {
-        cudaEvent_t e = g_event_pool.back();
-        g_event_pool.pop_back();
+cudaEvent_t take_event(const void* ctx) {
+    std::vector<cudaEvent_t>& pool = g_event_pool[ctx];
+    if (!pool.empty()) {
+        cudaEvent_t e = pool.back();
+        pool.pop_back();
         return e;
     }
     cudaEvent_t e = nullptr;
@@ -70,11 +78,12 @@ cudaEvent_t take_event() {
     return e;
 }
 
-// Runs `launch` with events around it when timing is on.
+// Runs `launch` with events around it when timing is on; ctx names the
+// context current meanwhile (a lane's, or nullptr for the caller's).
 template <typename F>
-cudaError_t timed(int kernel, cudaStream_t s, F&& launch) {
+cudaError_t timed(int kernel, cudaStream_t s, F&& launch, const void* ctx = nullptr) {
     if (!g_timing) return launch();
-    TimedLaunch t{kernel, take_event(), take_event()};
+    TimedLaunch t{kernel, take_event(ctx), take_event(ctx), ctx};
     cudaEventRecord(t.start, s);
     cudaError_t e = launch();
     cudaEventRecord(t.stop, s);
@@ -244,10 +253,9 @@ int check_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, 
 // Runs the four scoring stages; I/R/Z land in the given rows.  With a paged
 // K (pg), the key statistics read through the block table and write the
 // contiguous copy w.Kc, which the later stages read.
-int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
-               float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
-               const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr,
-               bool direct = false) {
+ScoreArgs score_args(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
+                     float lambda, int beta, float tau, float* I, float* R, float* Z,
+                     int64_t ld_out, const Workspace& w) {
     // I, R, Z as defined on the page (R may be null: not stored)
     ScoreArgs a{};
     a.K = K;
@@ -271,6 +279,22 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     a.Z = Z;
     a.ld_out = ld_out;
     a.status = w.status;
+    return a;
+}
+
+// Whether the importance kernel takes the key statistics and the Gram
+// completes sum_i (contiguous keys whose rows fit the resident importance
+// kernel and the one-row-block Gram): no pass over K is spent on them.
+bool stats_fused(const ScoreArgs& b) {
+    return !b.pg.table && rkv::gram_tc_supported(b) && rkv::importance_tc_supported(b) &&
+           rkv::importance_tc_resident(b) && rkv::gram_tc_rows(b);
+}
+
+int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
+               float lambda, int beta, float tau, float* I, float* R, float* Z, int64_t ld_out,
+               const Workspace& w, cudaStream_t s, const rkv::PagedIn* pg = nullptr,
+               bool direct = false) {
+    ScoreArgs a = score_args(d, K, Q, n_cached, n_obs, lambda, beta, tau, I, R, Z, ld_out, w);
     ScoreArgs b = a;  // what the stages after the key statistics read
     if (pg) {
         a.pg = *pg;
@@ -289,11 +313,7 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     const bool gram_tc = rkv::gram_tc_supported(b);
     const bool imp_tc = rkv::importance_tc_supported(b);
     a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
-    // contiguous keys whose rows fit the resident importance kernel and the
-    // one-row-block Gram: the importance kernel takes the key statistics and
-    // the Gram completes sum_i, so no pass over K is spent on the statistics
-    b.fused_stats = !pg && gram_tc && imp_tc && rkv::importance_tc_resident(b) &&
-                    rkv::gram_tc_rows(b);
+    b.fused_stats = !pg && stats_fused(b);
     cudaError_t e = b.fused_stats ? cudaSuccess
                                   : timed(pg ? kKeyStatsPaged : kKeyStats, s,
                                           [&] { return rkv::launch_key_stats(a, s); });
@@ -309,6 +329,167 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
         else
             e = timed(kGramSimt, s, [&] { return rkv::launch_gram_simt(b, s); });
     }
+    return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- overlap --
+// The step on two SM partitions of the device (rkv_lanes.cu).  The importance
+// and the Gram are bound by their SMs (the importance's time grows as the
+// SMs it gets shrink, the Gram's by the tensor pipe), the compaction by HBM,
+// which a part of the SMs already nearly fills.  So the problems are cut into
+// groups, the tensor lane (most SMs) runs importance and Gram group after
+// group, and the hbm lane (the rest) compacts each group once its Gram is
+// done, while the tensor lane goes on with the next.  The last group's
+// compaction takes the whole device.  Groups only shift the base pointers:
+// every kernel sees a smaller call of the same shape.
+// Eight groups with 112 of GB300's 152 SMs on the tensor lane measured best
+// on the Llama-shaped step (6.54 ms against 6.85 for one launch per stage;
+// 104-116 SMs and 6-9 groups were within 0.2 ms).  tensor_sms 0: the same
+// share of the device's SMs.
+int g_overlap_groups = 8;  // below 2: one launch per stage over all problems
+int g_overlap_tensor_sms = 0;
+std::mutex g_overlap_mu;  // one call at a time enqueues on the shared lanes
+
+int overlap_tensor_sms() {
+    if (g_overlap_tensor_sms > 0) return g_overlap_tensor_sms;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms * 112 / 152 / 4 * 4;
+}
+constexpr int kMaxGroups = 32;
+
+struct LaneEvents {
+    cudaEvent_t ev[kMaxGroups + 2] = {};
+    bool made = false;
+};
+
+// Per-group events of one lane, created in the lane's context.
+bool lane_events(const rkv::Lane* lane, LaneEvents* le) {
+    if (le->made) return true;
+    rkv::LaneScope scope(lane);
+    for (auto& e : le->ev)
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+    le->made = true;
+    return true;
+}
+
+ScoreArgs group_args(const ScoreArgs& b, int64_t p0, int64_t n) {
+    ScoreArgs c = b;
+    const int64_t es = 2;  // the fused path is bf16 only
+    c.K = static_cast<const char*>(b.K) + p0 * b.n_cap * b.d * es;
+    c.Q = static_cast<const char*>(b.Q) + p0 * b.G * b.n_obs * b.d * es;
+    c.P = n;
+    c.inv_norm += p0 * b.ld_ws;
+    c.sum_s += p0 * b.ld_ws;
+    c.s_rows = static_cast<char*>(b.s_rows) + p0 * 32 * b.d;  // 16 bf16 rows of d per problem
+    c.I += p0 * b.ld_out;
+    c.Z += p0 * b.ld_out;
+    if (c.R) c.R += p0 * b.ld_out;
+    return c;
+}
+
+struct CompactCall {
+    int n_cached, tail, budget, n_cap, ocap, row_bytes;
+    bool in_place;
+    const void *K, *V;
+    void *out_K, *out_V;
+    int32_t* out_idx;
+};
+
+cudaError_t compact_group(const ScoreArgs& g, int64_t p0, const CompactCall& c, cudaStream_t s) {
+    const int64_t rb = c.row_bytes;
+    return rkv::launch_compact(g.P, c.n_cached, g.Z, g.ld_out, c.tail, c.budget,
+                               c.out_idx + p0 * c.budget,
+                               static_cast<const char*>(c.K) + p0 * c.n_cap * rb,
+                               static_cast<const char*>(c.V) + p0 * c.n_cap * rb,
+                               static_cast<char*>(c.out_K) + p0 * c.ocap * rb,
+                               static_cast<char*>(c.out_V) + p0 * c.ocap * rb, c.n_cap, c.ocap,
+                               c.row_bytes, c.in_place, g.status, s);
+}
+
+// Returns -1 when the step does not take this schedule (the caller runs the
+// serial one), else an RKV_* code.
+int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s) {
+    if (g_overlap_groups < 2 || g_overlap_groups > kMaxGroups) return -1;
+    const int tensor_sms = overlap_tensor_sms();
+    // at least a few waves of the tensor lane per group, or nothing to gain
+    if (tensor_sms < 8 || base.P < 2 * (int64_t)g_overlap_groups * tensor_sms) return -1;
+    ScoreArgs b = base;
+    if (!stats_fused(b)) return -1;
+    b.fused_stats = true;
+    // a stream being captured into a graph keeps the one-launch schedule
+    // (the lanes' streams belong to other contexts)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return -1;
+    std::lock_guard<std::mutex> lock(g_overlap_mu);
+    const rkv::Lanes* L = rkv::lanes_for_current_device(tensor_sms);
+    if (!L) return -1;
+    const rkv::Lane* T = &L->tensor;
+    const rkv::Lane* H = &L->hbm;
+    // Group bounds: equal groups of whole waves of the tensor lane's
+    // persistent CTAs, the last one the remainder.  Each group costs the
+    // tensor lane a launch ramp and a tail of its two kernels (~45 us
+    // measured on the Llama-shaped step), and the step ends with the hbm
+    // lane's compaction of the second-to-last group and the whole device's of
+    // the last, so a handful of groups is the balance.
+    const int64_t wave = T->sms;
+    int64_t per = (b.P + g_overlap_groups - 1) / g_overlap_groups;
+    per = (per + wave - 1) / wave * wave;
+    int64_t bounds[kMaxGroups + 1];
+    int G = 0;
+    bounds[0] = 0;
+    while (G < kMaxGroups - 1 && bounds[G] + per < b.P) {
+        bounds[G + 1] = bounds[G] + per;
+        ++G;
+    }
+    bounds[++G] = b.P;
+    if (G < 2) return -1;
+    static std::map<const rkv::Lanes*, std::array<LaneEvents, 3>> events;  // per split and device
+    LaneEvents& ev_t = events[L][0];
+    LaneEvents& ev_h = events[L][1];
+    LaneEvents& ev_s = events[L][2];
+    if (!lane_events(T, &ev_t) || !lane_events(H, &ev_h) || !lane_events(nullptr, &ev_s))
+        return RKV_ERR_CUDA;
+    auto first = [&](int c) { return bounds[c]; };
+    auto group = [&](int c) { return group_args(b, bounds[c], bounds[c + 1] - bounds[c]); };
+    // ev_s[0]: the call's start on the caller's stream; ev_t[c]: the Gram of
+    // group c done; ev_h[0]: the hbm lane's last compaction done
+    cudaError_t e = cudaEventRecord(ev_s.ev[0], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(T->stream, ev_s.ev[0], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(H->stream, ev_s.ev[0], 0);
+    for (int c = 0; c < G && e == cudaSuccess; ++c) {
+        ScoreArgs g = group(c);
+        g.sms = T->sms;
+        {
+            rkv::LaneScope scope(T);
+            e = timed(kImportanceTc, T->stream,
+                      [&] { return rkv::launch_importance_tc(g, T->stream); }, T->ctx);
+            if (e == cudaSuccess)
+                e = timed(kGramTc, T->stream, [&] { return rkv::launch_gram_tc(g, T->stream); },
+                          T->ctx);
+            if (e == cudaSuccess) e = cudaEventRecord(ev_t.ev[c], T->stream);
+        }
+        if (e != cudaSuccess || c + 1 == G) break;
+        e = cudaStreamWaitEvent(H->stream, ev_t.ev[c], 0);
+        if (e == cudaSuccess) {
+            rkv::LaneScope scope(H);
+            e = timed(kCompact, H->stream, [&] { return compact_group(g, first(c), cc, H->stream); },
+                      H->ctx);
+        }
+    }
+    if (e == cudaSuccess) {
+        rkv::LaneScope scope(H);
+        e = cudaEventRecord(ev_h.ev[0], H->stream);
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_t.ev[G - 1], 0);
+    if (e == cudaSuccess) {
+        const ScoreArgs g = group(G - 1);
+        e = timed(kCompact, s, [&] { return compact_group(g, first(G - 1), cc, s); });
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_h.ev[0], 0);
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
@@ -427,7 +608,7 @@ int rkv_compress_ex(const rkv_desc* desc, const void* K, const void* V, const vo
                     void* workspace, size_t workspace_bytes, void* stream) {
     return rkv::compress_call(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau,
                               variant, out_K, out_V, out_idx, workspace, workspace_bytes, stream,
-                              false);
+                              false, true);
 }
 
 }  // extern "C"
@@ -441,7 +622,8 @@ namespace rkv {
 int compress_call(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
                   int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                   const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
-                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status) {
+                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status,
+                  bool lanes) {
     VarFlags vf;
     int rc = check_variant(variant, &vf);
     if (rc) return rc;
@@ -503,6 +685,15 @@ int compress_call(const rkv_desc* desc, const void* K, const void* V, const void
     if (sample && !fused) return RKV_ERR_UNSUPPORTED;
     if (clear_status && cudaMemsetAsync(w.status, 0, sizeof(DeviceStatus), s) != cudaSuccess)
         return RKV_ERR_CUDA;
+    if (lanes && fused && !vf.any()) {
+        // the two-partition schedule, where the step takes it
+        const ScoreArgs a = score_args(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
+                                       nullptr, w.Z, w.ld, w);
+        const CompactCall cc{n_cached, tail, budget, desc->n_capacity, ocap, row_bytes, in_place,
+                             K, V, out_K, out_V, out_idx};
+        rc = run_overlapped(a, cc, s);
+        if (rc >= 0) return rc;
+    }
     if (!fused && (vf.zvar || tail > n_obs)) {
         rc = run_scores_variant(desc, K, Q_obs, n_cached, n_obs, lambda, beta, tau, *variant,
                                 nullptr, nullptr, w.Z, w.ld, w, s);
@@ -828,6 +1019,14 @@ const char* rkv_strerror(int code) {
     }
 }
 
+int rkv_set_overlap(int groups, int tensor_sms) {
+    if (groups > kMaxGroups || (tensor_sms != 0 && tensor_sms < 8)) return RKV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_overlap_mu);
+    g_overlap_groups = groups;
+    g_overlap_tensor_sms = tensor_sms;
+    return RKV_OK;
+}
+
 int rkv_timing_enable(int on) {
     g_timing = on != 0;
     return RKV_OK;
@@ -840,8 +1039,8 @@ int rkv_timing_read(double* total_ms, int64_t* launches, int max_kernels, int re
         cudaEventElapsedTime(&ms, t.start, t.stop);
         g_total_ms[t.kernel] += ms;
         g_launches[t.kernel] += 1;
-        g_event_pool.push_back(t.start);
-        g_event_pool.push_back(t.stop);
+        g_event_pool[t.ctx].push_back(t.start);
+        g_event_pool[t.ctx].push_back(t.stop);
     }
     g_pending.clear();
     for (int k = 0; k < kNumKernels && k < max_kernels; ++k) {

@@ -69,6 +69,36 @@ struct ScoreArgs {
     // |khat_i|^2, s in fp32 at s_rows) and the Gram completes sum_i; no
     // separate statistics pass
     bool fused_stats = false;
+    // SMs the persistent kernels size their grid to (0: the whole device);
+    // the SM count of the partition they are launched on
+    int sms = 0;
+};
+
+// One SM partition of the device with a stream of its own (rkv_lanes.cu).
+struct Lane {
+    void* ctx = nullptr;  // the partition's CUcontext
+    cudaStream_t stream = nullptr;
+    int sms = 0;
+};
+// tensor: the Gram's partition; hbm: the importance and compaction's.
+struct Lanes {
+    Lane tensor, hbm;
+};
+// The split of the current device with about tensor_sms SMs on the tensor
+// lane (whole groups of the split, 4 SMs here), created on first use and kept; nullptr when the
+// driver offers no SM partitions.
+const Lanes* lanes_for_current_device(int tensor_sms);
+// Makes a lane's context current for the scope: kernels launched and events
+// created meanwhile belong to the lane (lane == nullptr: no change).
+class LaneScope {
+public:
+    explicit LaneScope(const Lane* lane);
+    ~LaneScope();
+    LaneScope(const LaneScope&) = delete;
+    LaneScope& operator=(const LaneScope&) = delete;
+
+private:
+    bool pushed_;
 };
 
 cudaError_t launch_key_stats(const ScoreArgs& a, cudaStream_t s);
@@ -166,10 +196,13 @@ cudaError_t launch_variant(int64_t P, int N, int n_obs, const VariantIn& v, floa
 cudaError_t launch_wait_timeout(DeviceStatus* st, cudaStream_t s);
 
 // rkv_compress_ex; with clear_status the workspace's device error word is
-// cleared (enqueued) once the arguments have passed every check.
+// cleared (enqueued) once the arguments have passed every check; with lanes
+// the step may take the two-partition schedule (rkv_set_overlap), whose first
+// use creates the partitions' contexts.
 int compress_call(const rkv_desc* desc, const void* K, const void* V, const void* Q_obs,
                   int n_cached, int budget, int n_obs, float lambda, int beta, float tau,
                   const rkv_variant* variant, void* out_K, void* out_V, int32_t* out_idx,
-                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status);
+                  void* workspace, size_t workspace_bytes, void* stream, bool clear_status,
+                  bool lanes);
 
 }  // namespace rkv

@@ -55,7 +55,8 @@ extern "C" int rkv_compress_noalloc(const rkv_desc* desc, const void* K, const v
     if (scratch_for_current_device(&scratch) != cudaSuccess) return RKV_ERR_CUDA;
     return rkv::compress_call(desc, K, V, Q_obs, n_cached, budget, n_obs, lambda, beta, tau,
                               nullptr, out_K, out_V, out_idx, scratch,
-                              (size_t)RKV_NOALLOC_SCRATCH_BYTES, stream, true);
+                              (size_t)RKV_NOALLOC_SCRATCH_BYTES, stream, true,
+                              false);  // creating partitions may allocate
 }
 
 extern "C" int rkv_noalloc_device_status(void* stream) {

@@ -28,7 +28,7 @@ EXPORTED = [
     "rkv_timing_read", "rkv_kernel_name", "rkv_compress_noalloc", "rkv_compress_ex",
     "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
     "rkv_sentence_reps", "rkv_sentence_penalty", "rkv_selftest_wait_timeout",
-    "rkv_noalloc_device_status", "rkv_noalloc_selftest_wait_timeout",
+    "rkv_noalloc_device_status", "rkv_noalloc_selftest_wait_timeout", "rkv_set_overlap",
 ]
 RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_DEVICE = 6
@@ -196,6 +196,8 @@ def load(path: str | None = None):
         lib.rkv_get_device_status.restype = i32
         lib.rkv_strerror.argtypes = [i32]
         lib.rkv_strerror.restype = ctypes.c_char_p
+        lib.rkv_set_overlap.argtypes = [i32, i32]
+        lib.rkv_set_overlap.restype = i32
         lib.rkv_timing_enable.argtypes = [i32]
         lib.rkv_timing_enable.restype = i32
         lib.rkv_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -438,6 +440,16 @@ def rkv_workspace_init(workspace, stream=None):
 def rkv_get_device_status(workspace, stream=None) -> int:
     """Synchronises the stream; returns RKV_OK or the device error code."""
     return int(load().rkv_get_device_status(workspace.data_ptr(), _stream_ptr(stream)))
+
+
+DEFAULT_OVERLAP = (8, 0)  # the library's default step schedule
+
+
+def rkv_set_overlap(groups: int, tensor_sms: int = 0):
+    """Step schedule of rkv_compress: groups >= 2 scores each group of
+    problems on about tensor_sms SMs (0: 112 of every 152) while the previous
+    group is compacted on the rest; groups < 2 is one launch per stage."""
+    _check(load().rkv_set_overlap(int(groups), int(tensor_sms)), "rkv_set_overlap")
 
 
 def rkv_timing_enable(on: bool = True):

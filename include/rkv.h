@@ -368,6 +368,24 @@ int rkv_selftest_wait_timeout(void* workspace, void* stream);
 /* Human-readable name of an RKV_* code. */
 const char* rkv_strerror(int code);
 
+/* Step schedule of rkv_compress / rkv_compress_ex (process-wide).  A call
+ * whose keys are contiguous bf16 rows with N <= 2048, that passes no variant,
+ * whose selection fits the fused compaction and whose stream is not being
+ * captured into a graph runs on two SM partitions of the device (driver green
+ * contexts, created at the first such call and kept): the problems are cut
+ * into `groups` equal groups; importance and Gram of each group run on the
+ * tensor partition (about tensor_sms SMs), and each group's selection and
+ * row copy run on the other SMs while the tensor partition scores the next
+ * group (the last group's on the whole device).  It needs at least
+ * 2 * groups * tensor_sms problems.  Results are bit for bit those of one
+ * launch per stage over the whole device (groups < 2).  Default: groups = 8,
+ * tensor_sms = 0 (112 of every 152 SMs).  Calls that take this schedule share
+ * the partitions' streams and run one after another whatever stream they
+ * were given; where the driver offers no partitions, the one-launch schedule
+ * runs.  rkv_compress_noalloc always takes the one-launch schedule.  Returns
+ * RKV_ERR_INVALID_ARG for groups > 32 or 0 < tensor_sms < 8. */
+int rkv_set_overlap(int groups, int tensor_sms);
+
 /* Per-kernel timing (not thread-safe).  While enabled, each launch of the
  * library is bracketed by CUDA events on its stream.  rkv_timing_read waits for
  * the events, writes per-kernel totals (milliseconds) and launch counts for up

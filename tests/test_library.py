@@ -212,6 +212,14 @@ def test_schedule_argument_errors(lib):
     assert call(T=0.0) == 1 and call(T=float("inf")) == 1
 
 
+def test_overlap_setting(lib):
+    """The step schedule setting checks its range and touches no device."""
+    assert lib.rkv_set_overlap(33, 104) == 1  # more groups than the schedule keeps events for
+    assert lib.rkv_set_overlap(4, 4) == 1     # fewer SMs than one partition group
+    assert lib.rkv_set_overlap(0, 104) == 0   # one launch per stage
+    assert lib.rkv_set_overlap(8, 0) == 0     # the default
+
+
 def test_binding_rejects_cpu_tensors(lib):
     from decode_kv_cache_02_gb300 import rkv
     K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)
