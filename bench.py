@@ -44,20 +44,20 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # with the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "importance_tc": ("k_importance_tc.cu", "9bfd3c1bdfb57b7f5e91f4c4d056f95d05bcd45d6cfedcfd56964d7a8790a5ba", (310468352 + 12898304) / 1024),
-        "gram_tc": ("k_gram_tc.cu", "6a17a059df70301d9e6d9c8b93c6b7a3c86d7e6a07a2edaa71413527997b4fea", (317357824 + 9674496) / 1024),
-        "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", (541691648 + 494446592) / 1024),
+        "importance_tc": ("k_importance_tc.cu", "c930a2d3d822ae049b2ad534be29552aa92f21304f30337f29358ec06f8747ec", (310466304 + 12754176) / 1024),
+        "gram_tc": ("k_gram_tc.cu", "a97ab1ebb4b6aa45acd0053a51d1b3e57e5b909e2df783f344f566b853e04f48", (317303808 + 9712640) / 1024),
+        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (541696256 + 493003776) / 1024),
     },
     # the Qwen-14B-shaped step, captured on 768 problems (K 830 MB)
     "qwen14b": {
-        "key_stats": ("k_key_stats.cu", "95b35392fb1c978ea7baa169ce85d537de074573cfd2711b5af30a594ca84177", (830589000 + 31737000) / 768),
-        "importance_tc": ("k_importance_tc.cu", "9bfd3c1bdfb57b7f5e91f4c4d056f95d05bcd45d6cfedcfd56964d7a8790a5ba", (1207313000 + 25321000) / 768),
-        "gram_tc": ("k_gram_tc_pairs.cu", "dab1c4a2a6a9ea890616f2f0e167444f8cf9c095bb971a59f270ebc27c8d7e1e", (3799878000 + 34044000) / 768),
-        "compact": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", (1623769000 + 1577997000) / 768),
+        "key_stats": ("k_key_stats.cu", "95b35392fb1c978ea7baa169ce85d537de074573cfd2711b5af30a594ca84177", (830620000 + 31650000) / 768),
+        "importance_tc": ("k_importance_tc.cu", "c930a2d3d822ae049b2ad534be29552aa92f21304f30337f29358ec06f8747ec", (1211576000 + 25311000) / 768),
+        "gram_tc": ("k_gram_tc_pairs.cu", "ed9472e6e08de81ce281fd4c00809133d27de62737a0af54ed516a6480406460", (3823608000 + 34100000) / 768),
+        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (1623737000 + 1578649000) / 768),
     },
     # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
-        "compact_paged": ("k_compact.cu", "e562cd968326ab9085bd693c3f7c1d83de3fd31394d4baf993ce76839f8e8e0b", 966686464 / 1024),
+        "compact_paged": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (512751616 + 453617152) / 1024),
     },
 }
 
@@ -388,6 +388,52 @@ def _step_fn(w, K, V, Q, out_K, out_V, idx, ws, stream, softmax=False, window=1,
     return step
 
 
+def _busy(intervals):
+    """Union of [start, end) intervals: (total length, merged list)."""
+    merged = []
+    for a, b in sorted(intervals):
+        if merged and a <= merged[-1][1]:
+            merged[-1][1] = max(merged[-1][1], b)
+        else:
+            merged.append([a, b])
+    return sum(b - a for a, b in merged), merged
+
+
+def trace_step(step) -> dict:
+    """One more step with the library's launch trace on (global-timer stamps
+    around every launch, one clock for both SM partitions): each launch's
+    lane and interval, each lane's busy time, and how long the tensor
+    partition (importance, Gram) and the other one (selection + copy) were
+    busy at the same time."""
+    torch.cuda.synchronize()
+    rkv.rkv_trace_enable(True)
+    step()
+    recs = rkv.rkv_trace_read()
+    rkv.rkv_trace_enable(False)
+    if not recs:
+        return {}
+    t0 = min(r[2] for r in recs)
+    span = (max(r[3] for r in recs) - t0) * 1e-6
+    lanes = {}
+    for name, lane, a, b in recs:
+        lanes.setdefault(lane, []).append(((a - t0) * 1e-6, (b - t0) * 1e-6))
+    out = {"span_ms": span, "lanes": {}, "launches": [
+        [name, lane, round((a - t0) * 1e-3, 1), round((b - t0) * 1e-3, 1)]
+        for name, lane, a, b in recs]}
+    names = {0: "caller stream (whole device)", 1: "tensor partition", 2: "hbm partition"}
+    merged = {}
+    for lane, iv in sorted(lanes.items()):
+        busy, merged[lane] = _busy(iv)
+        out["lanes"][names.get(lane, str(lane))] = {"launches": len(iv), "busy_ms": busy}
+    both = 0.0
+    for a, b in merged.get(1, []):
+        for c, d in merged.get(2, []):
+            both += max(0.0, min(b, d) - max(a, c))
+    out["tensor_and_hbm_busy_together_ms"] = both
+    out["launches_columns"] = ["kernel", "lane", "start_us", "end_us"]
+    return out
+
+
 def _time_steps(step, steps, warmup, ws, stream, local, world):
     """W untimed steps, then K steps between CUDA events on the launching
     stream with a barrier and a synchronize on both sides and the clocks
@@ -588,7 +634,7 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     rkv.load()
     if args.schedule == "one-launch":
-        rkv.rkv_set_overlap(0, 0)
+        rkv.rkv_set_overlap(rkv.RKV_SCHEDULE_ONE_LAUNCH)
     K, V, Q = wl.make_inputs(w, device=dev, seed=w.seed + rank)
     out_K = torch.empty_like(K)
     out_V = torch.empty_like(V)
@@ -644,7 +690,7 @@ def run_ours(args, w):
         "groups_per_step": kernels.get("gram_tc", {}).get("launches", 0) // max(1, args.steps)}
     r_elapsed, r_kernels = elapsed, kernels
     if grouped:
-        rkv.rkv_set_overlap(0, 0)
+        rkv.rkv_set_overlap(rkv.RKV_SCHEDULE_ONE_LAUNCH)
         try:
             r_elapsed, r_kernels, _ = _time_steps(step, args.steps, args.warmup, ws, stream,
                                                   local, world)
@@ -654,6 +700,8 @@ def run_ours(args, w):
         line["schedule"]["one_launch_ms_per_step"] = r_elapsed / args.steps
         line["schedule"]["one_launch_kernels_ms_per_step"] = {
             k: v["ms"] / args.steps for k, v in r_kernels.items()}
+    if grouped:
+        line["trace"] = trace_step(step)
     line["roofline"] = roofline(r_kernels, model, peaks, args.steps, w, region_ms=r_elapsed)
     line["roofline"]["schedule"] = "one launch per stage (kernel alone on the whole device)"
     # all kernels' fractions, for the record

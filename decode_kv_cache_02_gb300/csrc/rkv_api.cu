@@ -12,6 +12,7 @@
 // allocate, free or synchronise.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <array>
@@ -78,16 +79,51 @@ cudaEvent_t take_event(const void* ctx) {
     return e;
 }
 
-// Runs `launch` with events around it when timing is on; ctx names the
-// context current meanwhile (a lane's, or nullptr for the caller's).
+// ---------------------------------------------------------------- tracing --
+// A trace stamps the device's global nanosecond timer before and after each
+// launch, on the launch's own stream, with a one-thread kernel: unlike events,
+// the stamps of launches in different contexts (the SM partitions) share one
+// clock, so a trace shows which launches ran at the same time.
+constexpr int kTraceMax = 16384;
+__device__ unsigned long long g_trace_ns[kTraceMax];
+
+__global__ void trace_stamp_kernel(int slot) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    g_trace_ns[slot] = t;
+}
+
+struct TraceRecord {
+    int kernel, lane, slot;  // stamps at slot (start) and slot + 1 (end)
+};
+bool g_trace = false;
+std::vector<TraceRecord> g_trace_recs;
+int g_trace_slots = 0;
+
+// Runs `launch` with events around it when timing is on (and stamps when a
+// trace is on); lane names the SM partition whose context is current
+// meanwhile (nullptr: the caller's context and stream).
 template <typename F>
-cudaError_t timed(int kernel, cudaStream_t s, F&& launch, const void* ctx = nullptr) {
-    if (!g_timing) return launch();
-    TimedLaunch t{kernel, take_event(ctx), take_event(ctx), ctx};
-    cudaEventRecord(t.start, s);
-    cudaError_t e = launch();
-    cudaEventRecord(t.stop, s);
-    g_pending.push_back(t);
+cudaError_t timed(int kernel, cudaStream_t s, F&& launch, const rkv::Lane* lane = nullptr) {
+    const bool stamp = g_trace && g_trace_slots + 2 <= kTraceMax;
+    const int slot = g_trace_slots;
+    if (stamp) {
+        trace_stamp_kernel<<<1, 1, 0, s>>>(slot);
+        g_trace_slots += 2;
+        g_trace_recs.push_back(TraceRecord{kernel, lane ? lane->id : 0, slot});
+    }
+    cudaError_t e;
+    if (!g_timing) {
+        e = launch();
+    } else {
+        const void* ctx = lane ? lane->ctx : nullptr;
+        TimedLaunch t{kernel, take_event(ctx), take_event(ctx), ctx};
+        cudaEventRecord(t.start, s);
+        e = launch();
+        cudaEventRecord(t.stop, s);
+        g_pending.push_back(t);
+    }
+    if (stamp) trace_stamp_kernel<<<1, 1, 0, s>>>(slot + 1);
     return e;
 }
 
@@ -346,7 +382,8 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
 // on the Llama-shaped step (6.54 ms against 6.85 for one launch per stage;
 // 104-116 SMs and 6-9 groups were within 0.2 ms).  tensor_sms 0: the same
 // share of the device's SMs.
-int g_overlap_groups = 8;  // below 2: one launch per stage over all problems
+int g_overlap_mode = RKV_SCHEDULE_AUTO;
+int g_overlap_groups = 8;
 int g_overlap_tensor_sms = 0;
 std::mutex g_overlap_mu;  // one call at a time enqueues on the shared lanes
 
@@ -409,18 +446,50 @@ cudaError_t compact_group(const ScoreArgs& g, int64_t p0, const CompactCall& c, 
                                c.row_bytes, c.in_place, g.status, s);
 }
 
+// Whether the grouped schedule is expected to beat one launch per stage.
+// Per-problem device times measured on GB300 with one launch per stage over
+// the whole device (the Llama-8B shape): importance 4.9e-4 ns per key element
+// (N d), Gram 1.14e-6 ns per N^2 d, compaction 2.9e-4 ns per byte of kept
+// rows (both tensors; in place an upper bound).  Grouping stretches
+// importance and Gram by the device's SMs over the tensor partition's and
+// hides the compaction of every group but the last; each group costs ~28 us
+// of launch ramp and tail, and the step ends with about 1.3 groups'
+// compaction.  Llama-8B step (16,384 problems, N = 1152): +0.31 ms predicted,
+// +0.31 measured; the decode stream's rounds (8,192 problems, N = 1766, in
+// place): -0.2 ms predicted, -0.4 measured, so they keep one launch per stage.
+bool grouped_pays(const ScoreArgs& b, const CompactCall& cc, int tensor_sms, int groups) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= tensor_sms)
+        return false;
+    const double nd = (double)b.N * b.d;
+    const double t_score = 4.9e-4 * nd + 1.14e-6 * nd * b.N;          // ns a problem
+    const double t_compact = 2.9e-4 * (double)cc.budget * cc.row_bytes * 2;
+    const double stretch = (double)sms / tensor_sms - 1.0;
+    const double gain_ns = (double)b.P * (t_compact - stretch * t_score) - groups * 28e3 -
+                           1.3 * t_compact * (double)b.P / groups;
+    return gain_ns > 0.0;
+}
+
 // Returns -1 when the step does not take this schedule (the caller runs the
 // serial one), else an RKV_* code.
 int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s) {
-    if (g_overlap_groups < 2 || g_overlap_groups > kMaxGroups) return -1;
+    if (g_overlap_mode == RKV_SCHEDULE_ONE_LAUNCH) return -1;
     const int tensor_sms = overlap_tensor_sms();
     // at least a few waves of the tensor lane per group, or nothing to gain
     if (tensor_sms < 8 || base.P < 2 * (int64_t)g_overlap_groups * tensor_sms) return -1;
+    if (g_overlap_mode == RKV_SCHEDULE_AUTO && !grouped_pays(base, cc, tensor_sms, g_overlap_groups))
+        return -1;
     ScoreArgs b = base;
     if (!stats_fused(b)) return -1;
     b.fused_stats = true;
-    // a stream being captured into a graph keeps the one-launch schedule
-    // (the lanes' streams belong to other contexts)
+    // under a profiler or other injected tool (ncu cannot profile launches in
+    // a green context) and on a stream being captured into a graph (the
+    // lanes' streams belong to other contexts) the one-launch schedule runs
+    if (getenv("CUDA_INJECTION64_PATH") || getenv("NV_NSIGHT_INJECTION_TRANSPORT_TYPE") ||
+        getenv("NV_COMPUTE_PROFILER_PERFWORKS_DIR"))
+        return -1;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
         return -1;
@@ -431,7 +500,7 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
     const rkv::Lane* H = &L->hbm;
     // Group bounds: equal groups of whole waves of the tensor lane's
     // persistent CTAs, the last one the remainder.  Each group costs the
-    // tensor lane a launch ramp and a tail of its two kernels (~45 us
+    // tensor lane a launch ramp and a tail of its two kernels (~28 us
     // measured on the Llama-shaped step), and the step ends with the hbm
     // lane's compaction of the second-to-last group and the whole device's of
     // the last, so a handful of groups is the balance.
@@ -466,10 +535,10 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
         {
             rkv::LaneScope scope(T);
             e = timed(kImportanceTc, T->stream,
-                      [&] { return rkv::launch_importance_tc(g, T->stream); }, T->ctx);
+                      [&] { return rkv::launch_importance_tc(g, T->stream); }, T);
             if (e == cudaSuccess)
                 e = timed(kGramTc, T->stream, [&] { return rkv::launch_gram_tc(g, T->stream); },
-                          T->ctx);
+                          T);
             if (e == cudaSuccess) e = cudaEventRecord(ev_t.ev[c], T->stream);
         }
         if (e != cudaSuccess || c + 1 == G) break;
@@ -477,7 +546,7 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
         if (e == cudaSuccess) {
             rkv::LaneScope scope(H);
             e = timed(kCompact, H->stream, [&] { return compact_group(g, first(c), cc, H->stream); },
-                      H->ctx);
+                      H);
         }
     }
     if (e == cudaSuccess) {
@@ -1019,12 +1088,44 @@ const char* rkv_strerror(int code) {
     }
 }
 
-int rkv_set_overlap(int groups, int tensor_sms) {
-    if (groups > kMaxGroups || (tensor_sms != 0 && tensor_sms < 8)) return RKV_ERR_INVALID_ARG;
+int rkv_set_overlap(int mode, int groups, int tensor_sms) {
+    if (mode < RKV_SCHEDULE_ONE_LAUNCH || mode > RKV_SCHEDULE_GROUPED || groups < 2 ||
+        groups > kMaxGroups || (tensor_sms != 0 && tensor_sms < 8))
+        return RKV_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_overlap_mu);
+    g_overlap_mode = mode;
     g_overlap_groups = groups;
     g_overlap_tensor_sms = tensor_sms;
     return RKV_OK;
+}
+
+int rkv_trace_enable(int on) {
+    g_trace = on != 0;
+    if (g_trace) {
+        g_trace_recs.clear();
+        g_trace_slots = 0;
+    }
+    return RKV_OK;
+}
+
+int rkv_trace_read(int* kernel, int* lane, uint64_t* start_ns, uint64_t* end_ns, int max_records) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -RKV_ERR_CUDA;
+    const int n = (int)g_trace_recs.size() < max_records ? (int)g_trace_recs.size() : max_records;
+    std::vector<unsigned long long> ns((size_t)g_trace_slots + 1);
+    if (g_trace_slots > 0 &&
+        cudaMemcpyFromSymbol(ns.data(), g_trace_ns, sizeof(unsigned long long) * g_trace_slots) !=
+            cudaSuccess)
+        return -RKV_ERR_CUDA;
+    for (int i = 0; i < n; ++i) {
+        const TraceRecord& r = g_trace_recs[i];
+        if (kernel) kernel[i] = r.kernel;
+        if (lane) lane[i] = r.lane;
+        if (start_ns) start_ns[i] = ns[r.slot];
+        if (end_ns) end_ns[i] = ns[r.slot + 1];
+    }
+    g_trace_recs.clear();
+    g_trace_slots = 0;
+    return n;
 }
 
 int rkv_timing_enable(int on) {

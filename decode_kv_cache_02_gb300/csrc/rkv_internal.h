@@ -79,6 +79,7 @@ struct Lane {
     void* ctx = nullptr;  // the partition's CUcontext
     cudaStream_t stream = nullptr;
     int sms = 0;
+    int id = 0;  // 1: tensor lane, 2: hbm lane (0 is the caller's stream)
 };
 // tensor: the Gram's partition; hbm: the importance and compaction's.
 struct Lanes {

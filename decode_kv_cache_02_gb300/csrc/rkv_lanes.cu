@@ -108,6 +108,8 @@ bool make_lanes(int tensor_sms, Lanes* out) {
     if (want < 1 || want >= n) return false;
     // the tensor lane: the first `want` groups; the other: the remaining
     // groups and the split's remainder
+    out->tensor.id = 1;
+    out->hbm.id = 2;
     if (!make_lane(d, dev, groups, want, &out->tensor)) return false;
     CUdevResource other[kMaxGroups + 1];
     unsigned m = 0;

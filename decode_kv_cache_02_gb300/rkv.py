@@ -29,6 +29,7 @@ EXPORTED = [
     "rkv_score_ex", "rkv_paged_workspace_size", "rkv_paged_freed_per_seq", "rkv_paged_compress",
     "rkv_sentence_reps", "rkv_sentence_penalty", "rkv_selftest_wait_timeout",
     "rkv_noalloc_device_status", "rkv_noalloc_selftest_wait_timeout", "rkv_set_overlap",
+    "rkv_trace_enable", "rkv_trace_read",
 ]
 RKV_MAX_POOL_WINDOW = 255
 RKV_ERR_DEVICE = 6
@@ -196,8 +197,12 @@ def load(path: str | None = None):
         lib.rkv_get_device_status.restype = i32
         lib.rkv_strerror.argtypes = [i32]
         lib.rkv_strerror.restype = ctypes.c_char_p
-        lib.rkv_set_overlap.argtypes = [i32, i32]
+        lib.rkv_set_overlap.argtypes = [i32, i32, i32]
         lib.rkv_set_overlap.restype = i32
+        lib.rkv_trace_enable.argtypes = [i32]
+        lib.rkv_trace_enable.restype = i32
+        lib.rkv_trace_read.argtypes = [vp, vp, vp, vp, i32]
+        lib.rkv_trace_read.restype = i32
         lib.rkv_timing_enable.argtypes = [i32]
         lib.rkv_timing_enable.restype = i32
         lib.rkv_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double),
@@ -442,14 +447,36 @@ def rkv_get_device_status(workspace, stream=None) -> int:
     return int(load().rkv_get_device_status(workspace.data_ptr(), _stream_ptr(stream)))
 
 
-DEFAULT_OVERLAP = (8, 0)  # the library's default step schedule
+RKV_SCHEDULE_ONE_LAUNCH, RKV_SCHEDULE_AUTO, RKV_SCHEDULE_GROUPED = 0, 1, 2
+DEFAULT_OVERLAP = (RKV_SCHEDULE_AUTO, 8, 0)  # the library's default step schedule
 
 
-def rkv_set_overlap(groups: int, tensor_sms: int = 0):
-    """Step schedule of rkv_compress: groups >= 2 scores each group of
-    problems on about tensor_sms SMs (0: 112 of every 152) while the previous
-    group is compacted on the rest; groups < 2 is one launch per stage."""
-    _check(load().rkv_set_overlap(int(groups), int(tensor_sms)), "rkv_set_overlap")
+def rkv_set_overlap(mode: int, groups: int = 8, tensor_sms: int = 0):
+    """Step schedule of rkv_compress: RKV_SCHEDULE_ONE_LAUNCH, _AUTO (grouped
+    where the cost model predicts a gain) or _GROUPED (wherever eligible):
+    groups of problems scored on about tensor_sms SMs (0: 112 of every 152)
+    while the previous group is compacted on the rest."""
+    _check(load().rkv_set_overlap(int(mode), int(groups), int(tensor_sms)), "rkv_set_overlap")
+
+
+def rkv_trace_enable(on: bool = True):
+    load().rkv_trace_enable(1 if on else 0)
+
+
+def rkv_trace_read(max_records: int = 8192) -> list:
+    """[(kernel name, lane, start ns, end ns)] of the traced launches in
+    enqueue order (lane 0: the caller's stream, 1: the tensor partition, 2:
+    the other partition); clears the trace."""
+    lib = load()
+    n = int(max_records)
+    k = (ctypes.c_int * n)()
+    ln = (ctypes.c_int * n)()
+    t0 = (ctypes.c_uint64 * n)()
+    t1 = (ctypes.c_uint64 * n)()
+    m = lib.rkv_trace_read(k, ln, t0, t1, n)
+    if m < 0:
+        raise RkvError(-m, "rkv_trace_read")
+    return [(lib.rkv_kernel_name(k[i]).decode(), ln[i], t0[i], t1[i]) for i in range(m)]
 
 
 def rkv_timing_enable(on: bool = True):

@@ -371,20 +371,50 @@ const char* rkv_strerror(int code);
 /* Step schedule of rkv_compress / rkv_compress_ex (process-wide).  A call
  * whose keys are contiguous bf16 rows with N <= 2048, that passes no variant,
  * whose selection fits the fused compaction and whose stream is not being
- * captured into a graph runs on two SM partitions of the device (driver green
- * contexts, created at the first such call and kept): the problems are cut
- * into `groups` equal groups; importance and Gram of each group run on the
- * tensor partition (about tensor_sms SMs), and each group's selection and
+ * captured into a graph can run on two SM partitions of the device (driver
+ * green contexts, created at the first such call and kept): the problems are
+ * cut into `groups` equal groups; importance and Gram of each group run on
+ * the tensor partition (about tensor_sms SMs), and each group's selection and
  * row copy run on the other SMs while the tensor partition scores the next
  * group (the last group's on the whole device).  It needs at least
  * 2 * groups * tensor_sms problems.  Results are bit for bit those of one
- * launch per stage over the whole device (groups < 2).  Default: groups = 8,
- * tensor_sms = 0 (112 of every 152 SMs).  Calls that take this schedule share
- * the partitions' streams and run one after another whatever stream they
- * were given; where the driver offers no partitions, the one-launch schedule
- * runs.  rkv_compress_noalloc always takes the one-launch schedule.  Returns
- * RKV_ERR_INVALID_ARG for groups > 32 or 0 < tensor_sms < 8. */
-int rkv_set_overlap(int groups, int tensor_sms);
+ * launch per stage over the whole device.
+ *   mode RKV_SCHEDULE_ONE_LAUNCH: always one launch per stage;
+ *   mode RKV_SCHEDULE_AUTO (default): grouped where a cost model of the
+ *     kernels' measured per-problem times predicts a gain (the Llama-8B-shaped
+ *     step: yes; a few thousand problems or long rows compacted in place: no);
+ *   mode RKV_SCHEDULE_GROUPED: grouped wherever the call is eligible.
+ * Defaults: groups = 8, tensor_sms = 0 (112 of every 152 SMs).  Calls that
+ * take the grouped schedule share the partitions' streams and run one after
+ * another whatever stream they were given; where the driver offers no
+ * partitions the one-launch schedule runs, and so it does under a profiler or
+ * other tool injected into the process (CUDA_INJECTION64_PATH, or the
+ * variables Nsight Compute sets: ncu cannot profile launches in a green
+ * context).
+ * rkv_compress_noalloc always takes the one-launch schedule.  Returns
+ * RKV_ERR_INVALID_ARG for an unknown mode, groups outside 2..32 or
+ * 0 < tensor_sms < 8. */
+enum {
+    RKV_SCHEDULE_ONE_LAUNCH = 0,
+    RKV_SCHEDULE_AUTO = 1,
+    RKV_SCHEDULE_GROUPED = 2
+};
+int rkv_set_overlap(int mode, int groups, int tensor_sms);
+
+/* Launch trace (not thread-safe).  While enabled, each launch of the library
+ * is preceded and followed, on its own stream, by a one-thread kernel that
+ * stores the device's global nanosecond timer, so launches on the two SM
+ * partitions of the grouped step (rkv_set_overlap) are placed on one clock.
+ * Enabling clears the trace; up to 8192 launches are kept.  rkv_trace_read
+ * synchronises the device, writes per launch (in enqueue order, up to
+ * max_records) the kernel (index of rkv_kernel_name), the lane (0: the
+ * caller's stream, 1: the tensor partition, 2: the other partition) and the
+ * start and end stamps in ns, clears the trace and returns the number of
+ * records written (a negative RKV_* code on a CUDA error).  Any output
+ * pointer may be null. */
+int rkv_trace_enable(int on);
+int rkv_trace_read(int* kernel, int* lane, uint64_t* start_ns, uint64_t* end_ns,
+                   int max_records);
 
 /* Per-kernel timing (not thread-safe).  While enabled, each launch of the
  * library is bracketed by CUDA events on its stream.  rkv_timing_read waits for

@@ -37,9 +37,9 @@ def test_overlap_matches_one_launch_schedule(cuda_ok, serial_after, groups, tens
     P = 2600  # groups of whole waves of the tensor partition, the last one short
     K, V, Q = wl.make_inputs(w, device="cuda", problems=P)
     b = w.budget
-    rkv.rkv_set_overlap(0, tensor_sms)
+    rkv.rkv_set_overlap(rkv.RKV_SCHEDULE_ONE_LAUNCH, 8, tensor_sms)
     rK, rV, ridx = _compress(K, V, Q, w, in_place)
-    rkv.rkv_set_overlap(groups, tensor_sms)
+    rkv.rkv_set_overlap(rkv.RKV_SCHEDULE_GROUPED, groups, tensor_sms)
     for call in range(2):  # the partitions and their events are reused by the second call
         rkv.rkv_timing_read(reset=True)
         rkv.rkv_timing_enable(True)
@@ -65,3 +65,37 @@ def test_overlap_matches_one_launch_schedule(cuda_ok, serial_after, groups, tens
     assert bad == 0, f"{bad} kept-set mismatches outside the tie band ({excused} excused)"
     parity.check_gathered(oK, K, idx, b, problems)
     parity.check_gathered(oV, V, idx, b, problems)
+
+
+def test_partitions_run_at_the_same_time(cuda_ok, serial_after):
+    """The launch trace (one global timer for both partitions) shows the
+    groups' compactions running while the tensor partition scores the next
+    group, and every launch of the call on its lane."""
+    w = wl.BY_NAME["llama8b_full"]
+    K, V, Q = wl.make_inputs(w, device="cuda", problems=4096)
+    rkv.rkv_set_overlap(rkv.RKV_SCHEDULE_GROUPED, 8, 0)
+    _compress(K, V, Q, w, False)  # partitions created, kernels loaded
+    torch.cuda.synchronize()
+    rkv.rkv_trace_enable(True)
+    _compress(K, V, Q, w, False)
+    recs = rkv.rkv_trace_read()
+    rkv.rkv_trace_enable(False)
+    if not any(lane for _, lane, _, _ in recs):
+        pytest.skip("the driver offers no SM partitions: one launch per stage ran")
+    lanes = {}
+    for name, lane, a, b in recs:
+        assert b > a
+        lanes.setdefault(lane, []).append((name, a, b))
+    assert {n for n, _, _ in lanes[1]} == {"importance_tc", "gram_tc"}
+    assert {n for n, _, _ in lanes[2]} == {"compact"}
+    assert [n for n, _, _ in lanes[0]] == ["compact"]  # the last group, whole device
+    G = len([1 for n, _, _ in lanes[1] if n == "gram_tc"])
+    assert len(lanes[2]) == G - 1
+    # each group's compaction starts after its Gram ends, and at least one
+    # compaction overlaps a later group's scoring
+    grams = [(a, b) for n, a, b in lanes[1] if n == "gram_tc"]
+    comps = [(a, b) for _, a, b in lanes[2]]
+    assert all(c[0] >= g[1] for g, c in zip(grams, comps))
+    scoring = [(a, b) for _, a, b in lanes[1]]
+    overlap = sum(max(0, min(b, d) - max(a, c)) for a, b in scoring for c, d in comps)
+    assert overlap > 0

@@ -214,10 +214,12 @@ def test_schedule_argument_errors(lib):
 
 def test_overlap_setting(lib):
     """The step schedule setting checks its range and touches no device."""
-    assert lib.rkv_set_overlap(33, 104) == 1  # more groups than the schedule keeps events for
-    assert lib.rkv_set_overlap(4, 4) == 1     # fewer SMs than one partition group
-    assert lib.rkv_set_overlap(0, 104) == 0   # one launch per stage
-    assert lib.rkv_set_overlap(8, 0) == 0     # the default
+    assert lib.rkv_set_overlap(1, 33, 104) == 1  # more groups than the schedule keeps events for
+    assert lib.rkv_set_overlap(1, 1, 104) == 1   # one group is not a grouped schedule
+    assert lib.rkv_set_overlap(2, 4, 4) == 1     # fewer SMs than one partition group
+    assert lib.rkv_set_overlap(3, 8, 0) == 1     # no such mode
+    assert lib.rkv_set_overlap(0, 8, 104) == 0   # one launch per stage
+    assert lib.rkv_set_overlap(1, 8, 0) == 0     # the default
 
 
 def test_binding_rejects_cpu_tensors(lib):
