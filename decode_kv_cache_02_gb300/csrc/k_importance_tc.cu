@@ -756,8 +756,10 @@ importance_tcr_kernel(const __grid_constant__ KeyMaps kmap,
                     const int s = kk % C::kStages;
                     if (!(ok = mbar_wait(&k_empty[s], ((kk / C::kStages) & 1) ^ 1, s_abort))) break;
                     mbar_arrive_expect_tx(&k_full[s], C::kBlockBytes);
+                    // with the statistics folded in nothing else reads the
+                    // table before the compaction: check its ids here
                     load_key_rows(sK + s * C::kBlockBytes, kChunkBytes, C::KC, &kmap, &k_full[s], p,
-                                  b * kRows, kRows, prm.ks);
+                                  b * kRows, kRows, prm.ks, 0, kStats ? prm.status : nullptr);
                     ++kk;
                 }
             }

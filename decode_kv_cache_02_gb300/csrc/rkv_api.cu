@@ -319,11 +319,13 @@ ScoreArgs score_args(const rkv_desc* d, const void* K, const void* Q, int n_cach
 }
 
 // Whether the importance kernel takes the key statistics and the Gram
-// completes sum_i (contiguous keys whose rows fit the resident importance
-// kernel and the one-row-block Gram): no pass over K is spent on them.
+// completes sum_i (contiguous keys, or a paged pool the tensor-core stages
+// read in place, whose rows fit the resident importance kernel and the
+// one-row-block Gram): no pass over K is spent on them.
 bool stats_fused(const ScoreArgs& b) {
-    return !b.pg.table && rkv::gram_tc_supported(b) && rkv::importance_tc_supported(b) &&
-           rkv::importance_tc_resident(b) && rkv::gram_tc_rows(b);
+    return (!b.pg.table || b.paged_direct) && rkv::gram_tc_supported(b) &&
+           rkv::importance_tc_supported(b) && rkv::importance_tc_resident(b) &&
+           rkv::gram_tc_rows(b);
 }
 
 int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, int n_obs,
@@ -349,7 +351,9 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
     const bool gram_tc = rkv::gram_tc_supported(b);
     const bool imp_tc = rkv::importance_tc_supported(b);
     a.stats_sum = b.stats_sum = !imp_tc;  // the tensor-core importance completes sum_i itself
-    b.fused_stats = !pg && stats_fused(b);
+    // paged pools read in place (blocks of 128 rows or more) as well: the
+    // importance kernel's loads check the table's ids then
+    b.fused_stats = (!pg || direct) && stats_fused(b);
     cudaError_t e = b.fused_stats ? cudaSuccess
                                   : timed(pg ? kKeyStatsPaged : kKeyStats, s,
                                           [&] { return rkv::launch_key_stats(a, s); });

@@ -111,10 +111,11 @@ struct KeyMaps {
 // invalid ids at an outer coordinate past the pool, which reads as zeros, and
 // the rows past N of the sequence's last block through the tail map, which
 // reads them as zeros as well.
-// policy != 0: every copy carries that L2 cache policy.
+// policy != 0: every copy carries that L2 cache policy.  st != null: an
+// invalid block id the sequence's table names is recorded there.
 RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps* maps,
                            uint64_t* bar, int64_t p, int r0, int rows, const KeySource& ks,
-                           uint64_t policy = 0) {
+                           uint64_t policy = 0, DeviceStatus* st = nullptr) {
     if (ks.table == nullptr) {
         for (int c = 0; c < KC; ++c) {
             if (policy)
@@ -135,6 +136,7 @@ RKV_DEV void load_key_rows(uint8_t* dst, int chunk_bytes, int KC, const KeyMaps*
         if (lb < ks.nb) {
             const int blk = __ldg(row + lb);
             if ((unsigned)blk < (unsigned)ks.num_blocks) z = blk * ks.H + h;
+            else if (st) set_error(st, kDevErrIndex, (unsigned)lb);
         }
         const int y = r & ((1 << ks.log2bs) - 1);
         const CUtensorMap* map = &maps->main + (lb == ks.nb - 1 && ks.tail_rows > 0 ? 1 : 0);

@@ -133,13 +133,17 @@ def test_paged_identity_when_not_over_budget():
     _paged_check(w, 16)
 
 
-def test_paged_bad_block_id_is_reported():
+@pytest.mark.parametrize("bs,d,n,budget,blk", [(16, 64, 301, 200, 3), (128, 128, 600, 300, 3)])
+def test_paged_bad_block_id_is_reported(bs, d, n, budget, blk):
     """A table entry naming no block is caught by the kernels' own checks:
-    its rows are skipped and the device status reports it."""
-    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=301, budget=200, layers=1, batch=2,
-                                           kv_heads=2, head_dim=64)
-    K_pool, V_pool, Q, table = _make_paged(w, 16)
-    table[1, 3] = K_pool.shape[0] + 11
+    its rows are skipped and the device status reports it.  Blocks of 128
+    rows take the path whose importance kernel reads the pool in place with
+    the key statistics folded in (no separate statistics pass); the id is in
+    a block past the budget, which only the scoring reads."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(n_cached=n, budget=budget, layers=1, batch=2,
+                                           kv_heads=2, head_dim=d)
+    K_pool, V_pool, Q, table = _make_paged(w, bs)
+    table[1, blk] = K_pool.shape[0] + 11
     ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs,
                                            w.beta)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
