@@ -44,9 +44,9 @@ METRIC = "KV tokens compressed/sec + steps/sec (1 GB300); % tensor-pipe & % HBM 
 # with the problem count.
 NCU_TRAFFIC = {
     "llama8b_full": {
-        "importance_tc": ("k_importance_tc.cu", "c930a2d3d822ae049b2ad534be29552aa92f21304f30337f29358ec06f8747ec", (310466304 + 12754176) / 1024),
-        "gram_tc": ("k_gram_tc.cu", "a97ab1ebb4b6aa45acd0053a51d1b3e57e5b909e2df783f344f566b853e04f48", (317303808 + 9712640) / 1024),
-        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (541696256 + 493003776) / 1024),
+        "importance_tc": ("k_importance_tc.cu", "9debeb48aa3a2eafc245d0af2bc3979d401067cc8e37bdd45a4a9463acc7082d", (310465536 + 12756480) / 1024),
+        "gram_tc": ("k_gram_tc.cu", "a97ab1ebb4b6aa45acd0053a51d1b3e57e5b909e2df783f344f566b853e04f48", (317408256 + 9883904) / 1024),
+        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (541721600 + 492887808) / 1024),
     },
     # the Qwen-14B-shaped step, captured on 768 problems (K 830 MB)
     "qwen14b": {
@@ -57,7 +57,7 @@ NCU_TRAFFIC = {
     },
     # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
-        "compact_paged": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (512751616 + 453617152) / 1024),
+        "compact_paged": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (512742144 + 453292544) / 1024),
     },
 }
 
