@@ -66,3 +66,14 @@ def test_traffic_lookup_follows_source():
     assert t is None or t > 0
     assert bench.measured_traffic("llama8b_full", "no_such_kernel", 16) is None
     assert bench.measured_traffic("tiny", "gram_tc", 16) is None
+
+
+def test_trace_interval_union():
+    """The trace summary's busy time of a lane is the length of the union of
+    its launches' intervals (overlapping and touching intervals merged)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    busy, merged = bench._busy([(0.0, 1.0), (0.5, 2.0), (3.0, 4.0), (4.0, 4.5), (6.0, 6.0)])
+    assert merged == [[0.0, 2.0], [3.0, 4.5], [6.0, 6.0]]
+    assert busy == pytest.approx(3.5)
+    assert bench._busy([]) == (0, [])
