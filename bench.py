@@ -50,10 +50,10 @@ NCU_TRAFFIC = {
     },
     # the Qwen-14B-shaped step, captured on 768 problems (K 830 MB)
     "qwen14b": {
-        "key_stats": ("k_key_stats.cu", "95b35392fb1c978ea7baa169ce85d537de074573cfd2711b5af30a594ca84177", (830620000 + 31650000) / 768),
-        "importance_tc": ("k_importance_tc.cu", "c930a2d3d822ae049b2ad534be29552aa92f21304f30337f29358ec06f8747ec", (1211576000 + 25311000) / 768),
-        "gram_tc": ("k_gram_tc_pairs.cu", "ed9472e6e08de81ce281fd4c00809133d27de62737a0af54ed516a6480406460", (3823608000 + 34100000) / 768),
-        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (1623737000 + 1578649000) / 768),
+        "key_stats": ("k_key_stats.cu", "95b35392fb1c978ea7baa169ce85d537de074573cfd2711b5af30a594ca84177", (830592000 + 31349000) / 768),
+        "importance_tc": ("k_importance_tc.cu", "9debeb48aa3a2eafc245d0af2bc3979d401067cc8e37bdd45a4a9463acc7082d", (1215002000 + 25443000) / 768),
+        "gram_tc": ("k_gram_tc_pairs.cu", "ed9472e6e08de81ce281fd4c00809133d27de62737a0af54ed516a6480406460", (3823741000 + 34038000) / 768),
+        "compact": ("k_compact.cu", "e1f10483478e846d1525863f92693bb15ce63fdb2c3ec308a1192e61053d2281", (1623967000 + 1578236000) / 768),
     },
     # the paged round (bs 128: the pool read in place, 8 heads per block)
     "llama8b_full_paged": {
