@@ -222,6 +222,15 @@ def test_overlap_setting(lib):
     assert lib.rkv_set_overlap(1, 8, 0) == 0     # the default
 
 
+def test_trace_without_a_device(lib):
+    """The launch trace switches on and off on the host; reading it needs the
+    device and reports a CUDA error where there is none."""
+    assert lib.rkv_trace_enable(1) == 0
+    assert lib.rkv_trace_enable(0) == 0
+    if not __import__("torch").cuda.is_available():
+        assert lib.rkv_trace_read(None, None, None, None, 0) == -5  # -RKV_ERR_CUDA
+
+
 def test_binding_rejects_cpu_tensors(lib):
     from decode_kv_cache_02_gb300 import rkv
     K = torch.zeros(1, 16, 64, dtype=torch.bfloat16)
