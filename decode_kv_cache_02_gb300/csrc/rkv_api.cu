@@ -374,9 +374,10 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
 
 // ---------------------------------------------------------------- overlap --
 // The step on two SM partitions of the device (rkv_lanes.cu).  The importance
-// and the Gram are bound by their SMs (the importance's time grows as the
-// SMs it gets shrink, the Gram's by the tensor pipe), the compaction by HBM,
-// which a part of the SMs already nearly fills.  So the problems are cut into
+// and the Gram are bound by their SMs (the importance's time grows in
+// proportion as the SMs it gets shrink, the Gram's with the tensor pipes it
+// loses), while the compaction, spread over the whole device, is bound by
+// HBM, and on a few SMs moves ~65 GB/s per SM.  So the problems are cut into
 // groups, the tensor lane (most SMs) runs importance and Gram group after
 // group, and the hbm lane (the rest) compacts each group once its Gram is
 // done, while the tensor lane goes on with the next.  The last group's
@@ -384,8 +385,8 @@ int run_scores(const rkv_desc* d, const void* K, const void* Q, int n_cached, in
 // every kernel sees a smaller call of the same shape.
 // Eight groups with 112 of GB300's 152 SMs on the tensor lane measured best
 // on the Llama-shaped step (6.54 ms against 6.85 for one launch per stage;
-// 104-116 SMs and 6-9 groups were within 0.2 ms).  tensor_sms 0: the same
-// share of the device's SMs.
+// 6-9 groups within 0.06 ms; 108 SMs 6.71, 116 SMs 6.9).  tensor_sms 0: the
+// same share of the device's SMs.
 int g_overlap_mode = RKV_SCHEDULE_AUTO;
 int g_overlap_groups = 8;
 int g_overlap_tensor_sms = 0;
