@@ -564,6 +564,20 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
         e = timed(kCompact, s, [&] { return compact_group(g, first(G - 1), cc, s); });
     }
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_h.ev[0], 0);
+    if (e != cudaSuccess) {
+        // whatever was enqueued on the lanes still runs before the caller's
+        // stream goes on (best effort: the call reports the error either way)
+        {
+            rkv::LaneScope scope(T);
+            cudaEventRecord(ev_t.ev[kMaxGroups + 1], T->stream);
+        }
+        {
+            rkv::LaneScope scope(H);
+            cudaEventRecord(ev_h.ev[kMaxGroups + 1], H->stream);
+        }
+        cudaStreamWaitEvent(s, ev_t.ev[kMaxGroups + 1], 0);
+        cudaStreamWaitEvent(s, ev_h.ev[kMaxGroups + 1], 0);
+    }
     return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
 }
 
