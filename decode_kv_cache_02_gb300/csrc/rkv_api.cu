@@ -420,7 +420,10 @@ bool lane_events(const rkv::Lane* lane, LaneEvents* le) {
 ScoreArgs group_args(const ScoreArgs& b, int64_t p0, int64_t n) {
     ScoreArgs c = b;
     const int64_t es = 2;  // the fused path is bf16 only
-    c.K = static_cast<const char*>(b.K) + p0 * b.n_cap * b.d * es;
+    if (b.pg.table)  // a paged pool: the group's sequences' rows of the table (p0 % H == 0)
+        c.pg.table = b.pg.table + (p0 / b.pg.H) * b.pg.max_blocks;
+    else
+        c.K = static_cast<const char*>(b.K) + p0 * b.n_cap * b.d * es;
     c.Q = static_cast<const char*>(b.Q) + p0 * b.G * b.n_obs * b.d * es;
     c.P = n;
     c.inv_norm += p0 * b.ld_ws;
@@ -438,10 +441,16 @@ struct CompactCall {
     const void *K, *V;
     void *out_K, *out_V;
     int32_t* out_idx;
+    // a paged pool (K, V the pools, compacted in place through g.pg)
+    bool paged = false;
 };
 
 cudaError_t compact_group(const ScoreArgs& g, int64_t p0, const CompactCall& c, cudaStream_t s) {
     const int64_t rb = c.row_bytes;
+    if (c.paged)
+        return rkv::launch_compact_paged(g.P, c.n_cached, g.Z, g.ld_out, c.tail, c.budget,
+                                         c.out_idx + p0 * c.budget, nullptr, c.out_K, c.out_V,
+                                         g.pg, c.row_bytes, g.status, s);
     return rkv::launch_compact(g.P, c.n_cached, g.Z, g.ld_out, c.tail, c.budget,
                                c.out_idx + p0 * c.budget,
                                static_cast<const char*>(c.K) + p0 * c.n_cap * rb,
@@ -484,7 +493,12 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
     const int tensor_sms = overlap_tensor_sms();
     // at least a few waves of the tensor lane per group, or nothing to gain
     if (tensor_sms < 8 || base.P < 2 * (int64_t)g_overlap_groups * tensor_sms) return -1;
-    if (g_overlap_mode == RKV_SCHEDULE_AUTO && !grouped_pays(base, cc, tensor_sms, g_overlap_groups))
+    // automatic: the cost model's call; never for paged pools, whose
+    // compaction (a register copy through the table, in place) is too slow on
+    // the small partition (the 128-row-block paged round: 9.5 ms grouped
+    // against 7.1 ms one launch per stage)
+    if (g_overlap_mode == RKV_SCHEDULE_AUTO &&
+        (cc.paged || !grouped_pays(base, cc, tensor_sms, g_overlap_groups)))
         return -1;
     ScoreArgs b = base;
     if (!stats_fused(b)) return -1;
@@ -509,9 +523,12 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
     // measured on the Llama-shaped step), and the step ends with the hbm
     // lane's compaction of the second-to-last group and the whole device's of
     // the last, so a handful of groups is the balance.
+    // (paged: whole sequences, so that a group is a block of the table's rows)
     const int64_t wave = T->sms;
+    const int64_t unit = b.pg.table ? b.pg.H : 1;
     int64_t per = (b.P + g_overlap_groups - 1) / g_overlap_groups;
     per = (per + wave - 1) / wave * wave;
+    per = (per + unit - 1) / unit * unit;
     int64_t bounds[kMaxGroups + 1];
     int G = 0;
     bounds[0] = 0;
@@ -550,7 +567,8 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
         e = cudaStreamWaitEvent(H->stream, ev_t.ev[c], 0);
         if (e == cudaSuccess) {
             rkv::LaneScope scope(H);
-            e = timed(kCompact, H->stream, [&] { return compact_group(g, first(c), cc, H->stream); },
+            e = timed(cc.paged ? kCompactPaged : kCompact, H->stream,
+                      [&] { return compact_group(g, first(c), cc, H->stream); },
                       H);
         }
     }
@@ -561,7 +579,8 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_t.ev[G - 1], 0);
     if (e == cudaSuccess) {
         const ScoreArgs g = group(G - 1);
-        e = timed(kCompact, s, [&] { return compact_group(g, first(G - 1), cc, s); });
+        e = timed(cc.paged ? kCompactPaged : kCompact, s,
+                  [&] { return compact_group(g, first(G - 1), cc, s); });
     }
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev_h.ev[0], 0);
     if (e != cudaSuccess) {
@@ -972,13 +991,38 @@ int rkv_paged_compress(const rkv_paged_desc* desc, void* K_pool, void* V_pool,
     pg.log2bs = log2_exact(desc->block_size);
     pg.H = desc->num_kv_heads;
     pg.num_blocks = desc->num_blocks;
+    const int row_bytes = desc->head_dim * (int)es;
+    if (direct && !vf.any()) {
+        // the two-partition schedule, where the round takes it (pools read in
+        // place; the kept rows move inside their blocks, group by group)
+        ScoreArgs a = score_args(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
+                                 nullptr, w.Z, w.ld, w);
+        a.pg = pg;
+        a.paged_direct = true;
+        CompactCall cc{n_cached, tail, budget, flat.n_capacity, flat.n_capacity, row_bytes, true,
+                       K_pool, V_pool, K_pool, V_pool, out_idx};
+        cc.paged = true;
+        rc = run_overlapped(a, cc, s);
+        if (rc > 0) return rc;
+        if (rc == RKV_OK) {
+            cudaError_t e = cudaSuccess;
+            if (n_free > 0)
+                e = timed(kPagedRelease, s, [&] {
+                    return rkv::launch_paged_release(desc->num_seqs, block_table,
+                                                     desc->max_blocks_per_seq,
+                                                     blocks_for(budget, desc->block_size),
+                                                     blocks_for(n_cached, desc->block_size),
+                                                     out_freed, s);
+                });
+            return e == cudaSuccess ? RKV_OK : RKV_ERR_CUDA;
+        }
+    }
     if (vf.zvar && launch_penalty(variant, s) != cudaSuccess) return RKV_ERR_CUDA;
     rc = run_scores(&flat, K_pool, Q_obs, n_cached, n_obs, lambda, beta, tau, w.I,
                     vf.zvar ? w.R : nullptr, w.Z, w.ld, w, s, &pg, direct);
     if (rc) return rc;
     rkv::VariantIn vin;
     if (vf.any()) vin = variant_in(*variant, vf, lambda, w, samples(variant, n_cached, budget));
-    const int row_bytes = desc->head_dim * (int)es;
     cudaError_t e = timed(kCompactPaged, s, [&] {
         return rkv::launch_compact_paged(P, n_cached, w.Z, w.ld, tail, budget, out_idx,
                                          direct ? nullptr : w.Kc,

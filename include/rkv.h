@@ -368,21 +368,24 @@ int rkv_selftest_wait_timeout(void* workspace, void* stream);
 /* Human-readable name of an RKV_* code. */
 const char* rkv_strerror(int code);
 
-/* Step schedule of rkv_compress / rkv_compress_ex (process-wide).  A call
- * whose keys are contiguous bf16 rows with N <= 2048, that passes no variant,
- * whose selection fits the fused compaction and whose stream is not being
- * captured into a graph can run on two SM partitions of the device (driver
- * green contexts, created at the first such call and kept): the problems are
- * cut into `groups` equal groups; importance and Gram of each group run on
- * the tensor partition (about tensor_sms SMs), and each group's selection and
- * row copy run on the other SMs while the tensor partition scores the next
- * group (the last group's on the whole device).  It needs at least
+/* Step schedule of rkv_compress / rkv_compress_ex / rkv_paged_compress
+ * (process-wide).  A call whose keys are bf16 rows with N <= 2048 (contiguous,
+ * or a paged pool of blocks of 128 rows or more, grouped by whole sequences),
+ * that passes no variant, whose selection fits the fused compaction and whose
+ * stream is not being captured into a graph can run on two SM partitions of
+ * the device (driver green contexts, created at the first such call and
+ * kept): the problems are cut into `groups` equal groups; importance and Gram
+ * of each group run on the tensor partition (about tensor_sms SMs), and each
+ * group's selection and row copy run on the other SMs while the tensor
+ * partition scores the next group (the last group's on the whole device).
+ * It needs at least
  * 2 * groups * tensor_sms problems.  Results are bit for bit those of one
  * launch per stage over the whole device.
  *   mode RKV_SCHEDULE_ONE_LAUNCH: always one launch per stage;
  *   mode RKV_SCHEDULE_AUTO (default): grouped where a cost model of the
  *     kernels' measured per-problem times predicts a gain (the Llama-8B-shaped
- *     step: yes; a few thousand problems or long rows compacted in place: no);
+ *     step: yes; a few thousand problems or long rows compacted in place: no;
+ *     paged pools: never);
  *   mode RKV_SCHEDULE_GROUPED: grouped wherever the call is eligible.
  * Defaults: groups = 8, tensor_sms = 0 (112 of every 152 SMs).  Calls that
  * take the grouped schedule share the partitions' streams and run one after

@@ -151,3 +151,37 @@ def test_paged_bad_block_id_is_reported(bs, d, n, budget, blk):
                            workspace=ws)
     assert rkv.rkv_get_device_status(ws) == rkv.RKV_ERR_DEVICE
     assert rkv.rkv_get_device_status(ws) == 0  # read and cleared
+
+
+def test_paged_grouped_schedule_matches_one_launch():
+    """The grouped step schedule on a pool read in place (blocks of 128 rows):
+    groups of whole sequences scored on one SM partition while the previous
+    group's kept rows move inside their blocks on the other.  Pools, table,
+    kept indices and freed blocks must equal those of one launch per stage,
+    and the oracle's on a few sequences."""
+    w = wl.BY_NAME["llama8b_layer"].scaled(layers=1, batch=160, kv_heads=8)  # 1,280 problems
+    results = []
+    for mode in (rkv.RKV_SCHEDULE_ONE_LAUNCH, rkv.RKV_SCHEDULE_GROUPED):
+        K_pool, V_pool, Q, table = _make_paged(w, 128)
+        ws_bytes = rkv.rkv_paged_workspace_size(K_pool, table, w.gqa, w.n_cached, w.n_obs,
+                                               w.beta)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+        rkv.rkv_set_overlap(mode, 3, 104)
+        try:
+            rkv.rkv_timing_read(reset=True)
+            rkv.rkv_timing_enable(True)
+            idx, freed = rkv.rkv_paged_compress(K_pool, V_pool, Q, table, w.n_cached, w.budget,
+                                                w.n_obs, w.lam, w.beta, w.tau, workspace=ws)
+            rkv.rkv_timing_enable(False)
+            torch.cuda.synchronize()
+            launches = rkv.rkv_timing_read(reset=True)
+        finally:
+            rkv.rkv_set_overlap(*rkv.DEFAULT_OVERLAP)
+        assert rkv.rkv_get_device_status(ws) == 0
+        if mode == rkv.RKV_SCHEDULE_GROUPED and launches["gram_tc"][1] == 1:
+            pytest.skip("the driver offers no SM partitions: one launch per stage ran")
+        results.append((_raw(K_pool), _raw(V_pool), table.cpu().numpy(), idx.cpu().numpy(),
+                        freed.cpu().numpy()))
+    assert launches["gram_tc"][1] == launches["compact_paged"][1] == 3
+    for a, b in zip(results[0], results[1]):
+        np.testing.assert_array_equal(a, b)
