@@ -391,6 +391,7 @@ int g_overlap_mode = RKV_SCHEDULE_AUTO;
 int g_overlap_groups = 8;
 int g_overlap_tensor_sms = 0;
 std::mutex g_overlap_mu;  // one call at a time enqueues on the shared lanes
+bool g_lanes_refused = false;  // a partition refused the first launch of a call
 
 int overlap_tensor_sms() {
     if (g_overlap_tensor_sms > 0) return g_overlap_tensor_sms;
@@ -489,7 +490,7 @@ bool grouped_pays(const ScoreArgs& b, const CompactCall& cc, int tensor_sms, int
 // Returns -1 when the step does not take this schedule (the caller runs the
 // serial one), else an RKV_* code.
 int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s) {
-    if (g_overlap_mode == RKV_SCHEDULE_ONE_LAUNCH) return -1;
+    if (g_overlap_mode == RKV_SCHEDULE_ONE_LAUNCH || g_lanes_refused) return -1;
     const int tensor_sms = overlap_tensor_sms();
     // at least a few waves of the tensor lane per group, or nothing to gain
     if (tensor_sms < 8 || base.P < 2 * (int64_t)g_overlap_groups * tensor_sms) return -1;
@@ -558,6 +559,13 @@ int run_overlapped(const ScoreArgs& base, const CompactCall& cc, cudaStream_t s)
             rkv::LaneScope scope(T);
             e = timed(kImportanceTc, T->stream,
                       [&] { return rkv::launch_importance_tc(g, T->stream); }, T);
+            if (c == 0 && e != cudaSuccess) {
+                // the partition refused the call's first launch (its error is
+                // cleared by the launcher): nothing of the call has run, so
+                // one launch per stage takes this call and every later one
+                g_lanes_refused = true;
+                return -1;
+            }
             if (e == cudaSuccess)
                 e = timed(kGramTc, T->stream, [&] { return rkv::launch_gram_tc(g, T->stream); },
                           T);
